@@ -1,0 +1,501 @@
+"""Benchmark of the MoE permute / unpermute path on GB300.
+
+One step = the whole routed path on one batch of the skewed dispatch workload
+(T=16384 tokens, H=4096 bf16, E=128 experts, K=8, Zipf(1.2)-biased router):
+
+    mp_build_map -> mp_permute (+probs) -> mp_unpermute (probs)      forward
+    mp_unpermute_bwd (probs, grad probs) -> mp_permute_bwd           backward
+
+with the identity as the expert in between (the unpermute reads the permuted
+rows; the permute backward reads the unpermute backward's row gradients).
+
+`value` is algorithmic bytes per step / device time per step, in GB/s
+(1 GB = 1e9 B), inputs resident in HBM, L2 flushed between steps.  Byte
+accounting: every input row read once, every output row written once, maps
+and probabilities once.  `e2e` is the same metric through the same calls with
+the inputs copied from pinned host memory and the results copied back inside
+the timed region.  The JSON line also carries the per-op times, the roofline
+of the dominant kernel, the chunk sort+pad roundtrip (8,192 and 32,768 rows,
+H=2048, 16 experts x 8 rank chunks, align 128) and the oracle timed on the
+host cores (`cpu_baseline`).
+
+`--impl reference` times the oracle (plain C on the CPU) on a bounded sample
+of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "skewed"
+METRIC = ("permute+unpermute GB/s and % of GB300 HBM peak; tokens/s at "
+          "T=16K,H=4096,K=8")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture, keyed by op; valid only while the kernel source that was
+# profiled is unchanged (sha256 prefix of the .cu file).
+NCU_TRAFFIC = {}
+
+
+# --------------------------------------------------------------------------
+# byte accounting (per call)
+# --------------------------------------------------------------------------
+
+def routed_bytes(T, H, K, E, routed):
+    """Algorithmic bytes of each op for T tokens, K slots, `routed` routed slots."""
+    R, row = routed, 2 * H
+    tok = T * row
+    return {
+        "build_map": 4 * T * K + 4 * T * K + 4 * T * K + 4 * E + 4 * (E + 1),
+        "permute": tok + 4 * T * K + 4 * T * K + R * row + 4 * R,
+        "unpermute": R * row + 4 * T * K + 4 * T * K + tok,
+        "unpermute_bwd": tok + R * row + 4 * T * K + 4 * T * K + R * row + 4 * T * K,
+        "permute_bwd": R * row + 4 * T * K + tok,
+    }
+
+
+def chunk_bytes(N, H, padded_total, out_rows):
+    row = 2 * H + 4                      # bf16 row + fp32 prob
+    return {
+        "sort_chunks_pad": N * row + out_rows * row + out_rows * 4 + 8 * 17,
+        "unpad_restore": out_rows * 4 + N * row + N * row,
+    }
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def src_hash(name):
+    path = os.path.join(ROOT, "unpermute_routing_indices_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self, t0, t1):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "samples": 0}
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3])
+                          if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and --impl reference)
+# --------------------------------------------------------------------------
+
+def oracle_step_rate(seconds: float, sample_tokens: int = 256):
+    """Runs the oracle's version of one step on the first `sample_tokens`
+    tokens of the workload until `seconds` have passed; returns GB/s."""
+    import oracle
+    from unpermute_routing_indices_gb300 import workloads as wl
+
+    w = wl.routed(WORKLOAD, T=sample_tokens)
+    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+    it, t0 = 0, time.perf_counter()
+    nbytes = 0
+    while True:
+        rim, s2f, counts, offsets, _ = oracle.build_map(w["idx"], E)
+        routed = int(offsets[-1])
+        rows, rows_p = oracle.permute(w["x"], w["probs"], rim)
+        y = oracle.unpermute(rows, w["probs"], rim, T, H)
+        g_rows, g_probs = oracle.unpermute_bwd(w["g_y"], rows, w["probs"], rim)
+        g_x, _ = oracle.permute_bwd(g_rows, None, rim, T, H)
+        nbytes += sum(routed_bytes(T, H, K, E, routed).values())
+        it += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    sample = (f"{sample_tokens} tokens of the skewed workload (T={sample_tokens}, H={H}, "
+              f"E={E}, K={K}), whole fwd+bwd step, {it} steps in {dt:.1f} s")
+    return nbytes / dt / 1e9, it, dt, sample
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import unpermute_routing_indices_gb300 as mp
+    from unpermute_routing_indices_gb300 import workloads as wl
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- routed workload: per-rank batch (weak scaling), seeded per rank
+    base_seed = wl.ROUTED[WORKLOAD]["seed"] + 7919 * rank
+    w = wl.routed(WORKLOAD, seed=base_seed)
+    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+    R = T * K
+
+    def dev_t(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.to(dev)
+
+    idx, probs, x, gy = dev_t(w["idx"]), dev_t(w["probs"]), dev_t(w["x"]), dev_t(w["g_y"])
+    rim = torch.empty((T, K), dtype=torch.int32, device=dev)
+    s2f = torch.empty(R, dtype=torch.int32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    ws = torch.empty(mp.mp_build_map_workspace_size(T, K, E), dtype=torch.uint8, device=dev)
+    rows = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    rows_p = torch.empty(R, dtype=torch.float32, device=dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    g_rows = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    g_probs = torch.empty((T, K), dtype=torch.float32, device=dev)
+    g_x = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    ops = ["build_map", "permute", "unpermute", "unpermute_bwd", "permute_bwd"]
+    launches = {"build_map": 3, "permute": 1, "unpermute": 1, "unpermute_bwd": 1,
+                "permute_bwd": 1}
+
+    def call(op):
+        if op == "build_map":
+            mp.mp_build_map(idx, E, row_id_map=rim, sorted_to_flat=s2f, counts=counts,
+                            offsets=offsets, workspace=ws)
+        elif op == "permute":
+            mp.mp_permute(x, rim, probs, out=rows, out_probs=rows_p)
+        elif op == "unpermute":
+            mp.mp_unpermute(rows, rim, probs, out=y)
+        elif op == "unpermute_bwd":
+            mp.mp_unpermute_bwd(gy, rim, rows, probs, g_rows=g_rows, g_probs=g_probs)
+        elif op == "permute_bwd":
+            mp.mp_permute_bwd(g_rows, rim, g_x=g_x)
+
+    stream = torch.cuda.current_stream(dev)
+    nev = len(ops) + 1
+
+    def timed_steps(n, record):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n)]
+        for i in range(n):
+            flush.fill_(float(i))                       # L2 flush between steps
+            evs[i][0].record(stream)
+            for j, op in enumerate(ops):
+                call(op)
+                evs[i][j + 1].record(stream)
+        return evs
+
+    for _ in range(args.warmup):
+        timed_steps(1, False)
+    torch.cuda.synchronize()
+    routed = int(offsets[-1].item())
+    nbytes = routed_bytes(T, H, K, E, routed)
+    step_bytes = sum(nbytes.values())
+
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.time()
+        evs = timed_steps(args.steps, True)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier()
+    clocks = clk.summary(t0, t1)
+
+    per_op = {op: 0.0 for op in ops}
+    step_ms = []
+    for e in evs:
+        step_ms.append(e[0].elapsed_time(e[-1]))
+        for j, op in enumerate(ops):
+            per_op[op] += e[j].elapsed_time(e[j + 1])
+    ms = sum(step_ms) / len(step_ms)
+    per_op = {op: v / args.steps for op, v in per_op.items()}
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    peak, peak_kind = measured_peaks()
+    gbs = world * step_bytes / (ms * 1e-3) / 1e9
+    dom = max(ops, key=lambda o: per_op[o])
+    dom_src = {"build_map": "map.cu"}.get(dom, "rows.cu")
+    traffic = None
+    tr = NCU_TRAFFIC.get(dom)
+    if tr is not None and tr["src"] == src_hash(dom_src):
+        traffic = tr["bytes"]
+    achieved = nbytes[dom] / (per_op[dom] * 1e-3) / 1e9
+
+    # ---- e2e through host buffers (pinned), same calls
+    h_in = {k: torch.from_numpy(np.ascontiguousarray(w[k])).pin_memory()
+            for k in ("idx", "probs", "x", "g_y")}
+    h_out = {"y": torch.empty((T, H), dtype=torch.int16).pin_memory(),
+             "g_x": torch.empty((T, H), dtype=torch.int16).pin_memory(),
+             "g_probs": torch.empty((T, K), dtype=torch.float32).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        idx.copy_(h_in["idx"], non_blocking=True)
+        probs.copy_(h_in["probs"], non_blocking=True)
+        x.view(torch.int16).copy_(h_in["x"].view(torch.int16), non_blocking=True)
+        gy.view(torch.int16).copy_(h_in["g_y"].view(torch.int16), non_blocking=True)
+        for op in ops:
+            call(op)
+        h_out["y"].copy_(y.view(torch.int16), non_blocking=True)
+        h_out["g_x"].copy_(g_x.view(torch.int16), non_blocking=True)
+        h_out["g_probs"].copy_(g_probs, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    barrier()
+
+    # ---- chunk sort+pad roundtrip (context: the pages' only published timing)
+    sort_pad = {}
+    if rank == 0 and not args.no_chunks:
+        sort_pad = bench_chunks(mp, wl, dev, flush, args)
+
+    out = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy; router logits N(0,1) + 2 ln Zipf(1.2) bias)",
+        "config": {"workload": f"{WORKLOAD} dispatch T={T} H={H} E={E} K={K}, fwd+bwd step",
+                   "T": T, "H": H, "E": E, "K": K, "routed_rows": routed,
+                   "bytes_per_step": step_bytes,
+                   "l2": "flushed between steps (fill of a 2xL2 buffer, outside the events)",
+                   "parallelism": f"dp{world} (independent token batches, no collective)"},
+        "pct_of_nominal_peak": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_peak": round(100 * gbs / world / peak, 2),
+        "tokens_per_s": round(world * T / (ms * 1e-3), 1),
+        "ops": {op: {"us": round(per_op[op] * 1e3, 2), "bytes": nbytes[op],
+                     "GB/s": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9, 1),
+                     "frac_of_measured": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9 / peak, 4)}
+                for op in ops},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": nbytes[dom]},
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": sum(launches.values()) * args.steps,
+        "clocks": clocks,
+    }
+    if sort_pad:
+        out["sort_pad_roundtrip"] = sort_pad
+    if rank == 0 and not args.no_cpu:
+        v, it, dt, sample = oracle_step_rate(args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": 1,
+                               "kind": "oracle", "sample": sample}
+    if world > 1:
+        dist.destroy_process_group()
+    return out if rank == 0 else None
+
+
+def bench_chunks(mp, wl, dev, flush, args):
+    import torch
+
+    res = {}
+    stream = torch.cuda.current_stream(dev)
+    for N in (8192, 32768):
+        c = wl.chunks(N)
+        G, align, H = c["G"], c["align"], c["H"]
+        out_rows = wl.padded_rows_bound(N, G, align)
+
+        def t(a):
+            tt = torch.from_numpy(np.ascontiguousarray(a))
+            if a.dtype == np.uint16:
+                tt = tt.view(torch.int16).view(torch.bfloat16)
+            return tt.to(dev)
+
+        x, p, sz, od = t(c["x"]), t(c["probs"]), t(c["split_sizes"]), t(c["chunk_order"])
+        out = torch.empty((out_rows, H), dtype=torch.bfloat16, device=dev)
+        out_p = torch.empty(out_rows, dtype=torch.float32, device=dev)
+        row_map = torch.empty(out_rows, dtype=torch.int32, device=dev)
+        goff = torch.empty(G + 1, dtype=torch.int64, device=dev)
+        y = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        y_p = torch.empty(N, dtype=torch.float32, device=dev)
+
+        def roundtrip():
+            mp.mp_sort_chunks_pad(x, sz, od, G, align, out_rows, p, out=out, out_probs=out_p,
+                                  row_map=row_map, group_off=goff)
+            mp.mp_unpad_restore(out, row_map, N, out_p, y=y, y_probs=y_p)
+
+        for _ in range(5):
+            roundtrip()
+        n = max(50, min(args.steps, 200))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for e in evs:
+            flush.fill_(1.0)
+            e[0].record(stream)
+            mp.mp_sort_chunks_pad(x, sz, od, G, align, out_rows, p, out=out, out_probs=out_p,
+                                  row_map=row_map, group_off=goff)
+            e[1].record(stream)
+            mp.mp_unpad_restore(out, row_map, N, out_p, y=y, y_probs=y_p)
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        sp = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+        ur = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+        rt = statistics.median(e[0].elapsed_time(e[2]) for e in evs)
+        padded = int(goff[-1].item())
+        b = chunk_bytes(N, H, padded, out_rows)
+        res[str(N)] = {"roundtrip_ms": round(rt, 4), "sort_pad_us": round(sp * 1e3, 2),
+                       "unpad_restore_us": round(ur * 1e3, 2),
+                       "roundtrip_GB/s": round((b["sort_chunks_pad"] + b["unpad_restore"])
+                                               / (rt * 1e-3) / 1e9, 1),
+                       "out_rows": out_rows, "padded_rows": padded,
+                       "published_b200_fused_ms": {8192: 0.1717, 32768: 0.2029}[N]}
+    return res
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    from unpermute_routing_indices_gb300 import workloads as wl
+
+    cfg = wl.ROUTED[WORKLOAD]
+    T, H, E, K = cfg["T"], cfg["H"], cfg["E"], cfg["K"]
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_step_rate(per_step)
+    vals, secs = [], 0.0
+    sample = ""
+    for _ in range(args.steps):
+        v, it, dt, sample = oracle_step_rate(per_step)
+        vals.append(v)
+        secs += dt
+    v = statistics.mean(vals)
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / max(1, args.steps), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded numpy)",
+            "config": {"workload": f"{WORKLOAD} dispatch T={T} H={H} E={E} K={K}, fwd+bwd step",
+                       "T": T, "H": H, "E": E, "K": K},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-chunks", action="store_true", help="skip the sort+pad roundtrip")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

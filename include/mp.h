@@ -1,0 +1,234 @@
+/*
+ * mp.h -- C ABI of libmp: Mixture-of-Experts token permute / unpermute on one
+ * GB300 GPU (sm_103a).
+ *
+ * The operations and their sources (web pages, cited by title and section):
+ *   [d9d]   "d9d 0.1.0 -- d9d/kernel/moe/permute_with_probs.py", a copy of
+ *           TransformerEngine permutation.py: make_row_id_map (and its worked
+ *           example), _permute_kernel, _unpermute_kernel,
+ *           _unpermute_bwd_with_merging_probs_kernel, and the autograd classes
+ *           _moe_permute_mask_map / _moe_unpermute_mask_map.
+ *   [MBI]   "core.transformer.moe.batch_invariant" (Megatron-Core API docs):
+ *           _rank_tree_unpermute_kernel, _rank_tree_unpermute_bwd_kernel,
+ *           _unpermute_loop, unpermute.
+ *   [xt]    "permute different with torch version" (xtuner issue 1323).
+ *   [mops]  "moe-ops 0.1.0" README: "Why this library", "Layout conventions",
+ *           "Operators" (permute / unpermute / permute_backward).
+ *   [TE-PR] "[PyTorch] Fuse MoE chunk sorting and padding"
+ *           (TransformerEngine PR 3509): Description, Changes, Diagram.
+ *
+ * Common rules for every entry point
+ * ----------------------------------
+ *  - Pointers marked "device" are CUDA device (or managed) pointers; the
+ *    caller owns every buffer.  The library never allocates, never frees and
+ *    never synchronises: each call enqueues kernels on `stream` (a
+ *    cudaStream_t passed as void*; NULL is the legacy default stream) and
+ *    returns.  Grids depend on the shape arguments only, so a call can be
+ *    captured in a CUDA graph and replayed with new routing in the same
+ *    buffers.
+ *  - Tensors are dense and row-major.  bf16 tensors are passed as their
+ *    16-bit patterns (mp_bf16_t).  A row of H bf16 values is 2*H bytes.
+ *    Rows move as 16-byte vectors when H % 8 == 0 and every row pointer is
+ *    16-byte aligned, else element by element; results are identical.
+ *  - Routes: T tokens, K slots per token, R = T*K <= 2^31 - 1.
+ *    E <= MP_MAX_EXPERTS.
+ *  - Errors found on the host (a NULL required pointer, a negative or
+ *    out-of-range size, a too-small workspace) return a negative mp_status_t
+ *    and launch nothing.  A failing launch returns MP_ERR_CUDA;
+ *    mp_last_cuda_error() then gives the cudaError_t of the calling thread.
+ *  - Errors in the data (an expert index outside [-1,E), bad chunk sizes) are
+ *    never fatal: the offending entry is treated as empty, and, if
+ *    `dev_status` is not NULL, the kernel ORs an MP_STATUS_* bit into the
+ *    device word *dev_status (which the caller zeroes beforehand and reads
+ *    when it likes).
+ *  - Empty inputs (T == 0 or N == 0) are valid: nothing is copied.
+ */
+#ifndef MP_H
+#define MP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t mp_status_t;
+typedef uint16_t mp_bf16_t;   /* bit pattern of a bfloat16 value            */
+typedef void *mp_stream_t;    /* a cudaStream_t                             */
+
+#define MP_OK 0
+#define MP_ERR_INVALID_ARG (-1) /* bad pointer or size: nothing launched     */
+#define MP_ERR_WORKSPACE (-2)   /* workspace NULL, misaligned or too small   */
+#define MP_ERR_UNSUPPORTED (-3) /* size beyond a documented limit            */
+#define MP_ERR_CUDA (-4)        /* a launch failed (see mp_last_cuda_error)  */
+
+/* Bits ORed into *dev_status by the kernels. */
+#define MP_STATUS_BAD_EXPERT 0x1     /* idx value outside [-1,E): taken as -1   */
+#define MP_STATUS_BAD_SPLIT 0x2      /* split_sizes[c] < 0: taken as 0          */
+#define MP_STATUS_BAD_ORDER 0x4      /* chunk_order entry outside [0,C): skipped */
+#define MP_STATUS_SPLIT_OVERFLOW 0x8 /* sum of split sizes > N: rows >= N unread */
+#define MP_STATUS_ROWS_OVERFLOW 0x10 /* padded total > out_rows: excess dropped  */
+#define MP_STATUS_BAD_ROW 0x20       /* row_map entry outside [-1,N): skipped    */
+
+#define MP_MAX_EXPERTS 1024
+#define MP_MAX_CHUNKS 1024
+
+/* Text for a status code (static storage). */
+const char *mp_status_string(mp_status_t status);
+
+/* cudaError_t of the last MP_ERR_CUDA returned on the calling thread. */
+int32_t mp_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------ */
+/* Routing map  [d9d make_row_id_map; mops "Operators: permute"; xt]         */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace mp_build_map needs for these sizes (a multiple
+ * of 256; 0 never).  Returns 0 for invalid sizes. */
+size_t mp_build_map_workspace_size(int64_t T, int32_t K, int32_t E);
+
+/*
+ * Counting sort of the routes by expert: histogram, exclusive scan, stable
+ * rank.  Rows are ordered by expert, then token, then slot.
+ *   idx            device int32 [T,K]  expert of slot k of token t; -1 = empty
+ *                                      slot (no row).
+ *   row_id_map     device int32 [T,K]  out: row of (t,k) in the permuted
+ *                                      tensor, -1 for an empty slot.
+ *   sorted_to_flat device int32 [T*K]  out, may be NULL: t*K+k for each row
+ *                                      below offsets[E], -1 after it.
+ *   counts         device int32 [E]    out: routes per expert.
+ *   offsets        device int32 [E+1]  out: offsets[0] = 0, offsets[e+1] =
+ *                                      offsets[e] + counts[e]; expert e owns
+ *                                      rows [offsets[e], offsets[e+1]).
+ *   workspace      device, >= mp_build_map_workspace_size(T,K,E) bytes,
+ *                  4-byte aligned; scratch, contents undefined after the call.
+ *   dev_status     device int32 or NULL: MP_STATUS_BAD_EXPERT.
+ * Deterministic: the result does not depend on scheduling.
+ */
+mp_status_t mp_build_map(const int32_t *idx, int64_t T, int32_t K, int32_t E,
+                         int32_t *row_id_map, int32_t *sorted_to_flat, int32_t *counts,
+                         int32_t *offsets, void *workspace, size_t workspace_bytes,
+                         int32_t *dev_status, mp_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Permute / unpermute  [d9d _permute_kernel, _unpermute_kernel; MBI]        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * out[row_id_map[t,k], :] = x[t, :]  and  out_probs[row_id_map[t,k]] =
+ * probs[t,k], for every non-empty slot.  The row is copied whatever its
+ * probability.
+ *   x          device bf16 [T,H]
+ *   probs      device fp32 [T,K] or NULL (then out_probs is ignored)
+ *   row_id_map device int32 [T,K] from mp_build_map
+ *   out        device bf16 [R_out,H], R_out > every row id (T*K suffices);
+ *              rows no slot maps to are not written.
+ *   out_probs  device fp32 [R_out] or NULL
+ */
+mp_status_t mp_permute(const mp_bf16_t *x, const float *probs, const int32_t *row_id_map,
+                       int64_t T, int32_t K, int32_t H, mp_bf16_t *out, float *out_probs,
+                       mp_stream_t stream);
+
+/*
+ * Batch-invariant combine: for each token t and element h,
+ *   acc = +0.0f; for k = 0..K-1 (slot order, empty slots skipped):
+ *       acc = fmaf(probs[t,k], float(rows[row_id_map[t,k], h]), acc)
+ *   out[t,h] = bf16 round-to-nearest-even(acc)
+ * With probs == NULL: acc = acc + float(row) (a plain sum).  FP32 fused
+ * multiply-adds in slot order from zero, one BF16 rounding
+ * [MBI _rank_tree_unpermute_kernel; unpermute].  A token with no routed
+ * slot gets +0.
+ *   rows  device bf16 [>= max row id + 1, H];  out device bf16 [T,H].
+ */
+mp_status_t mp_unpermute(const mp_bf16_t *rows, const float *probs,
+                         const int32_t *row_id_map, int64_t T, int32_t K, int32_t H,
+                         mp_bf16_t *out, mp_stream_t stream);
+
+/*
+ * Backward of mp_permute [d9d _moe_permute_mask_map.backward; mops
+ * permute_backward]:
+ *   g_x[t,h]     = bf16_rne(sum over k in slot order, fp32 from +0, of
+ *                  float(g_out[row_id_map[t,k], h]))      (= mp_unpermute, no probs)
+ *   g_probs[t,k] = g_out_probs[row_id_map[t,k]], 0 for an empty slot.
+ *   g_out_probs / g_probs: both NULL or both given.
+ */
+mp_status_t mp_permute_bwd(const mp_bf16_t *g_out, const float *g_out_probs,
+                           const int32_t *row_id_map, int64_t T, int32_t K, int32_t H,
+                           mp_bf16_t *g_x, float *g_probs, mp_stream_t stream);
+
+/*
+ * Backward of mp_unpermute.
+ * With probs [d9d _unpermute_bwd_with_merging_probs_kernel]:
+ *   g_rows[row_id_map[t,k], h] = bf16_rne(probs[t,k] * float(g_y[t,h]))
+ *   g_probs[t,k] = sum_h float(rows[row_id_map[t,k], h]) * float(g_y[t,h])
+ *                  in fp32 (fixed reduction tree, so deterministic; 0 for an
+ *                  empty slot).  `rows` is the forward input.
+ * Without probs [MBI _rank_tree_unpermute_bwd_kernel]: g_rows[row] = g_y[t]
+ * for each routed slot; rows and g_probs may be NULL.
+ */
+mp_status_t mp_unpermute_bwd(const mp_bf16_t *g_y, const mp_bf16_t *rows,
+                             const float *probs, const int32_t *row_id_map, int64_t T,
+                             int32_t K, int32_t H, mp_bf16_t *g_rows, float *g_probs,
+                             mp_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Chunk sort + pad, unpad + restore  [TE-PR]                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Fused sort + pad.  The N-row input holds C consecutive chunks, chunk c
+ * having split_sizes[c] rows (input order).  Output group g (G groups, C % G
+ * == 0) is made of chunks chunk_order[g*C/G .. (g+1)*C/G) in that order, each
+ * chunk's rows consecutive and in input order, then zero rows up to a
+ * multiple of `align`.  Output rows past the padded total, up to out_rows,
+ * are zero too.
+ *   x, probs            device bf16 [N,H], fp32 [N] or NULL
+ *   split_sizes         device int32 [C]   (runtime data: a graph replays with
+ *   chunk_order         device int32 [C]    new sizes in the same buffers)
+ *   out, out_probs      device bf16 [out_rows,H], fp32 [out_rows] or NULL
+ *   row_map             device int32 [out_rows] out: input row at each output
+ *                       row, -1 for padding (the map the restore uses)
+ *   group_off           device int64 [G+1] out: first row of each group, and
+ *                       the padded total at [G]
+ *   dev_status          MP_STATUS_BAD_SPLIT / BAD_ORDER / SPLIT_OVERFLOW /
+ *                       ROWS_OVERFLOW
+ * Limits: 1 <= C <= MP_MAX_CHUNKS, align >= 1, N < 2^31, out_rows < 2^31.
+ */
+mp_status_t mp_sort_chunks_pad(const mp_bf16_t *x, const float *probs,
+                               const int32_t *split_sizes, const int32_t *chunk_order,
+                               int32_t C, int32_t G, int32_t align, int64_t N,
+                               int64_t out_rows, int32_t H, mp_bf16_t *out,
+                               float *out_probs, int32_t *row_map, int64_t *group_off,
+                               int32_t *dev_status, mp_stream_t stream);
+
+/*
+ * Unpad + restore: y[row_map[d]] = padded[d] (and y_probs likewise) for every
+ * d with row_map[d] >= 0; padding rows are dropped.  Rows of y that no d
+ * names are not written.  row_map must not name a row twice.
+ * dev_status: MP_STATUS_BAD_ROW for an entry outside [-1,N).
+ */
+mp_status_t mp_unpad_restore(const mp_bf16_t *padded, const float *padded_probs,
+                             const int32_t *row_map, int64_t out_rows, int64_t N,
+                             int32_t H, mp_bf16_t *y, float *y_probs, int32_t *dev_status,
+                             mp_stream_t stream);
+
+/* Backward of mp_sort_chunks_pad: g_x[row_map[d]] = g_out[d] (padding
+ * gradients discarded) -- mp_unpad_restore applied to the gradients. */
+mp_status_t mp_sort_chunks_pad_bwd(const mp_bf16_t *g_out, const float *g_out_probs,
+                                   const int32_t *row_map, int64_t out_rows, int64_t N,
+                                   int32_t H, mp_bf16_t *g_x, float *g_probs,
+                                   int32_t *dev_status, mp_stream_t stream);
+
+/* Backward of mp_unpad_restore: g_padded[d] = g_y[row_map[d]], and zero for
+ * padding rows ("contributes zero gradient"). */
+mp_status_t mp_unpad_restore_bwd(const mp_bf16_t *g_y, const float *g_y_probs,
+                                 const int32_t *row_map, int64_t out_rows, int64_t N,
+                                 int32_t H, mp_bf16_t *g_padded, float *g_padded_probs,
+                                 int32_t *dev_status, mp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MP_H */

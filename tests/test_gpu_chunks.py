@@ -1,0 +1,126 @@
+"""Parity of the fused chunk sort+pad, unpad+restore and their backwards
+(through the C ABI) with the oracle: bit-exact layouts, maps, offsets and
+copies, status bits for bad metadata."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import unpermute_routing_indices_gb300 as mp
+from unpermute_routing_indices_gb300 import workloads as wl
+from tests.gpu_util import DEV, d, h, status_word
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(x, probs, sizes, order, G, align, out_rows, expect_flags=()):
+    N = x.shape[0]
+    st = status_word()
+    out, out_p, row_map, goff = mp.mp_sort_chunks_pad(
+        d(x), d(sizes), d(order), G, align, out_rows, d(probs) if probs is not None else None,
+        status=st)
+    o_out, o_out_p, o_map, o_goff, fl = oracle.sort_chunks_pad(x, probs, sizes, order, G,
+                                                               align, out_rows)
+    np.testing.assert_array_equal(h(row_map), o_map)
+    np.testing.assert_array_equal(h(goff), o_goff)
+    np.testing.assert_array_equal(h(out), o_out)
+    if probs is not None:
+        np.testing.assert_array_equal(h(out_p), o_out_p)
+    want = {k for k, v in fl.items() if v}
+    assert mp.status_bits(int(h(st)[0])) == want
+    assert want == set(expect_flags)
+    return out, out_p, row_map, o_map
+
+
+@pytest.mark.parametrize("N", [8192, 32768])
+@pytest.mark.parametrize("capacity", [False, True])
+def test_sort_pad_roundtrip_workload(N, capacity):
+    c = wl.chunks(N)
+    G, align = c["G"], c["align"]
+    exact_rows = int(sum(-(-int(s) // align) * align for s in
+                         c["split_sizes"][c["chunk_order"]].reshape(G, -1).sum(1)))
+    out_rows = wl.padded_rows_bound(N, G, align) if capacity else exact_rows
+    out, out_p, row_map, o_map = run_case(c["x"], c["probs"], c["split_sizes"],
+                                          c["chunk_order"], G, align, out_rows)
+    # restore
+    y, y_p = mp.mp_unpad_restore(out, row_map, N, out_p)
+    np.testing.assert_array_equal(h(y), c["x"])
+    np.testing.assert_array_equal(h(y_p), c["probs"])
+    # backwards
+    g_out = wl.random_rows(out_rows, c["H"], c["g_seed"])
+    g_out_p = np.random.default_rng(c["g_seed"]).standard_normal(out_rows).astype(np.float32)
+    g_x, g_xp = mp.mp_sort_chunks_pad_bwd(d(g_out), row_map, N, d(g_out_p))
+    o_gx, o_gxp = oracle.sort_chunks_pad_bwd(g_out, g_out_p, o_map, N)
+    np.testing.assert_array_equal(h(g_x), o_gx)
+    np.testing.assert_array_equal(h(g_xp), o_gxp)
+    g_y = wl.random_rows(N, c["H"], c["g_seed"] + 1)
+    g_yp = np.random.default_rng(c["g_seed"] + 1).standard_normal(N).astype(np.float32)
+    g_pad, g_padp = mp.mp_unpad_restore_bwd(d(g_y), row_map, d(g_yp))
+    o_gpad, o_gpadp = oracle.unpad_restore_bwd(g_y, g_yp, o_map, N)
+    np.testing.assert_array_equal(h(g_pad), o_gpad)
+    np.testing.assert_array_equal(h(g_padp), o_gpadp)
+    assert np.all(h(g_pad)[o_map < 0] == 0)
+
+
+def _meta(seed, G, R, max_size=40, empty_group=False):
+    rng = np.random.default_rng(seed)
+    C = G * R
+    sizes = rng.integers(0, max_size, size=C).astype(np.int32)
+    sizes[rng.random(C) < 0.25] = 0
+    order = rng.permutation(C).astype(np.int32)
+    if empty_group:
+        sizes[order[:R]] = 0
+    return sizes, order
+
+
+@pytest.mark.parametrize("G,R,align,H,empty_group,extra", [
+    (16, 8, 128, 2048, True, 0),
+    (4, 3, 8, 37, False, 5),        # element path, capacity tail
+    (1, 1, 1, 64, False, 0),        # one chunk, no padding
+    (32, 32, 16, 128, True, 100),   # C = MP_MAX_CHUNKS
+    (5, 2, 3, 24, False, 0),
+])
+def test_sort_pad_edges(G, R, align, H, empty_group, extra):
+    sizes, order = _meta(G * 100 + R, G, R, empty_group=empty_group)
+    N = int(sizes.sum())
+    x = wl.random_rows(N, H, 3)
+    probs = np.random.default_rng(1).random(N).astype(np.float32)
+    out_rows = N + G * (align - 1) + extra
+    out, out_p, row_map, _ = run_case(x, probs, sizes, order, G, align, out_rows)
+    y, y_p = mp.mp_unpad_restore(out, row_map, N, out_p)
+    np.testing.assert_array_equal(h(y), x)
+    np.testing.assert_array_equal(h(y_p), probs)
+    # without probs
+    out2, none, _, _ = mp.mp_sort_chunks_pad(d(x), d(sizes), d(order), G, align, out_rows)
+    assert none is None
+    np.testing.assert_array_equal(h(out2), h(out))
+
+
+def test_sort_pad_status_bits():
+    x = wl.random_rows(64, 16, 5)
+    p = np.arange(64, dtype=np.float32)
+    run_case(x, p, np.array([10, -3, 12, 5], np.int32), np.array([0, 1, 2, 3], np.int32),
+             2, 4, 48, expect_flags=("bad_split",))
+    run_case(x, p, np.array([40, 40], np.int32), np.array([1, 0], np.int32), 1, 1, 90,
+             expect_flags=("split_overflow",))
+    run_case(x, p, np.array([30, 30], np.int32), np.array([0, 1], np.int32), 2, 8, 50,
+             expect_flags=("rows_overflow",))
+    run_case(x, p, np.array([3, 3, 3, 3], np.int32), np.array([0, 7, 2, 3], np.int32), 2, 2,
+             16, expect_flags=("bad_order",))
+
+
+def test_restore_bad_row_sets_status():
+    padded = d(wl.random_rows(8, 16, 1))
+    row_map = d(np.array([0, 1, -1, 9, 2, -5, 3, 4], np.int32))
+    st = status_word()
+    y = torch.zeros((5, 16), dtype=torch.bfloat16, device=DEV)
+    mp.mp_unpad_restore(padded, row_map, 5, y=y, status=st)
+    assert mp.status_bits(int(h(st)[0])) == {"bad_row"}
+    want = np.zeros((5, 16), np.uint16)
+    src = h(padded)
+    for dd, s in enumerate([0, 1, -1, 9, 2, -5, 3, 4]):
+        if 0 <= s < 5:
+            want[s] = src[dd]
+    np.testing.assert_array_equal(h(y), want)

@@ -1,0 +1,299 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle.
+
+Bar: bit-exact for every integer, layout and copied output and for the bf16
+outputs of unpermute / permute_bwd / unpermute_bwd (both sides run the same
+slot-order fp32 FMA chain and one round-to-nearest-even); g_probs of
+unpermute_bwd within the fp32 summation bound against the oracle's fp64 sum
+(gpu_util.gprobs_bound).  Small and mid workloads are compared element by
+element; the full-size skewed (T=16384, H=4096, E=128, K=8) and large
+(T=32768, H=7168, E=256, K=8) workloads in full for the map and on sampled
+tokens for the rows, in the launch configuration the benchmark uses.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import unpermute_routing_indices_gb300 as mp
+from unpermute_routing_indices_gb300 import workloads as wl
+from tests.gpu_util import DEV, bf16_ulp_distance, d, gprobs_bound, h, status_word
+
+pytestmark = pytest.mark.gpu
+
+
+def f32(bits):
+    return oracle.f32_from_bf16(bits) if bits.size < 4096 else \
+        (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def check_map(idx, E, expect_status=0):
+    st = status_word()
+    rim, s2f, counts, offsets = mp.mp_build_map(d(idx), E, status=st)
+    o_rim, o_s2f, o_counts, o_offsets, bad = oracle.build_map(idx, E)
+    np.testing.assert_array_equal(h(rim), o_rim)
+    np.testing.assert_array_equal(h(s2f), o_s2f)
+    np.testing.assert_array_equal(h(counts), o_counts)
+    np.testing.assert_array_equal(h(offsets), o_offsets)
+    assert int(h(st)[0]) == expect_status
+    assert (bad > 0) == bool(expect_status & 1)
+    return rim, o_rim
+
+
+# --------------------------------------------------------------------------
+# routing map
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "mid", "skewed", "large"])
+def test_build_map_workloads(name):
+    idx, _, E = wl.routing(name)
+    check_map(idx, E)
+
+
+def _edge_idx(case):
+    rng = np.random.default_rng(sum(map(ord, case)))
+    if case == "one":
+        return np.zeros((1, 1), np.int32), 1
+    if case == "ragged_dups_empty":
+        idx = rng.integers(-1, 37, size=(3001, 3)).astype(np.int32)
+        return idx, 37
+    if case == "max_experts":
+        return rng.integers(0, 1024, size=(5000, 2)).astype(np.int32), 1024
+    if case == "one_hot_expert":
+        return np.full((4099, 4), 5, np.int32), 8
+    if case == "e1":
+        return np.zeros((2049, 3), np.int32), 1
+    if case == "k16":
+        return rng.integers(0, 64, size=(777, 16)).astype(np.int32), 64
+    if case == "all_empty":
+        return -np.ones((300, 4), np.int32), 16
+    raise KeyError(case)
+
+
+@pytest.mark.parametrize("case", ["one", "ragged_dups_empty", "max_experts", "one_hot_expert",
+                                  "e1", "k16", "all_empty"])
+def test_build_map_edges(case):
+    idx, E = _edge_idx(case)
+    check_map(idx, E)
+
+
+def test_build_map_bad_index_sets_status():
+    rng = np.random.default_rng(5)
+    idx = rng.integers(0, 20, size=(2500, 4)).astype(np.int32)
+    idx[7, 1] = 20
+    idx[1999, 3] = -7
+    check_map(idx, 20, expect_status=mp.STATUS_BITS["bad_expert"])
+
+
+def test_build_map_empty_batch():
+    rim, s2f, counts, offsets = mp.mp_build_map(torch.zeros((0, 4), dtype=torch.int32,
+                                                            device=DEV), 9)
+    assert h(counts).sum() == 0 and np.all(h(offsets) == 0)
+
+
+def test_build_map_is_deterministic():
+    idx, _, E = wl.routing("skewed")
+    a = mp.mp_build_map(d(idx), E)
+    for _ in range(3):
+        b = mp.mp_build_map(d(idx), E)
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+
+
+# --------------------------------------------------------------------------
+# permute / unpermute / backwards, element by element
+# --------------------------------------------------------------------------
+
+def _full_case(name, H=None, T=None, empty=False, rows_seed=7):
+    w = wl.routed(name, T=T, H=H)
+    if empty:
+        rng = np.random.default_rng(3)
+        w["idx"][rng.random(w["idx"].shape) < 0.15] = -1
+    T, H, K = w["T"], w["H"], w["K"]
+    w["rows_in"] = wl.random_rows(T * K, H, seed=rows_seed)
+    w["g_rows_in"] = wl.random_rows(T * K, H, seed=rows_seed + 1)
+    return w
+
+
+@pytest.mark.parametrize("name,H,T,empty", [
+    ("tiny", None, None, False),
+    ("mid", None, None, False),
+    ("mid", None, 1234, True),          # ragged T, empty slots
+    ("mid", 40, 3000, False),           # H % 8 == 0 but short rows
+    ("mid", 37, 999, True),             # element path (H % 8 != 0)
+    ("skewed", 264, 3000, False),       # skewed routing, odd vector count
+])
+def test_forward_and_backward_elementwise(name, H, T, empty):
+    w = _full_case(name, H=H, T=T, empty=empty)
+    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+    idx, probs = d(w["idx"]), d(w["probs"])
+    rim, _, _, _ = mp.mp_build_map(idx, E)
+    o_rim, *_ = oracle.build_map(w["idx"], E)
+    np.testing.assert_array_equal(h(rim), o_rim)
+    mapped = np.sort(o_rim[o_rim >= 0])
+
+    # permute
+    out, out_p = mp.mp_permute(d(w["x"]), rim, probs)
+    o_out, o_out_p = oracle.permute(w["x"], w["probs"], o_rim)
+    np.testing.assert_array_equal(h(out)[mapped], o_out[mapped])
+    np.testing.assert_array_equal(h(out_p)[mapped], o_out_p[mapped])
+    out2, _ = mp.mp_permute(d(w["x"]), rim)
+    np.testing.assert_array_equal(h(out2)[mapped], o_out[mapped])
+
+    # unpermute of independent rows, with and without probs
+    rows = d(w["rows_in"])
+    y = mp.mp_unpermute(rows, rim, probs)
+    np.testing.assert_array_equal(h(y), oracle.unpermute(w["rows_in"], w["probs"], o_rim, T, H))
+    y0 = mp.mp_unpermute(rows, rim)
+    np.testing.assert_array_equal(h(y0), oracle.unpermute(w["rows_in"], None, o_rim, T, H))
+
+    # permute backward
+    g_out = d(w["g_rows_in"])
+    g_op = d(w["g_out_probs"])
+    g_x, g_p = mp.mp_permute_bwd(g_out, rim, g_op)
+    o_gx, o_gp = oracle.permute_bwd(w["g_rows_in"], w["g_out_probs"], o_rim, T, H)
+    np.testing.assert_array_equal(h(g_x), o_gx)
+    np.testing.assert_array_equal(h(g_p), o_gp)
+
+    # unpermute backward with probs
+    g_rows, g_probs = mp.mp_unpermute_bwd(d(w["g_y"]), rim, rows, probs)
+    o_grows, o_gprobs = oracle.unpermute_bwd(w["g_y"], w["rows_in"], w["probs"], o_rim)
+    np.testing.assert_array_equal(h(g_rows)[mapped], o_grows[mapped])
+    gp = h(g_probs).astype(np.float64)
+    rf = f32(w["rows_in"])[np.maximum(o_rim, 0)]           # [T,K,H]
+    gyf = f32(w["g_y"])[:, None, :]
+    bound = gprobs_bound(rf, gyf, o_gprobs)
+    assert np.all(np.abs(gp - o_gprobs) <= bound)
+    assert np.all(gp[o_rim < 0] == 0)
+    # ... and without probs: a plain copy of g_y to every row
+    g_rows0, none = mp.mp_unpermute_bwd(d(w["g_y"]), rim)
+    assert none is None
+    o_grows0, _ = oracle.unpermute_bwd(w["g_y"], None, None, o_rim)
+    np.testing.assert_array_equal(h(g_rows0)[mapped], o_grows0[mapped])
+
+
+def test_misaligned_rows_take_the_element_path():
+    w = _full_case("mid", H=64, T=500)
+    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+    rim, *_ = mp.mp_build_map(d(w["idx"]), E)
+    o_rim, *_ = oracle.build_map(w["idx"], E)
+    base = torch.empty(T * H + 1, dtype=torch.bfloat16, device=DEV)
+    x = base[1:].view(T, H)                              # 2-byte offset: not 16-B aligned
+    x.copy_(d(w["x"]))
+    out, _ = mp.mp_permute(x, rim)
+    o_out, _ = oracle.permute(w["x"], None, o_rim)
+    np.testing.assert_array_equal(h(out), o_out)
+    rbase = torch.empty(T * K * H + 1, dtype=torch.bfloat16, device=DEV)
+    rows = rbase[1:].view(T * K, H)
+    rows.copy_(d(w["rows_in"]))
+    y = mp.mp_unpermute(rows, rim, d(w["probs"]))
+    np.testing.assert_array_equal(h(y), oracle.unpermute(w["rows_in"], w["probs"], o_rim, T, H))
+
+
+def test_unpermute_k1_unit_probs_is_identity():
+    rng = np.random.default_rng(2)
+    T, H, E = 3000, 512, 16
+    idx = rng.integers(0, E, size=(T, 1)).astype(np.int32)
+    x = wl.random_rows(T, H, 9)
+    rim, *_ = mp.mp_build_map(d(idx), E)
+    rows, _ = mp.mp_permute(d(x), rim)
+    ones = torch.ones((T, 1), dtype=torch.float32, device=DEV)
+    np.testing.assert_array_equal(h(mp.mp_unpermute(rows, rim, ones)), x)
+    np.testing.assert_array_equal(h(mp.mp_unpermute(rows, rim)), x)
+
+
+def test_unpermute_is_batch_invariant():
+    """A token's output bits do not change with the rest of the batch."""
+    w = _full_case("mid", T=2048)
+    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+    rim, *_ = mp.mp_build_map(d(w["idx"]), E)
+    rows, _ = mp.mp_permute(d(w["rows_in"][:T]), rim)
+    y_full = h(mp.mp_unpermute(rows, rim, d(w["probs"])))
+    rng = np.random.default_rng(4)
+    sel = np.sort(rng.choice(T, 300, replace=False))
+    for trial in range(2):
+        perm = rng.permutation(300)
+        idx_s = w["idx"][sel][perm]
+        rim_s, *_ = mp.mp_build_map(d(idx_s), E)
+        rows_s, _ = mp.mp_permute(d(w["rows_in"][:T][sel][perm]), rim_s)
+        y_s = h(mp.mp_unpermute(rows_s, rim_s, d(w["probs"][sel][perm])))
+        np.testing.assert_array_equal(y_s, y_full[sel][perm])
+
+
+def test_unpermute_bwd_is_deterministic():
+    w = _full_case("mid", T=2048)
+    rim, *_ = mp.mp_build_map(d(w["idx"]), w["E"])
+    rows, gy, probs = d(w["rows_in"]), d(w["g_y"]), d(w["probs"])
+    a = mp.mp_unpermute_bwd(gy, rim, rows, probs)
+    for _ in range(3):
+        b = mp.mp_unpermute_bwd(gy, rim, rows, probs)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_unpermute_ulp_fallback_not_needed():
+    """The fallback tolerance (1 bf16 ulp) is stated but unused: distance 0."""
+    w = _full_case("tiny")
+    rim, *_ = mp.mp_build_map(d(w["idx"]), w["E"])
+    o_rim, *_ = oracle.build_map(w["idx"], w["E"])
+    y = h(mp.mp_unpermute(d(w["rows_in"]), rim, d(w["probs"])))
+    o = oracle.unpermute(w["rows_in"], w["probs"], o_rim, w["T"], w["H"])
+    assert bf16_ulp_distance(y, o).max() <= 1
+    assert bf16_ulp_distance(y, o).max() == 0
+
+
+# --------------------------------------------------------------------------
+# full-size workloads, sampled
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["skewed", "large"])
+def test_full_size_sampled(name):
+    w = wl.routed(name)
+    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+    R = T * K
+    rng = np.random.default_rng(11)
+    sample = np.unique(np.concatenate([rng.choice(T, 192, replace=False), [0, T - 1]]))
+
+    idx, probs = d(w["idx"]), d(w["probs"])
+    rim, s2f, counts, offsets = mp.mp_build_map(idx, E)
+    o_rim, o_s2f, o_counts, o_offsets, _ = oracle.build_map(w["idx"], E)
+    np.testing.assert_array_equal(h(rim), o_rim)
+    np.testing.assert_array_equal(h(s2f), o_s2f)
+    np.testing.assert_array_equal(h(offsets), o_offsets)
+
+    rs = torch.from_numpy(o_rim[sample].ravel().astype(np.int64)).to(DEV)
+    # permute: every slot of a sampled token holds its row
+    out, out_p = mp.mp_permute(d(w["x"]), rim, probs)
+    got = h(out.index_select(0, rs)).reshape(len(sample), K, H)
+    np.testing.assert_array_equal(got, np.repeat(w["x"][sample][:, None, :], K, axis=1))
+    np.testing.assert_array_equal(h(out_p.index_select(0, rs)).reshape(-1, K),
+                                  w["probs"][sample])
+    del out
+
+    # unpermute of counter-based rows (any row can be rebuilt on the host)
+    seed = 77
+    rows = wl.hashed_rows_torch(R, H, seed, DEV)
+    y = h(mp.mp_unpermute(rows, rim, probs).index_select(
+        0, torch.from_numpy(sample).to(DEV)))
+    rim_s = o_rim[sample]
+    flat_rows = rim_s.ravel()
+    rows_s = wl.hashed_rows(flat_rows, H, seed)
+    local = np.arange(flat_rows.size, dtype=np.int32).reshape(rim_s.shape)
+    np.testing.assert_array_equal(
+        y, oracle.unpermute(rows_s, w["probs"][sample], local, len(sample), H))
+
+    # unpermute backward (probs gradient within the fp32 bound)
+    gy = d(w["g_y"])
+    g_rows, g_probs = mp.mp_unpermute_bwd(gy, rim, rows, probs)
+    o_grows, o_gp = oracle.unpermute_bwd(w["g_y"][sample], rows_s, w["probs"][sample], local)
+    got = h(g_rows.index_select(0, rs))
+    np.testing.assert_array_equal(got, o_grows)
+    gp = h(g_probs)[sample].astype(np.float64)
+    bound = gprobs_bound(f32(rows_s).reshape(len(sample), K, H),
+                         f32(w["g_y"][sample])[:, None, :], o_gp)
+    assert np.all(np.abs(gp - o_gp) <= bound)
+
+    # permute backward of the same counter-based rows
+    g_x, _ = mp.mp_permute_bwd(rows, rim)
+    o_gx, _ = oracle.permute_bwd(rows_s, None, local, len(sample), H)
+    np.testing.assert_array_equal(h(g_x)[sample], o_gx)

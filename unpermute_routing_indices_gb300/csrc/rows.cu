@@ -1,0 +1,375 @@
+// Row movement of the permute / unpermute path and its backward.
+//
+//   k_permute        out[row_id_map[t,k]] = x[t]            (d9d _permute_kernel)
+//   k_unpermute      out[t] = bf16(fma chain over slots)     (Megatron
+//                    batch_invariant _rank_tree_unpermute_kernel); also the
+//                    permute backward (plain sum + probs gather)
+//   k_unpermute_bwd  g_rows[row] = bf16(p * g_y[t]), g_probs = <rows[row], g_y[t]>
+//                    (d9d _unpermute_bwd_with_merging_probs_kernel)
+//
+// One group of `tpt` threads (a power of two, at most a CTA) owns a token;
+// a CTA of ROW_THREADS threads holds ROW_THREADS / tpt tokens.  Each thread
+// moves VPT 16-byte vectors of the row per pass (uint4 = 8 bf16), or single
+// bf16 elements when rows are not 16-byte aligned.  The token's row is read
+// once into registers and stored once per slot (permute), or its K source
+// rows are all requested before the first FMA so that K * VPT loads are in
+// flight per thread (unpermute).  Every token writes only its own rows, so no
+// store ever collides and no atomics are needed.
+#include "common.cuh"
+
+namespace mp {
+namespace {
+
+constexpr int ROW_THREADS = 256;
+constexpr int KB = 8;  // slots whose rows are in flight together
+
+struct RowGrid {
+    int tpt_log2;
+    unsigned blocks;
+};
+
+inline RowGrid row_grid(int64_t T, int nvec, int vpt)
+{
+    const int want = (nvec + vpt - 1) / vpt;
+    int l = ceil_log2(want < 1 ? 1 : want);
+    if (l > 8) l = 8;
+    const int64_t tokens_per_block = ROW_THREADS >> l;
+    return RowGrid{l, (unsigned)((T + tokens_per_block - 1) / tokens_per_block)};
+}
+
+template <typename V, int VPT, bool PROBS>
+__global__ void __launch_bounds__(ROW_THREADS)
+    k_permute(const V *__restrict__ x, const float *__restrict__ probs,
+              const int32_t *__restrict__ map, int64_t T, int K, int nvec, int tpt_log2,
+              V *__restrict__ out, float *__restrict__ out_probs)
+{
+    const int tpt = 1 << tpt_log2;
+    const int lane = threadIdx.x & (tpt - 1);
+    const int64_t t = (int64_t)blockIdx.x * (ROW_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
+    if (t >= T) return;
+    const int32_t *m = map + t * K;
+    const V *src = x + t * nvec;
+    for (int c0 = 0; c0 < nvec; c0 += tpt * VPT) {
+        V v[VPT];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int c = c0 + j * tpt + lane;
+            v[j] = (c < nvec) ? ld_stream(src + c) : zero_vec<V>();
+        }
+        for (int k = 0; k < K; ++k) {
+            const int32_t row = __ldg(m + k);
+            if (row < 0) continue;
+            V *dst = out + (int64_t)row * nvec;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int c = c0 + j * tpt + lane;
+                if (c < nvec) st_row(dst + c, v[j]);
+            }
+        }
+    }
+    if (PROBS && lane == 0) {
+        for (int k = 0; k < K; ++k) {
+            const int32_t row = __ldg(m + k);
+            if (row >= 0) out_probs[row] = __ldg(probs + t * K + k);
+        }
+    }
+}
+
+// acc = fmaf(p, r, acc) per slot in slot order (PROBS), or acc = acc + r.
+template <typename V, int VPT, bool PROBS, bool GATHER_PROBS>
+__global__ void __launch_bounds__(ROW_THREADS)
+    k_unpermute(const V *__restrict__ rows, const float *__restrict__ probs,
+                const int32_t *__restrict__ map, int64_t T, int K, int nvec, int tpt_log2,
+                V *__restrict__ out, const float *__restrict__ g_out_probs,
+                float *__restrict__ g_probs)
+{
+    constexpr int L = Lanes<V>::N;
+    const int tpt = 1 << tpt_log2;
+    const int lane = threadIdx.x & (tpt - 1);
+    const int64_t t = (int64_t)blockIdx.x * (ROW_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
+    if (t >= T) return;
+    const int32_t *m = map + t * K;
+    for (int c0 = 0; c0 < nvec; c0 += tpt * VPT) {
+        float acc[VPT][L];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+#pragma unroll
+            for (int e = 0; e < L; ++e) acc[j][e] = 0.0f;
+        for (int kb = 0; kb < K; kb += KB) {
+            int32_t rk[KB];
+            float pk[KB];
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                const int k = kb + i;
+                rk[i] = (k < K) ? __ldg(m + k) : -1;
+                pk[i] = (PROBS && k < K) ? __ldg(probs + t * K + k) : 1.0f;
+            }
+            V r[KB][VPT];
+#pragma unroll
+            for (int i = 0; i < KB; ++i)
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    const int c = c0 + j * tpt + lane;
+                    r[i][j] = (rk[i] >= 0 && c < nvec) ? ld_stream(rows + (int64_t)rk[i] * nvec + c)
+                                                       : zero_vec<V>();
+                }
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                if (rk[i] < 0) continue;
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    float f[L];
+                    unpack(r[i][j], f);
+#pragma unroll
+                    for (int e = 0; e < L; ++e)
+                        acc[j][e] = PROBS ? __fmaf_rn(pk[i], f[e], acc[j][e]) : __fadd_rn(acc[j][e], f[e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int c = c0 + j * tpt + lane;
+            if (c < nvec) st_row(out + t * nvec + c, pack(acc[j]));
+        }
+    }
+    if (GATHER_PROBS && lane == 0) {
+        for (int k = 0; k < K; ++k) {
+            const int32_t row = __ldg(m + k);
+            g_probs[t * K + k] = row >= 0 ? __ldg(g_out_probs + row) : 0.0f;
+        }
+    }
+}
+
+// Backward of the weighted combine.  All threads stay to the end (the probs
+// gradient is a CTA reduction), so tokens past T run with no routed slot.
+template <typename V, int VPT>
+__global__ void __launch_bounds__(ROW_THREADS)
+    k_unpermute_bwd(const V *__restrict__ gy, const V *__restrict__ rows,
+                    const float *__restrict__ probs, const int32_t *__restrict__ map, int64_t T,
+                    int K, int nvec, int tpt_log2, V *__restrict__ g_rows,
+                    float *__restrict__ g_probs)
+{
+    constexpr int L = Lanes<V>::N;
+    __shared__ float s_red[ROW_THREADS / 32][KB];
+    const int tpt = 1 << tpt_log2;
+    const int lane = threadIdx.x & (tpt - 1);
+    const int64_t t = (int64_t)blockIdx.x * (ROW_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
+    const bool active = t < T;
+    const int32_t *m = map + t * K;
+
+    for (int kb = 0; kb < K; kb += KB) {
+        int32_t rk[KB];
+        float pk[KB], dot[KB];
+#pragma unroll
+        for (int i = 0; i < KB; ++i) {
+            const int k = kb + i;
+            rk[i] = (active && k < K) ? __ldg(m + k) : -1;
+            pk[i] = (active && k < K) ? __ldg(probs + t * K + k) : 0.0f;
+            dot[i] = 0.0f;
+        }
+        for (int c0 = 0; c0 < nvec; c0 += tpt * VPT) {
+            V g[VPT];
+            V r[KB][VPT];
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int c = c0 + j * tpt + lane;
+                g[j] = (active && c < nvec) ? ld_stream(gy + t * nvec + c) : zero_vec<V>();
+            }
+#pragma unroll
+            for (int i = 0; i < KB; ++i)
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    const int c = c0 + j * tpt + lane;
+                    r[i][j] = (rk[i] >= 0 && c < nvec) ? ld_stream(rows + (int64_t)rk[i] * nvec + c)
+                                                       : zero_vec<V>();
+                }
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                if (rk[i] < 0) continue;
+#pragma unroll
+                for (int j = 0; j < VPT; ++j) {
+                    const int c = c0 + j * tpt + lane;
+                    if (c >= nvec) continue;
+                    float gf[L], rf[L], o[L];
+                    unpack(g[j], gf);
+                    unpack(r[i][j], rf);
+#pragma unroll
+                    for (int e = 0; e < L; ++e) {
+                        o[e] = __fmul_rn(pk[i], gf[e]);
+                        dot[i] = __fmaf_rn(rf[e], gf[e], dot[i]);
+                    }
+                    st_row(g_rows + (int64_t)rk[i] * nvec + c, pack(o));
+                }
+            }
+        }
+        // Reduce each slot's partial over the token's threads: a butterfly
+        // inside the warp, then the token's warps in order.
+        const int width = tpt < 32 ? tpt : 32;
+#pragma unroll
+        for (int i = 0; i < KB; ++i)
+            for (int o = width >> 1; o > 0; o >>= 1) dot[i] += __shfl_xor_sync(FULL_MASK, dot[i], o);
+        if (tpt > 32) {
+            const int warp = threadIdx.x >> 5;
+            if ((threadIdx.x & 31) == 0)
+#pragma unroll
+                for (int i = 0; i < KB; ++i) s_red[warp][i] = dot[i];
+            __syncthreads();
+            if (active && lane == 0) {
+                const int w0 = warp, nw = tpt >> 5;
+                for (int i = 0; i < KB && kb + i < K; ++i) {
+                    float s = 0.0f;
+                    for (int w = 0; w < nw; ++w) s += s_red[w0 + w][i];
+                    g_probs[t * K + kb + i] = rk[i] >= 0 ? s : 0.0f;
+                }
+            }
+            __syncthreads();
+        } else if (active && lane == 0) {
+            for (int i = 0; i < KB && kb + i < K; ++i)
+                g_probs[t * K + kb + i] = rk[i] >= 0 ? dot[i] : 0.0f;
+        }
+    }
+}
+
+inline bool rows_ok(int64_t T, int32_t K, int32_t H)
+{
+    return T >= 0 && K >= 1 && H >= 1 && T * (int64_t)K <= INT32_MAX;
+}
+
+inline bool vec_ok(int32_t H, std::initializer_list<const void *> ptrs)
+{
+    if (H % 8 != 0) return false;
+    for (const void *p : ptrs)
+        if (p != nullptr && !aligned16(p)) return false;
+    return true;
+}
+
+constexpr int PERMUTE_VPT = 4;
+constexpr int UNPERMUTE_VPT = 2;
+constexpr int BWD_VPT = 2;
+constexpr int ELEM_VPT = 8;
+
+template <typename V, int VPT>
+void launch_permute(const void *x, const float *probs, const int32_t *map, int64_t T, int K,
+                    int nvec, void *out, float *out_probs, cudaStream_t s)
+{
+    const RowGrid g = row_grid(T, nvec, VPT);
+    if (probs != nullptr && out_probs != nullptr)
+        k_permute<V, VPT, true><<<g.blocks, ROW_THREADS, 0, s>>>(
+            (const V *)x, probs, map, T, K, nvec, g.tpt_log2, (V *)out, out_probs);
+    else
+        k_permute<V, VPT, false><<<g.blocks, ROW_THREADS, 0, s>>>(
+            (const V *)x, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr);
+}
+
+template <typename V, int VPT>
+void launch_unpermute(const void *rows, const float *probs, const int32_t *map, int64_t T, int K,
+                      int nvec, void *out, const float *g_out_probs, float *g_probs,
+                      cudaStream_t s)
+{
+    const RowGrid g = row_grid(T, nvec, VPT);
+    if (probs != nullptr)
+        k_unpermute<V, VPT, true, false><<<g.blocks, ROW_THREADS, 0, s>>>(
+            (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr, nullptr);
+    else if (g_probs != nullptr)
+        k_unpermute<V, VPT, false, true><<<g.blocks, ROW_THREADS, 0, s>>>(
+            (const V *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, g_out_probs,
+            g_probs);
+    else
+        k_unpermute<V, VPT, false, false><<<g.blocks, ROW_THREADS, 0, s>>>(
+            (const V *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr, nullptr);
+}
+
+template <typename V, int VPT>
+void launch_unpermute_bwd(const void *gy, const void *rows, const float *probs,
+                          const int32_t *map, int64_t T, int K, int nvec, void *g_rows,
+                          float *g_probs, cudaStream_t s)
+{
+    const RowGrid g = row_grid(T, nvec, VPT);
+    k_unpermute_bwd<V, VPT><<<g.blocks, ROW_THREADS, 0, s>>>(
+        (const V *)gy, (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)g_rows, g_probs);
+}
+
+}  // namespace
+}  // namespace mp
+
+using namespace mp;
+
+extern "C" mp_status_t mp_permute(const mp_bf16_t *x, const float *probs,
+                                  const int32_t *row_id_map, int64_t T, int32_t K, int32_t H,
+                                  mp_bf16_t *out, float *out_probs, mp_stream_t stream)
+{
+    if (!rows_ok(T, K, H)) return MP_ERR_INVALID_ARG;
+    if (T == 0) return MP_OK;
+    if (x == nullptr || row_id_map == nullptr || out == nullptr) return MP_ERR_INVALID_ARG;
+    if ((probs == nullptr) != (out_probs == nullptr)) return MP_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (vec_ok(H, {x, out}))
+        launch_permute<uint4, PERMUTE_VPT>(x, probs, row_id_map, T, K, H / 8, out, out_probs, s);
+    else
+        launch_permute<uint16_t, ELEM_VPT>(x, probs, row_id_map, T, K, H, out, out_probs, s);
+    return check_launch();
+}
+
+extern "C" mp_status_t mp_unpermute(const mp_bf16_t *rows, const float *probs,
+                                    const int32_t *row_id_map, int64_t T, int32_t K, int32_t H,
+                                    mp_bf16_t *out, mp_stream_t stream)
+{
+    if (!rows_ok(T, K, H)) return MP_ERR_INVALID_ARG;
+    if (T == 0) return MP_OK;
+    if (rows == nullptr || row_id_map == nullptr || out == nullptr) return MP_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (vec_ok(H, {rows, out}))
+        launch_unpermute<uint4, UNPERMUTE_VPT>(rows, probs, row_id_map, T, K, H / 8, out, nullptr,
+                                               nullptr, s);
+    else
+        launch_unpermute<uint16_t, ELEM_VPT>(rows, probs, row_id_map, T, K, H, out, nullptr,
+                                             nullptr, s);
+    return check_launch();
+}
+
+extern "C" mp_status_t mp_permute_bwd(const mp_bf16_t *g_out, const float *g_out_probs,
+                                      const int32_t *row_id_map, int64_t T, int32_t K, int32_t H,
+                                      mp_bf16_t *g_x, float *g_probs, mp_stream_t stream)
+{
+    if (!rows_ok(T, K, H)) return MP_ERR_INVALID_ARG;
+    if (T == 0) return MP_OK;
+    if (g_out == nullptr || row_id_map == nullptr || g_x == nullptr) return MP_ERR_INVALID_ARG;
+    if ((g_out_probs == nullptr) != (g_probs == nullptr)) return MP_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (vec_ok(H, {g_out, g_x}))
+        launch_unpermute<uint4, UNPERMUTE_VPT>(g_out, nullptr, row_id_map, T, K, H / 8, g_x,
+                                               g_out_probs, g_probs, s);
+    else
+        launch_unpermute<uint16_t, ELEM_VPT>(g_out, nullptr, row_id_map, T, K, H, g_x,
+                                             g_out_probs, g_probs, s);
+    return check_launch();
+}
+
+extern "C" mp_status_t mp_unpermute_bwd(const mp_bf16_t *g_y, const mp_bf16_t *rows,
+                                        const float *probs, const int32_t *row_id_map, int64_t T,
+                                        int32_t K, int32_t H, mp_bf16_t *g_rows, float *g_probs,
+                                        mp_stream_t stream)
+{
+    if (!rows_ok(T, K, H)) return MP_ERR_INVALID_ARG;
+    if (T == 0) return MP_OK;
+    if (g_y == nullptr || row_id_map == nullptr || g_rows == nullptr) return MP_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (probs == nullptr) {
+        // No merging probs: the token's gradient goes unchanged to each row.
+        if (vec_ok(H, {g_y, g_rows}))
+            launch_permute<uint4, PERMUTE_VPT>(g_y, nullptr, row_id_map, T, K, H / 8, g_rows,
+                                               nullptr, s);
+        else
+            launch_permute<uint16_t, ELEM_VPT>(g_y, nullptr, row_id_map, T, K, H, g_rows, nullptr,
+                                               s);
+        return check_launch();
+    }
+    if (rows == nullptr || g_probs == nullptr) return MP_ERR_INVALID_ARG;
+    if (vec_ok(H, {g_y, rows, g_rows}))
+        launch_unpermute_bwd<uint4, BWD_VPT>(g_y, rows, probs, row_id_map, T, K, H / 8, g_rows,
+                                             g_probs, s);
+    else
+        launch_unpermute_bwd<uint16_t, ELEM_VPT>(g_y, rows, probs, row_id_map, T, K, H, g_rows,
+                                                 g_probs, s);
+    return check_launch();
+}

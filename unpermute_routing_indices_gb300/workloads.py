@@ -170,3 +170,66 @@ def chunks(N: int, H: int = CHUNKS["H"], seed: int = CHUNKS["seed"], grads: bool
 def padded_rows_bound(N: int, G: int, align: int) -> int:
     """Capacity that fits any split of N rows into G groups padded to align."""
     return N + G * (align - 1)
+
+
+# --------------------------------------------------------------------------
+# counter-based rows: any row can be drawn alone, on either side
+# --------------------------------------------------------------------------
+#
+# bits(i, h) = fmix32((seed * 0x9E3779B1 + i * H + h) mod 2^32), the 32-bit
+# finaliser of MurmurHash3 (x ^= x>>16; x *= 0x85EBCA6B; x ^= x>>13;
+# x *= 0xC2B2AE35; x ^= x>>16).  The bf16 value keeps the hash's sign bit and
+# its 7 low mantissa bits, with an exponent in [120, 127]: magnitudes in
+# [2^-7, 2).  numpy and torch evaluate the same integer recipe, so a test can
+# fill a full-size tensor on the GPU and rebuild just the rows it samples on
+# the host.
+
+_M32 = 0xFFFFFFFF
+
+
+def _fmix32_np(x: np.ndarray) -> np.ndarray:
+    x = x.astype(np.uint64) & _M32
+    x ^= x >> np.uint64(16)
+    x = (x * np.uint64(0x85EBCA6B)) & np.uint64(_M32)
+    x ^= x >> np.uint64(13)
+    x = (x * np.uint64(0xC2B2AE35)) & np.uint64(_M32)
+    x ^= x >> np.uint64(16)
+    return x
+
+
+def _hash_to_bf16_np(hv: np.ndarray) -> np.ndarray:
+    sign = (hv >> np.uint64(16)) & np.uint64(0x8000)
+    exp = (np.uint64(120) + ((hv >> np.uint64(7)) & np.uint64(7))) << np.uint64(7)
+    return (sign | exp | (hv & np.uint64(0x7F))).astype(np.uint16)
+
+
+def hashed_rows(row_ids, H: int, seed: int) -> np.ndarray:
+    """Rows `row_ids` (any order) of the counter-based bf16 tensor, as uint16."""
+    r = np.asarray(row_ids, dtype=np.uint64).reshape(-1, 1)
+    ctr = (np.uint64(seed) * np.uint64(0x9E3779B1) + r * np.uint64(H)
+           + np.arange(H, dtype=np.uint64)[None, :])
+    return _hash_to_bf16_np(_fmix32_np(ctr))
+
+
+def hashed_rows_torch(n_rows: int, H: int, seed: int, device, chunk_rows: int = 8192):
+    """The whole [n_rows, H] counter-based tensor as torch.bfloat16 on `device`
+    (integer work in int64 with explicit 32-bit masks)."""
+    import torch
+
+    out = torch.empty((n_rows, H), dtype=torch.int16, device=device)
+    cols = torch.arange(H, dtype=torch.int64, device=device)
+    base = (seed * 0x9E3779B1) & _M32
+    for r0 in range(0, n_rows, chunk_rows):
+        r1 = min(n_rows, r0 + chunk_rows)
+        rows = torch.arange(r0, r1, dtype=torch.int64, device=device)
+        x = (base + rows[:, None] * H + cols[None, :]) & _M32
+        x = x ^ (x >> 16)
+        x = (x * 0x85EBCA6B) & _M32
+        x = x ^ (x >> 13)
+        x = (x * 0xC2B2AE35) & _M32
+        x = x ^ (x >> 16)
+        sign = (x >> 16) & 0x8000
+        exp = (120 + ((x >> 7) & 7)) << 7
+        bits = sign | exp | (x & 0x7F)
+        out[r0:r1] = (bits - ((bits >> 15) << 16)).to(torch.int16)
+    return out.view(torch.bfloat16)
