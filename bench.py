@@ -215,7 +215,7 @@ def run_gpu(args):
 
     # ---- routed workload: per-rank batch (weak scaling), seeded per rank
     base_seed = wl.ROUTED[WORKLOAD]["seed"] + 7919 * rank
-    w = wl.routed(WORKLOAD, seed=base_seed)
+    w = wl.routed(WORKLOAD, T=args.tokens, seed=base_seed)
     T, H, E, K = w["T"], w["H"], w["E"], w["K"]
     R = T * K
 
@@ -489,6 +489,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-chunks", action="store_true", help="skip the sort+pad roundtrip")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="smaller T of the same workload (profiling captures only)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
