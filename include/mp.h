@@ -111,6 +111,38 @@ mp_status_t mp_build_map(const int32_t *idx, int64_t T, int32_t K, int32_t E,
                          int32_t *offsets, void *workspace, size_t workspace_bytes,
                          int32_t *dev_status, mp_stream_t stream);
 
+/*
+ * Allocation-free mp_build_map.  The pages have no counterpart: this entry
+ * point exists for callers that cannot call cudaMalloc -- an inference
+ * runtime or plugin that plans all device memory at start-up and forbids
+ * allocation afterwards, a framework whose allocator owns the device memory,
+ * or a latency-critical path that must not risk the implicit device
+ * synchronisation of cudaMalloc.  It computes exactly what mp_build_map
+ * computes, but its scratch (the per-tile expert counts) lives in a static
+ * device array inside the library, MP_NOALLOC_SCRATCH_BYTES per GPU, which
+ * every GPU that loads the library holds until the process exits.  The
+ * caller still passes every input and output.
+ *   - Limit: (E+1) * ceil(T*K / 2048) * 4 <= MP_NOALLOC_SCRATCH_BYTES
+ *     (e.g. E=128 up to T*K = 4,161,536 routes; E=256 up to 2,088,960).
+ *     Larger sizes return MP_ERR_UNSUPPORTED and launch nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current, and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array.  Calls that overlap on the GPU (other
+ *     streams, other threads) race on it and give wrong maps: serialise them.
+ *     Nothing needs clearing between calls: every entry a call reads was
+ *     written earlier in the same call.
+ *   - Never calls cudaMalloc, cudaFree or any allocating routine.
+ * Arguments, outputs and errors are those of mp_build_map without the
+ * workspace.
+ */
+#define MP_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+mp_status_t mp_build_map_noalloc(const int32_t *idx, int64_t T, int32_t K, int32_t E,
+                                 int32_t *row_id_map, int32_t *sorted_to_flat,
+                                 int32_t *counts, int32_t *offsets, int32_t *dev_status,
+                                 mp_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Permute / unpermute  [d9d _permute_kernel, _unpermute_kernel; MBI]        */
 /* ------------------------------------------------------------------------ */

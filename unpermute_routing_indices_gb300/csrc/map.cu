@@ -19,6 +19,8 @@
 //                popc(peers & lanemask_lt) is the stable rank inside the chunk.
 //                Per-warp counters, seeded by a scan across the CTA's warps
 //                from the tile base, carry the rank from chunk to chunk.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace mp {
@@ -275,6 +277,80 @@ extern "C" mp_status_t mp_build_map(const int32_t *idx, int64_t T, int32_t K, in
             (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
             return MP_ERR_WORKSPACE;
     }
+    cudaStream_t s = as_stream(stream);
+    if (ntiles > 0)
+        k_map_count<<<(unsigned)ntiles, MAP_THREADS, (E + 1) * sizeof(int32_t), s>>>(
+            idx, n, E, (int)ntiles, tile_counts, dev_status);
+    k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)ntiles, counts, offsets);
+    if (ntiles > 0)
+        k_map_rank<<<(unsigned)ntiles, MAP_THREADS, MAP_WARPS * (E + 1) * sizeof(int32_t), s>>>(
+            idx, n, E, (int)ntiles, tile_counts, row_id_map, sorted_to_flat);
+    return check_launch();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free routing map: the same three launches as mp_build_map, with
+// the tile counts in a static device array owned by the library, for callers
+// that cannot allocate device memory.
+// ---------------------------------------------------------------------------
+
+namespace mp {
+
+constexpr int NOALLOC_SCRATCH_INTS = MP_NOALLOC_SCRATCH_BYTES / sizeof(int32_t);
+
+// One copy per GPU that loads the library, held until the process exits.
+static __device__ __align__(256) int32_t g_map_scratch[NOALLOC_SCRATCH_INTS];
+
+namespace {
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_scratch_mutex;
+int32_t *g_scratch_addr[NOALLOC_MAX_DEVICES] = {};
+
+// Device address of g_map_scratch on the current device.  The host-side name
+// is only a stand-in, so the address is looked up once per device (with that
+// device current) and cached.
+mp_status_t scratch_on_current_device(int32_t **addr)
+{
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) {
+        set_last_cuda_error(err);
+        return MP_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return MP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_map_scratch);
+        if (err != cudaSuccess || p == nullptr) {
+            set_last_cuda_error(err);
+            return MP_ERR_CUDA;
+        }
+        g_scratch_addr[dev] = static_cast<int32_t *>(p);
+    }
+    *addr = g_scratch_addr[dev];
+    return MP_OK;
+}
+}  // namespace
+}  // namespace mp
+
+extern "C" mp_status_t mp_build_map_noalloc(const int32_t *idx, int64_t T, int32_t K, int32_t E,
+                                            int32_t *row_id_map, int32_t *sorted_to_flat,
+                                            int32_t *counts, int32_t *offsets,
+                                            int32_t *dev_status, mp_stream_t stream)
+{
+    if (T < 0 || K < 1 || E < 1) return MP_ERR_INVALID_ARG;
+    if (!map_sizes_ok(T, K, E)) return MP_ERR_UNSUPPORTED;
+    if (counts == nullptr || offsets == nullptr) return MP_ERR_INVALID_ARG;
+    const int64_t n = T * (int64_t)K;
+    if (n > 0 && (idx == nullptr || row_id_map == nullptr)) return MP_ERR_INVALID_ARG;
+    const int64_t ntiles = map_tiles(n);
+    if ((int64_t)(E + 1) * ntiles > NOALLOC_SCRATCH_INTS) return MP_ERR_UNSUPPORTED;
+    int32_t *tile_counts = nullptr;
+    const mp_status_t st = scratch_on_current_device(&tile_counts);
+    if (st != MP_OK) return st;
+    // Every tile count the scan and rank kernels read is first written by
+    // k_map_count in this call, so the array needs no clearing.
     cudaStream_t s = as_stream(stream);
     if (ntiles > 0)
         k_map_count<<<(unsigned)ntiles, MAP_THREADS, (E + 1) * sizeof(int32_t), s>>>(
