@@ -122,9 +122,11 @@ mp_status_t mp_build_map(const int32_t *idx, int64_t T, int32_t K, int32_t E,
  * device array inside the library, MP_NOALLOC_SCRATCH_BYTES per GPU, which
  * every GPU that loads the library holds until the process exits.  The
  * caller still passes every input and output.
- *   - Limit: (E+1) * ceil(T*K / 2048) * 4 <= MP_NOALLOC_SCRATCH_BYTES
- *     (e.g. E=128 up to T*K = 4,161,536 routes; E=256 up to 2,088,960).
- *     Larger sizes return MP_ERR_UNSUPPORTED and launch nothing.
+ *   - Limit: (E+1) * tiles * 4 <= MP_NOALLOC_SCRATCH_BYTES, where tiles =
+ *     ceil(T*K / (2048*f)) and f is the smallest of 1, 2, 4, 8 that gives at
+ *     most 64 tiles (so every E is accepted up to 1,048,576 routes; E=128 up
+ *     to 33,292,288 routes, E=1024 up to 4,177,920).  Larger sizes return
+ *     MP_ERR_UNSUPPORTED and launch nothing.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current, and caches it; make
  *     that first call before any stream capture.

@@ -68,11 +68,15 @@ def _edge_idx(case):
         return rng.integers(0, 64, size=(777, 16)).astype(np.int32), 64
     if case == "all_empty":
         return -np.ones((300, 4), np.int32), 16
+    if case == "three_launch":       # count matrix too large for the fused rank
+        return rng.integers(-1, 1024, size=(25600, 8)).astype(np.int32), 1024
+    if case == "tile_x8":            # 1M routes: 8 sub-tiles per tile
+        return rng.integers(0, 16, size=(131072, 8)).astype(np.int32), 16
     raise KeyError(case)
 
 
 @pytest.mark.parametrize("case", ["one", "ragged_dups_empty", "max_experts", "one_hot_expert",
-                                  "e1", "k16", "all_empty"])
+                                  "e1", "k16", "all_empty", "three_launch", "tile_x8"])
 def test_build_map_edges(case):
     idx, E = _edge_idx(case)
     check_map(idx, E)

@@ -65,11 +65,37 @@ def test_noalloc_map_matches_the_workspace_map_on_consecutive_calls():
         assert torch.equal(got[4], st_ref)
 
 
+def _tiles(routes):
+    """Tile count of the map, as include/mp.h states it."""
+    f = 1
+    while f < 8 and -(-routes // (2048 * f)) > 64:
+        f *= 2
+    return -(-routes // (2048 * f))
+
+
 def test_noalloc_map_rejects_sizes_beyond_its_scratch():
     lib = _lib.load()
     E, K = 1024, 8
-    T = (1 << 20) // 4 // (E + 1) * 2048 // K + 2048    # one tile too many
-    null = ctypes.c_void_p(0x1000)                       # never touched: rejected first
-    code = lib.mp_build_map_noalloc(null, T, K, E, null, None, null, null, None, None)
+    limit_words = (1 << 20) // 4
+    T = 4096
+    while (E + 1) * _tiles(T * K) <= limit_words:
+        T += 4096
+    # Real, correctly sized buffers: were the size accepted, the call would
+    # still be valid and in bounds.
+    idx = torch.zeros((T, K), dtype=torch.int32, device=DEV)
+    rim = torch.empty((T, K), dtype=torch.int32, device=DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    stream = ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream)
+    code = lib.mp_build_map_noalloc(_p(idx), T, K, E, _p(rim), None, _p(counts), _p(offsets),
+                                    None, stream)
+    torch.cuda.synchronize()
     assert code == -3                                     # MP_ERR_UNSUPPORTED
     assert b"limit" in lib.mp_status_string(code)
+    # one tile fewer is accepted and matches the workspace entry point
+    T_ok = T - 4096
+    ok = _noalloc(lib, idx[:T_ok], E)
+    ref = mp.mp_build_map(idx[:T_ok].contiguous(), E)
+    torch.cuda.synchronize()
+    for a, b in zip(ok[:4], ref):
+        assert torch.equal(a, b)

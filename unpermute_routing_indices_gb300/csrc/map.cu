@@ -7,18 +7,28 @@
 // example in make_row_id_map (d9d / TransformerEngine permutation.py):
 // expert-major, tokens ascending, slots ascending.
 //
-// Three launches, no atomics whose order reaches the result:
-//   k_map_count  one CTA per tile of MAP_TILE routes: per-tile histogram over
-//                E+1 buckets (bucket E collects empty and bad slots), stored
-//                expert-major as tile_counts[b][tile].
-//   k_map_scan   one CTA: exclusive scan of tile_counts in expert-major order.
-//                Entry [b][tile] becomes the first row of bucket b's routes in
-//                that tile; [b][0] is offsets[b], and [E][0] the routed total.
-//   k_map_rank   one CTA per tile: each warp walks 8 chunks of 32 consecutive
-//                routes; __match_any_sync groups the lanes of one expert and
-//                popc(peers & lanemask_lt) is the stable rank inside the chunk.
-//                Per-warp counters, seeded by a scan across the CTA's warps
-//                from the tile base, carry the rank from chunk to chunk.
+// The routes are cut into tiles of 2048*f consecutive routes (f, a power of
+// two up to 8, keeps the tile count near 64).  Inside a tile, warp w owns the
+// contiguous range [w*256f, (w+1)*256f) and walks it in chunks of 32 routes:
+// __match_any_sync groups the lanes that name one expert, and
+// popc(peers & lanemask_lt) is a lane's stable rank inside the chunk.
+//
+//   k_map_count  one CTA per tile: per-tile histogram over E+1 buckets
+//                (bucket E collects empty and bad slots, so sorted_to_flat is
+//                written in full), stored expert-major as tile_counts[b][tile].
+//   k_map_rank   one CTA per tile.  Before it needs the counts it builds its
+//                per-warp histograms from idx alone; launched as a
+//                programmatic dependent of k_map_count, that part overlaps
+//                the count kernel.  It then waits for the tile counts, derives
+//                for every bucket the routes in earlier tiles and the total
+//                (the exclusive scan, done redundantly by every CTA from a
+//                shared-memory copy of the count matrix), seeds per-warp
+//                counters with a scan across its warps, and walks its routes
+//                again to write row_id_map and sorted_to_flat.  CTA 0 writes
+//                counts and offsets.
+// When the count matrix is too large for shared memory, a single-CTA
+// k_map_scan turns it into bases first and k_map_rank reads them (3 launches).
+// No atomics whose order reaches the result: the map is deterministic.
 #include <mutex>
 
 #include "common.cuh"
@@ -35,11 +45,36 @@ namespace {
 
 constexpr int MAP_THREADS = 256;
 constexpr int MAP_WARPS = MAP_THREADS / 32;
-constexpr int MAP_CHUNKS = 8;                          // 32-route chunks per warp
-constexpr int MAP_TILE = MAP_WARPS * MAP_CHUNKS * 32;  // 2048 routes per tile
+constexpr int MAP_CHUNKS = 8;                          // 32-route chunks per warp group
+constexpr int MAP_GROUP = MAP_CHUNKS * 32;             // 256 routes per warp group
+constexpr int MAP_SUB = MAP_WARPS * MAP_GROUP;         // 2048 routes: a tile with f = 1
+constexpr int MAP_TARGET_TILES = 64;
+constexpr int MAP_MAX_F = 8;
+constexpr int64_t MAP_FUSED_MAX_COUNTS = 32768;        // count matrix held in shared memory
 constexpr int SCAN_THREADS = 1024;
 constexpr int SCAN_ITEMS = 8;                          // per thread and pass
 constexpr int SCAN_PASS = SCAN_THREADS * SCAN_ITEMS;
+
+struct MapPlan {
+    int f;           // tile = 2048 * f routes
+    int64_t ntiles;
+    bool fused;      // scan inside k_map_rank
+};
+
+inline MapPlan map_plan(int64_t n, int E)
+{
+    int f = 1;
+    while (f < MAP_MAX_F && (n + (int64_t)MAP_SUB * f - 1) / ((int64_t)MAP_SUB * f) > MAP_TARGET_TILES)
+        f *= 2;
+    const int64_t ntiles = (n + (int64_t)MAP_SUB * f - 1) / ((int64_t)MAP_SUB * f);
+    return MapPlan{f, ntiles, (int64_t)(E + 1) * ntiles <= MAP_FUSED_MAX_COUNTS};
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ int bucket_of(int32_t v, int E) { return (v >= 0 && v < E) ? v : E; }
 
@@ -50,38 +85,51 @@ __device__ __forceinline__ unsigned lanemask_lt()
     return m;
 }
 
-// Buckets of this lane's 8 routes; -1 past the end.
+// Buckets of this lane's 8 routes of one warp group; -1 past the end.
 __device__ __forceinline__ void load_buckets(const int32_t *__restrict__ idx, int64_t n, int E,
                                              int64_t base, int lane, int (&bk)[MAP_CHUNKS],
                                              bool &bad)
 {
+    int32_t v[MAP_CHUNKS];
 #pragma unroll
     for (int c = 0; c < MAP_CHUNKS; ++c) {
         const int64_t i = base + c * 32 + lane;
-        int32_t v = -1;
-        if (i < n) v = __ldg(idx + i);
-        bk[c] = (i < n) ? bucket_of(v, E) : -1;
-        bad |= (i < n) && v != -1 && bk[c] == E;
+        v[c] = (i < n) ? __ldg(idx + i) : -1;
+    }
+#pragma unroll
+    for (int c = 0; c < MAP_CHUNKS; ++c) {
+        const int64_t i = base + c * 32 + lane;
+        bk[c] = (i < n) ? bucket_of(v[c], E) : -1;
+        bad |= (i < n) && v[c] != -1 && bk[c] == E;
     }
 }
 
+// First route of warp `warp`'s range in tile `tile`.
+__device__ __forceinline__ int64_t warp_base(int tile, int warp, int f)
+{
+    return (int64_t)tile * MAP_SUB * f + (int64_t)warp * MAP_GROUP * f;
+}
+
 __global__ void __launch_bounds__(MAP_THREADS)
-    k_map_count(const int32_t *__restrict__ idx, int64_t n, int E, int ntiles,
+    k_map_count(const int32_t *__restrict__ idx, int64_t n, int E, int f, int ntiles,
                 int32_t *__restrict__ tile_counts, int32_t *status)
 {
+    griddep_launch_dependents();   // the rank kernel's idx-only pass may start now
     extern __shared__ int32_t s_hist[];  // [E+1]
     for (int b = threadIdx.x; b <= E; b += MAP_THREADS) s_hist[b] = 0;
     __syncthreads();
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t base = (int64_t)blockIdx.x * MAP_TILE + warp * (MAP_CHUNKS * 32);
-    int bk[MAP_CHUNKS];
+    const int64_t base = warp_base(blockIdx.x, warp, f);
     bool bad = false;
-    load_buckets(idx, n, E, base, lane, bk, bad);
+    for (int g = 0; g < f; ++g) {
+        int bk[MAP_CHUNKS];
+        load_buckets(idx, n, E, base + g * MAP_GROUP, lane, bk, bad);
 #pragma unroll
-    for (int c = 0; c < MAP_CHUNKS; ++c) {
-        const unsigned peers = __match_any_sync(FULL_MASK, bk[c]);
-        if (bk[c] >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[bk[c]], __popc(peers));
+        for (int c = 0; c < MAP_CHUNKS; ++c) {
+            const unsigned peers = __match_any_sync(FULL_MASK, bk[c]);
+            if (bk[c] >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[bk[c]], __popc(peers));
+        }
     }
     if (__any_sync(FULL_MASK, bad) && lane == 0) or_status(status, MP_STATUS_BAD_EXPERT);
     __syncthreads();
@@ -94,6 +142,8 @@ __global__ void __launch_bounds__(MAP_THREADS)
 // bank conflicts.
 __device__ __forceinline__ int spad(int i) { return i + (i >> 5); }
 
+// Single-CTA exclusive scan of the expert-major count matrix (3-launch path,
+// and the T == 0 case where it only writes zero counts and offsets).
 __global__ void __launch_bounds__(SCAN_THREADS)
     k_map_scan(int32_t *__restrict__ tile_counts, int E, int ntiles, int32_t *__restrict__ counts,
                int32_t *__restrict__ offsets)
@@ -144,7 +194,6 @@ __global__ void __launch_bounds__(SCAN_THREADS)
             s_val[spad(tid * SCAN_ITEMS + j)] = run;
             run += v[j];
         }
-        // every thread learns the pass total from the last thread's prefix
         __syncthreads();
         const int32_t last = s_val[spad(SCAN_PASS - 1)];
 #pragma unroll
@@ -169,34 +218,120 @@ __global__ void __launch_bounds__(SCAN_THREADS)
     }
 }
 
-__global__ void __launch_bounds__(MAP_THREADS)
-    k_map_rank(const int32_t *__restrict__ idx, int64_t n, int E, int ntiles,
-               const int32_t *__restrict__ bases, int32_t *__restrict__ row_id_map,
-               int32_t *__restrict__ sorted_to_flat)
+// In-place exclusive scan of a[0..n), n <= 5 * MAP_THREADS, in shared memory;
+// returns the total.  Every thread of the CTA calls it.
+__device__ int32_t cta_exclusive_scan(int32_t *a, int n, int32_t *s_warp)
 {
-    extern __shared__ int32_t s_cnt[];  // [MAP_WARPS][E+1]
+    constexpr int PER = 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lo = tid * PER;
+    int32_t v[PER], sum = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        v[j] = (lo + j < n) ? a[lo + j] : 0;
+        sum += v[j];
+    }
+    int32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int32_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < MAP_WARPS; ++w) {
+        if (w < warp) before += s_warp[w];
+        total += s_warp[w];
+    }
+    int32_t run = before + incl - sum;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        if (lo + j < n) a[lo + j] = run;
+        run += v[j];
+    }
+    __syncthreads();
+    return total;
+}
+
+inline size_t rank_smem(int E, int64_t ntiles, bool fused)
+{
+    size_t words = (size_t)(MAP_WARPS + 1) * (E + 1) + MAP_WARPS;
+    if (fused) words += (size_t)(E + 1) + (size_t)(E + 1) * ntiles;
+    return words * sizeof(int32_t);
+}
+
+template <bool FUSED>
+__global__ void __launch_bounds__(MAP_THREADS)
+    k_map_rank(const int32_t *__restrict__ idx, int64_t n, int E, int f, int ntiles,
+               const int32_t *__restrict__ tile_counts, int32_t *__restrict__ row_id_map,
+               int32_t *__restrict__ sorted_to_flat, int32_t *__restrict__ counts,
+               int32_t *__restrict__ offsets)
+{
+    extern __shared__ int32_t sm[];
     const int stride = E + 1;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t *s_cnt = sm;                              // [MAP_WARPS][E+1] per-warp counters
+    int32_t *s_base = s_cnt + MAP_WARPS * stride;     // [E+1] first row of each bucket here
+    int32_t *s_warp = s_base + stride;                // [MAP_WARPS]
+    int32_t *s_tot = s_warp + MAP_WARPS;              // [E+1] bucket totals (FUSED)
+    int32_t *s_mat = s_tot + stride;                  // [ntiles][E+1] counts (FUSED)
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tile = blockIdx.x;
     int32_t *mine = s_cnt + warp * stride;
-    for (int b = threadIdx.x; b < MAP_WARPS * stride; b += MAP_THREADS) s_cnt[b] = 0;
+    for (int b = tid; b < MAP_WARPS * stride; b += MAP_THREADS) s_cnt[b] = 0;
     __syncthreads();
 
-    const int64_t base = (int64_t)blockIdx.x * MAP_TILE + warp * (MAP_CHUNKS * 32);
-    int bk[MAP_CHUNKS];
+    // Per-warp histograms of this tile: reads idx only.
+    const int64_t base = warp_base(tile, warp, f);
     bool bad = false;
-    load_buckets(idx, n, E, base, lane, bk, bad);
-    unsigned peers[MAP_CHUNKS];
+    for (int g = 0; g < f; ++g) {
+        int bk[MAP_CHUNKS];
+        load_buckets(idx, n, E, base + g * MAP_GROUP, lane, bk, bad);
 #pragma unroll
-    for (int c = 0; c < MAP_CHUNKS; ++c) {
-        peers[c] = __match_any_sync(FULL_MASK, bk[c]);
-        if (bk[c] >= 0 && lane == __ffs(peers[c]) - 1) mine[bk[c]] += __popc(peers[c]);
-        __syncwarp();
+        for (int c = 0; c < MAP_CHUNKS; ++c) {
+            const unsigned peers = __match_any_sync(FULL_MASK, bk[c]);
+            if (bk[c] >= 0 && lane == __ffs(peers) - 1) mine[bk[c]] += __popc(peers);
+            __syncwarp();
+        }
+    }
+
+    griddep_wait();   // the tile counts of every tile are complete from here on
+
+    if (FUSED) {
+        // Copy the expert-major count matrix, transposed to tile-major so the
+        // per-bucket sums below read consecutive words.
+        const int M = stride * ntiles;
+        for (int j = tid; j < M; j += MAP_THREADS) {
+            const int b = j / ntiles, t = j - b * ntiles;
+            s_mat[t * stride + b] = tile_counts[j];
+        }
+        __syncthreads();
+        for (int b = tid; b <= E; b += MAP_THREADS) {
+            int32_t tot = 0, pre = 0;
+            for (int t = 0; t < ntiles; ++t) {
+                const int32_t v = s_mat[t * stride + b];
+                tot += v;
+                pre += (t < tile) ? v : 0;
+            }
+            s_tot[b] = tot;
+            s_base[b] = pre;
+            if (tile == 0 && b < E) counts[b] = tot;
+        }
+        __syncthreads();
+        cta_exclusive_scan(s_tot, stride, s_warp);   // s_tot: offsets of the buckets
+        for (int b = tid; b <= E; b += MAP_THREADS) {
+            s_base[b] += s_tot[b];
+            if (tile == 0) offsets[b] = s_tot[b];
+        }
+    } else {
+        for (int b = tid; b <= E; b += MAP_THREADS) s_base[b] = tile_counts[(int64_t)b * ntiles + tile];
     }
     __syncthreads();
 
     // Per bucket: exclusive scan over the warps, seeded with the tile's base row.
-    for (int b = threadIdx.x; b <= E; b += MAP_THREADS) {
-        int32_t run = bases[(int64_t)b * ntiles + blockIdx.x];
+    for (int b = tid; b <= E; b += MAP_THREADS) {
+        int32_t run = s_base[b];
 #pragma unroll
         for (int w = 0; w < MAP_WARPS; ++w) {
             const int32_t c = s_cnt[w * stride + b];
@@ -207,28 +342,87 @@ __global__ void __launch_bounds__(MAP_THREADS)
     __syncthreads();
 
     const unsigned lt = lanemask_lt();
+    for (int g = 0; g < f; ++g) {
+        int bk[MAP_CHUNKS];
+        const int64_t gbase = base + g * MAP_GROUP;
+        load_buckets(idx, n, E, gbase, lane, bk, bad);
 #pragma unroll
-    for (int c = 0; c < MAP_CHUNKS; ++c) {
-        const int b = bk[c];
-        int32_t row = 0;
-        if (b >= 0) row = mine[b] + __popc(peers[c] & lt);
-        __syncwarp();
-        if (b >= 0 && lane == __ffs(peers[c]) - 1) mine[b] += __popc(peers[c]);
-        __syncwarp();
-        if (b >= 0) {
-            const int64_t i = base + c * 32 + lane;
-            const bool routed = b < E;
-            row_id_map[i] = routed ? row : -1;
-            if (sorted_to_flat != nullptr) sorted_to_flat[row] = routed ? (int32_t)i : -1;
+        for (int c = 0; c < MAP_CHUNKS; ++c) {
+            const int b = bk[c];
+            const unsigned peers = __match_any_sync(FULL_MASK, b);
+            int32_t row = 0;
+            if (b >= 0) row = mine[b] + __popc(peers & lt);
+            __syncwarp();
+            if (b >= 0 && lane == __ffs(peers) - 1) mine[b] += __popc(peers);
+            __syncwarp();
+            if (b >= 0) {
+                const int64_t i = gbase + c * 32 + lane;
+                const bool routed = b < E;
+                row_id_map[i] = routed ? row : -1;
+                if (sorted_to_flat != nullptr) sorted_to_flat[row] = routed ? (int32_t)i : -1;
+            }
         }
     }
 }
 
-inline int64_t map_tiles(int64_t n) { return (n + MAP_TILE - 1) / MAP_TILE; }
-
 inline bool map_sizes_ok(int64_t T, int32_t K, int32_t E)
 {
     return T >= 0 && K >= 1 && E >= 1 && E <= MP_MAX_EXPERTS && T * (int64_t)K <= INT32_MAX;
+}
+
+inline size_t map_workspace_bytes(int64_t n, int E)
+{
+    const MapPlan p = map_plan(n, E);
+    const size_t bytes = (size_t)(E + 1) * (size_t)p.ntiles * sizeof(int32_t);
+    return bytes == 0 ? 256 : (bytes + 255) / 256 * 256;
+}
+
+// Enqueues the map kernels; tile_counts holds (E+1) * plan.ntiles words.
+mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int32_t *row_id_map,
+                       int32_t *sorted_to_flat, int32_t *counts, int32_t *offsets,
+                       int32_t *tile_counts, int32_t *dev_status, cudaStream_t s)
+{
+    const MapPlan p = map_plan(n, E);
+    if (p.ntiles == 0) {
+        k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, 0, counts, offsets);
+        return check_launch();
+    }
+    const unsigned grid = (unsigned)p.ntiles;
+    k_map_count<<<grid, MAP_THREADS, (E + 1) * sizeof(int32_t), s>>>(idx, n, E, p.f, (int)p.ntiles,
+                                                                     tile_counts, dev_status);
+    const size_t smem = rank_smem(E, p.ntiles, p.fused);
+    cudaError_t err = cudaSuccess;
+    if (p.fused) {
+        if (smem > 48 * 1024)
+            err = cudaFuncSetAttribute(k_map_rank<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+        if (err == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(grid);
+            cfg.blockDim = dim3(MAP_THREADS);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            err = cudaLaunchKernelEx(&cfg, k_map_rank<true>, idx, n, E, p.f, (int)p.ntiles,
+                                     (const int32_t *)tile_counts, row_id_map, sorted_to_flat,
+                                     counts, offsets);
+        }
+    } else {
+        k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)p.ntiles, counts, offsets);
+        k_map_rank<false><<<grid, MAP_THREADS, smem, s>>>(idx, n, E, p.f, (int)p.ntiles, tile_counts,
+                                                          row_id_map, sorted_to_flat, counts,
+                                                          offsets);
+    }
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        set_last_cuda_error(err);
+        return MP_ERR_CUDA;
+    }
+    return check_launch();
 }
 
 }  // namespace
@@ -253,9 +447,7 @@ extern "C" int32_t mp_last_cuda_error(void) { return g_last_cuda_error; }
 extern "C" size_t mp_build_map_workspace_size(int64_t T, int32_t K, int32_t E)
 {
     if (!map_sizes_ok(T, K, E)) return 0;
-    const int64_t ntiles = map_tiles(T * (int64_t)K);
-    const size_t bytes = (size_t)(E + 1) * (size_t)ntiles * sizeof(int32_t);
-    return bytes == 0 ? 256 : (bytes + 255) / 256 * 256;
+    return map_workspace_bytes(T * (int64_t)K, E);
 }
 
 extern "C" mp_status_t mp_build_map(const int32_t *idx, int64_t T, int32_t K, int32_t E,
@@ -269,23 +461,13 @@ extern "C" mp_status_t mp_build_map(const int32_t *idx, int64_t T, int32_t K, in
     if (counts == nullptr || offsets == nullptr) return MP_ERR_INVALID_ARG;
     const int64_t n = T * (int64_t)K;
     if (n > 0 && (idx == nullptr || row_id_map == nullptr)) return MP_ERR_INVALID_ARG;
-    const int64_t ntiles = map_tiles(n);
-    int32_t *tile_counts = static_cast<int32_t *>(workspace);
-    if (ntiles > 0) {
-        const size_t need = mp_build_map_workspace_size(T, K, E);
-        if (workspace == nullptr || workspace_bytes < need ||
+    if (n > 0) {
+        if (workspace == nullptr || workspace_bytes < map_workspace_bytes(n, E) ||
             (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
             return MP_ERR_WORKSPACE;
     }
-    cudaStream_t s = as_stream(stream);
-    if (ntiles > 0)
-        k_map_count<<<(unsigned)ntiles, MAP_THREADS, (E + 1) * sizeof(int32_t), s>>>(
-            idx, n, E, (int)ntiles, tile_counts, dev_status);
-    k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)ntiles, counts, offsets);
-    if (ntiles > 0)
-        k_map_rank<<<(unsigned)ntiles, MAP_THREADS, MAP_WARPS * (E + 1) * sizeof(int32_t), s>>>(
-            idx, n, E, (int)ntiles, tile_counts, row_id_map, sorted_to_flat);
-    return check_launch();
+    return launch_map(idx, n, E, row_id_map, sorted_to_flat, counts, offsets,
+                      static_cast<int32_t *>(workspace), dev_status, as_stream(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -344,20 +526,12 @@ extern "C" mp_status_t mp_build_map_noalloc(const int32_t *idx, int64_t T, int32
     if (counts == nullptr || offsets == nullptr) return MP_ERR_INVALID_ARG;
     const int64_t n = T * (int64_t)K;
     if (n > 0 && (idx == nullptr || row_id_map == nullptr)) return MP_ERR_INVALID_ARG;
-    const int64_t ntiles = map_tiles(n);
-    if ((int64_t)(E + 1) * ntiles > NOALLOC_SCRATCH_INTS) return MP_ERR_UNSUPPORTED;
+    if ((int64_t)(E + 1) * map_plan(n, E).ntiles > NOALLOC_SCRATCH_INTS) return MP_ERR_UNSUPPORTED;
     int32_t *tile_counts = nullptr;
     const mp_status_t st = scratch_on_current_device(&tile_counts);
     if (st != MP_OK) return st;
-    // Every tile count the scan and rank kernels read is first written by
+    // Every tile count the rank (and scan) kernels read is first written by
     // k_map_count in this call, so the array needs no clearing.
-    cudaStream_t s = as_stream(stream);
-    if (ntiles > 0)
-        k_map_count<<<(unsigned)ntiles, MAP_THREADS, (E + 1) * sizeof(int32_t), s>>>(
-            idx, n, E, (int)ntiles, tile_counts, dev_status);
-    k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)ntiles, counts, offsets);
-    if (ntiles > 0)
-        k_map_rank<<<(unsigned)ntiles, MAP_THREADS, MAP_WARPS * (E + 1) * sizeof(int32_t), s>>>(
-            idx, n, E, (int)ntiles, tile_counts, row_id_map, sorted_to_flat);
-    return check_launch();
+    return launch_map(idx, n, E, row_id_map, sorted_to_flat, counts, offsets, tile_counts,
+                      dev_status, as_stream(stream));
 }

@@ -20,8 +20,25 @@
 namespace mp {
 namespace {
 
-constexpr int ROW_THREADS = 256;
-constexpr int KB = 8;  // slots whose rows are in flight together
+// Launch shape (overridable at build time for tuning sweeps).
+#ifndef MP_ROW_THREADS
+#define MP_ROW_THREADS 128
+#endif
+#ifndef MP_SLOT_BATCH
+#define MP_SLOT_BATCH 8
+#endif
+#ifndef MP_PERMUTE_VPT
+#define MP_PERMUTE_VPT 4
+#endif
+#ifndef MP_UNPERMUTE_VPT
+#define MP_UNPERMUTE_VPT 1
+#endif
+#ifndef MP_BWD_VPT
+#define MP_BWD_VPT 1
+#endif
+
+constexpr int ROW_THREADS = MP_ROW_THREADS;
+constexpr int KB = MP_SLOT_BATCH;  // slots whose rows are in flight together
 
 struct RowGrid {
     int tpt_log2;
@@ -32,7 +49,8 @@ inline RowGrid row_grid(int64_t T, int nvec, int vpt)
 {
     const int want = (nvec + vpt - 1) / vpt;
     int l = ceil_log2(want < 1 ? 1 : want);
-    if (l > 8) l = 8;
+    const int lmax = ceil_log2(ROW_THREADS);
+    if (l > lmax) l = lmax;
     const int64_t tokens_per_block = ROW_THREADS >> l;
     return RowGrid{l, (unsigned)((T + tokens_per_block - 1) / tokens_per_block)};
 }
@@ -243,9 +261,9 @@ inline bool vec_ok(int32_t H, std::initializer_list<const void *> ptrs)
     return true;
 }
 
-constexpr int PERMUTE_VPT = 4;
-constexpr int UNPERMUTE_VPT = 2;
-constexpr int BWD_VPT = 2;
+constexpr int PERMUTE_VPT = MP_PERMUTE_VPT;
+constexpr int UNPERMUTE_VPT = MP_UNPERMUTE_VPT;
+constexpr int BWD_VPT = MP_BWD_VPT;
 constexpr int ELEM_VPT = 8;
 
 template <typename V, int VPT>
