@@ -81,6 +81,9 @@ def _meta(seed, G, R, max_size=40, empty_group=False):
     (1, 1, 1, 64, False, 0),        # one chunk, no padding
     (32, 32, 16, 128, True, 100),   # C = MP_MAX_CHUNKS
     (5, 2, 3, 24, False, 0),
+    (8, 4, 64, 512, True, 7),       # bulk engine, 1 KiB rows, 16 slots
+    (4, 4, 16, 7168, False, 3),     # bulk engine, 14 KiB rows
+    (2, 2, 4, 24576, True, 0),      # bulk engine, 48 KiB rows, 2 slots
 ])
 def test_sort_pad_edges(G, R, align, H, empty_group, extra):
     sizes, order = _meta(G * 100 + R, G, R, empty_group=empty_group)
@@ -124,3 +127,21 @@ def test_restore_bad_row_sets_status():
         if 0 <= s < 5:
             want[s] = src[dd]
     np.testing.assert_array_equal(h(y), want)
+
+
+def test_bulk_engine_many_rounds_per_cta():
+    """More output rows than CTAs x 256, so every CTA runs several rounds and
+    the slot ring wraps many times."""
+    G, R, align, H = 16, 8, 128, 512
+    sizes, order = _meta(99, G, R, max_size=3600)
+    N = int(sizes.sum())
+    assert N > 2 * 2 * 152 * 256                 # at least two rounds per CTA
+    x = wl.random_rows(N, H, 12)
+    probs = np.random.default_rng(2).random(N).astype(np.float32)
+    out_rows = N + G * (align - 1)
+    out, out_p, row_map, o_map = run_case(x, probs, sizes, order, G, align, out_rows)
+    y, y_p = mp.mp_unpad_restore(out, row_map, N, out_p)
+    np.testing.assert_array_equal(h(y), x)
+    np.testing.assert_array_equal(h(y_p), probs)
+    g_pad, _ = mp.mp_unpad_restore_bwd(d(x), row_map)
+    np.testing.assert_array_equal(h(g_pad), h(out))

@@ -64,8 +64,9 @@ def test_routed_path_graph_replay():
         np.testing.assert_array_equal(h(g_x), o_gx)
 
 
-def test_sort_pad_graph_replay_with_new_sizes():
-    N, H, G, align = 4096, 128, 16, 128
+@pytest.mark.parametrize("H", [128, 1024])      # vector and bulk engines
+def test_sort_pad_graph_replay_with_new_sizes(H):
+    N, G, align = 4096, 16, 128
     out_rows = wl.padded_rows_bound(N, G, align)
     layouts = [wl.chunk_layout(N, seed=s) for s in (10, 11, 12)]
     x_np = wl.random_rows(N, H, 4)

@@ -21,12 +21,12 @@
 //                programmatic dependent of k_map_count, that part overlaps
 //                the count kernel.  It then waits for the tile counts, derives
 //                for every bucket the routes in earlier tiles and the total
-//                (the exclusive scan, done redundantly by every CTA from a
-//                shared-memory copy of the count matrix), seeds per-warp
+//                (the exclusive scan, done redundantly by every CTA with warp
+//                reductions over the count matrix in L2), seeds per-warp
 //                counters with a scan across its warps, and walks its routes
 //                again to write row_id_map and sorted_to_flat.  CTA 0 writes
 //                counts and offsets.
-// When the count matrix is too large for shared memory, a single-CTA
+// When the count matrix is large (every rank CTA would read too much), a single-CTA
 // k_map_scan turns it into bases first and k_map_rank reads them (3 launches).
 // No atomics whose order reaches the result: the map is deterministic.
 #include <mutex>
@@ -50,7 +50,7 @@ constexpr int MAP_GROUP = MAP_CHUNKS * 32;             // 256 routes per warp gr
 constexpr int MAP_SUB = MAP_WARPS * MAP_GROUP;         // 2048 routes: a tile with f = 1
 constexpr int MAP_TARGET_TILES = 64;
 constexpr int MAP_MAX_F = 8;
-constexpr int64_t MAP_FUSED_MAX_COUNTS = 32768;        // count matrix held in shared memory
+constexpr int64_t MAP_FUSED_MAX_COUNTS = 32768;        // count matrix each rank CTA reads
 constexpr int SCAN_THREADS = 1024;
 constexpr int SCAN_ITEMS = 8;                          // per thread and pass
 constexpr int SCAN_PASS = SCAN_THREADS * SCAN_ITEMS;
@@ -258,7 +258,8 @@ __device__ int32_t cta_exclusive_scan(int32_t *a, int n, int32_t *s_warp)
 inline size_t rank_smem(int E, int64_t ntiles, bool fused)
 {
     size_t words = (size_t)(MAP_WARPS + 1) * (E + 1) + MAP_WARPS;
-    if (fused) words += (size_t)(E + 1) + (size_t)(E + 1) * ntiles;
+    if (fused) words += (size_t)(E + 1);
+    (void)ntiles;
     return words * sizeof(int32_t);
 }
 
@@ -275,7 +276,6 @@ __global__ void __launch_bounds__(MAP_THREADS)
     int32_t *s_base = s_cnt + MAP_WARPS * stride;     // [E+1] first row of each bucket here
     int32_t *s_warp = s_base + stride;                // [MAP_WARPS]
     int32_t *s_tot = s_warp + MAP_WARPS;              // [E+1] bucket totals (FUSED)
-    int32_t *s_mat = s_tot + stride;                  // [ntiles][E+1] counts (FUSED)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tile = blockIdx.x;
     int32_t *mine = s_cnt + warp * stride;
@@ -299,24 +299,39 @@ __global__ void __launch_bounds__(MAP_THREADS)
     griddep_wait();   // the tile counts of every tile are complete from here on
 
     if (FUSED) {
-        // Copy the expert-major count matrix, transposed to tile-major so the
-        // per-bucket sums below read consecutive words.
-        const int M = stride * ntiles;
-        for (int j = tid; j < M; j += MAP_THREADS) {
-            const int b = j / ntiles, t = j - b * ntiles;
-            s_mat[t * stride + b] = tile_counts[j];
-        }
-        __syncthreads();
-        for (int b = tid; b <= E; b += MAP_THREADS) {
-            int32_t tot = 0, pre = 0;
-            for (int t = 0; t < ntiles; ++t) {
-                const int32_t v = s_mat[t * stride + b];
-                tot += v;
-                pre += (t < tile) ? v : 0;
+        // Warp w sums buckets w, w+8, ...: its lanes read the bucket's row of
+        // the expert-major count matrix (consecutive tiles, coalesced) and
+        // two warp reductions give the bucket's total and the routes of
+        // earlier tiles.  Eight buckets are read before any is reduced.
+        constexpr int BU = 8;
+        for (int b0 = warp; b0 <= E; b0 += MAP_WARPS * BU) {
+            int32_t v0[BU], v1[BU];
+#pragma unroll
+            for (int u = 0; u < BU; ++u) {
+                const int b = b0 + u * MAP_WARPS;
+                const int32_t *row = tile_counts + (int64_t)b * ntiles;
+                v0[u] = (b <= E && lane < ntiles) ? row[lane] : 0;
+                v1[u] = (b <= E && lane + 32 < ntiles) ? row[lane + 32] : 0;
             }
-            s_tot[b] = tot;
-            s_base[b] = pre;
-            if (tile == 0 && b < E) counts[b] = tot;
+#pragma unroll
+            for (int u = 0; u < BU; ++u) {
+                const int b = b0 + u * MAP_WARPS;
+                int32_t tot = v0[u] + v1[u];
+                int32_t pre = (lane < tile ? v0[u] : 0) + (lane + 32 < tile ? v1[u] : 0);
+                if (b <= E)
+                    for (int t = lane + 64; t < ntiles; t += 32) {   // more than 64 tiles
+                        const int32_t v = tile_counts[(int64_t)b * ntiles + t];
+                        tot += v;
+                        pre += (t < tile) ? v : 0;
+                    }
+                const int32_t T_ = __reduce_add_sync(FULL_MASK, tot);
+                const int32_t P_ = __reduce_add_sync(FULL_MASK, pre);
+                if (lane == 0 && b <= E) {
+                    s_tot[b] = T_;
+                    s_base[b] = P_;
+                    if (tile == 0 && b < E) counts[b] = T_;
+                }
+            }
         }
         __syncthreads();
         cta_exclusive_scan(s_tot, stride, s_warp);   // s_tot: offsets of the buckets
