@@ -49,7 +49,11 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture, keyed by op; valid only while the kernel source that was
 # profiled is unchanged (sha256 prefix of the .cu file).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # one-pass capture of the full bench workload (dram__bytes_read.sum 1,209,081,600
+    # + dram__bytes_write.sum 1,014,064,896); profiles/traffic_skewed_T16384_row_kernels.md
+    "unpermute_bwd": {"bytes": 2223146496, "src": "61e7a019030b1a1a"},
+}
 
 
 # --------------------------------------------------------------------------
