@@ -166,6 +166,34 @@ def dist_env():
 
 
 # --------------------------------------------------------------------------
+# data-parallel bookkeeping (one rank per GPU; every rank runs the whole path
+# on its own token batch, so the only cross-rank traffic is timing)
+# --------------------------------------------------------------------------
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Seed of rank `rank`'s token batch: independent batches, same distribution."""
+    return base_seed + 7919 * rank
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's time (a MAX all-reduce); the value itself at world 1."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: int, world: int, ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank moved per step over the slowest
+    rank's step time (weak scaling)."""
+    return world * bytes_per_rank_step / (ms * 1e-3) / 1e9
+
+
+# --------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline and --impl reference)
 # --------------------------------------------------------------------------
 
@@ -218,7 +246,7 @@ def run_gpu(args):
             dist.barrier()
 
     # ---- routed workload: per-rank batch (weak scaling), seeded per rank
-    base_seed = wl.ROUTED[WORKLOAD]["seed"] + 7919 * rank
+    base_seed = rank_seed(wl.ROUTED[WORKLOAD]["seed"], rank)
     w = wl.routed(WORKLOAD, T=args.tokens, seed=base_seed)
     T, H, E, K = w["T"], w["H"], w["E"], w["K"]
     R = T * K
@@ -299,13 +327,10 @@ def run_gpu(args):
             per_op[op] += e[j].elapsed_time(e[j + 1])
     ms = sum(step_ms) / len(step_ms)
     per_op = {op: v / args.steps for op, v in per_op.items()}
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     peak, peak_kind = measured_peaks()
-    gbs = world * step_bytes / (ms * 1e-3) / 1e9
+    gbs = job_throughput(step_bytes, world, ms)
     dom = max(ops, key=lambda o: per_op[o])
     dom_src = {"build_map": "map.cu"}.get(dom, "rows.cu")
     traffic = None
@@ -347,10 +372,7 @@ def run_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     barrier()
 
     # ---- chunk sort+pad roundtrip (context: the pages' only published timing)
@@ -379,7 +401,7 @@ def run_gpu(args):
                      "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": nbytes[dom]},
-        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(job_throughput(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": sum(launches.values()) * args.steps,
