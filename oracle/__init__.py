@@ -57,6 +57,8 @@ def _load():
         lib.orc_bf16_from_f32.restype = ctypes.c_uint16
         lib.orc_build_map.argtypes = [P, i64, i32, i32, P, P, P, P]
         lib.orc_build_map.restype = i64
+        lib.orc_build_map_capacity.argtypes = [P, i64, i32, i32, i32, P, P, P, P]
+        lib.orc_build_map_capacity.restype = i64
         lib.orc_permute.argtypes = [P, P, P, i64, i32, i32, P, P]
         lib.orc_permute.restype = None
         lib.orc_unpermute.argtypes = [P, P, P, i64, i32, i32, P]
@@ -123,6 +125,20 @@ def build_map(idx: np.ndarray, E: int):
     offsets = np.empty(E + 1, np.int32)
     bad = lib.orc_build_map(_p(idx), T, K, E, _p(row_id_map), _p(s2f), _p(counts),
                             _p(offsets))
+    return row_id_map, s2f, counts, offsets, int(bad)
+
+
+def build_map_capacity(idx: np.ndarray, E: int, capacity: int):
+    """build_map keeping at most `capacity` routes per expert (earliest first)."""
+    lib = _load()
+    idx = _c(idx, np.int32)
+    T, K = idx.shape
+    row_id_map = np.empty((T, K), np.int32)
+    s2f = np.empty(T * K, np.int32)
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    bad = lib.orc_build_map_capacity(_p(idx), T, K, E, capacity, _p(row_id_map), _p(s2f),
+                                     _p(counts), _p(offsets))
     return row_id_map, s2f, counts, offsets, int(bad)
 
 

@@ -141,6 +141,61 @@ int64_t orc_build_map(const int32_t *idx, int64_t T, int32_t K, int32_t E,
     return bad;
 }
 
+/*
+ * Counting sort with an expert capacity: expert e keeps at most `capacity`
+ * routes, the first ones in flat (t,k) order; the others are dropped like
+ * empty slots (row_id_map = -1).  counts[e] is the number kept, offsets its
+ * exclusive scan, so offsets[E] is the number of rows the permuted tensor
+ * holds -- the "effective output token count, ... tokens not dropped" of
+ * num_out_tokens [d9d, moe_permute_with_probs].  capacity < 0: no limit.
+ * sorted_to_flat: t*K+k for kept rows, -1 from offsets[E] on.
+ * Returns the number of idx entries outside [-1, E).
+ */
+int64_t orc_build_map_capacity(const int32_t *idx, int64_t T, int32_t K, int32_t E,
+                               int32_t capacity, int32_t *row_id_map,
+                               int32_t *sorted_to_flat, int32_t *counts, int32_t *offsets)
+{
+    const int64_t n = T * (int64_t)K;
+    int64_t bad = 0;
+    for (int32_t e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int e = orc_expert_of(idx, i, E);
+        if (e >= 0) {
+            if (capacity < 0 || counts[e] < capacity)
+                counts[e] += 1;
+        } else if (idx[i] != -1) {
+            bad += 1;
+        }
+    }
+    offsets[0] = 0;
+    for (int32_t e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+    for (int64_t i = 0; i < n; ++i)
+        row_id_map[i] = -1;
+    if (sorted_to_flat)
+        for (int64_t i = 0; i < n; ++i)
+            sorted_to_flat[i] = -1;
+    for (int32_t e = 0; e < E; ++e) {
+        int32_t taken = 0;
+        for (int64_t t = 0; t < T; ++t) {
+            for (int32_t k = 0; k < K; ++k) {
+                int64_t i = t * K + k;
+                if (orc_expert_of(idx, i, E) != e)
+                    continue;
+                if (capacity < 0 || taken < capacity) {
+                    int32_t row = offsets[e] + taken;
+                    row_id_map[i] = row;
+                    if (sorted_to_flat)
+                        sorted_to_flat[row] = (int32_t)i;
+                }
+                taken += 1;
+            }
+        }
+    }
+    return bad;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Permute / unpermute                                                       */
 /* ------------------------------------------------------------------------ */

@@ -474,3 +474,54 @@ def test_sort_pad_flags():
     *_, fl = oracle.sort_chunks_pad(x, p, np.array([3, 3], np.int32),
                                     np.array([0, 9], np.int32), 1, 1, 6)
     assert fl["bad_order"] == 1
+
+
+# --------------------------------------------------------------------------
+# expert capacity (token dropping)
+# --------------------------------------------------------------------------
+
+def _brute_capacity(idx, E, cap):
+    T, K = idx.shape
+    keys = sorted((int(idx[t, k]), t, k) for t in range(T) for k in range(K)
+                  if 0 <= idx[t, k] < E)
+    kept, seen = [], {}
+    for e, t, k in keys:
+        seen[e] = seen.get(e, 0) + 1
+        if cap < 0 or seen[e] <= cap:
+            kept.append((e, t, k))
+    rim = -np.ones((T, K), np.int32)
+    s2f = -np.ones(T * K, np.int32)
+    for row, (e, t, k) in enumerate(kept):
+        rim[t, k] = row
+        s2f[row] = t * K + k
+    counts = np.array([sum(1 for key in kept if key[0] == e) for e in range(E)], np.int32)
+    return rim, s2f, counts, np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_build_map_capacity_brute_force(seed):
+    rng = np.random.default_rng(500 + seed)
+    T, K, E = int(rng.integers(0, 14)), int(rng.integers(1, 5)), int(rng.integers(1, 6))
+    cap = int(rng.integers(-1, 6))
+    idx = rng.integers(-1, E, size=(T, K)).astype(np.int32)
+    got = oracle.build_map_capacity(idx, E, cap)
+    for a, b in zip(got[:4], _brute_capacity(idx, E, cap)):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_build_map_capacity_limits_reduce_to_plain_map():
+    idx, _, _ = _case(3, 40, 4, 7, 1)
+    plain = oracle.build_map(idx, 7)
+    for cap in (-1, 160, 10**6):
+        for a, b in zip(oracle.build_map_capacity(idx, 7, cap)[:4], plain[:4]):
+            np.testing.assert_array_equal(a, b)
+    rim, s2f, counts, offsets, _ = oracle.build_map_capacity(idx, 7, 0)
+    assert np.all(rim == -1) and np.all(s2f == -1) and offsets[-1] == 0
+
+
+def test_build_map_capacity_keeps_the_earliest_tokens():
+    idx = np.array([[0, 1], [0, 2], [0, 1], [1, 0]], np.int32)
+    rim, s2f, counts, offsets, _ = oracle.build_map_capacity(idx, 3, 2)
+    np.testing.assert_array_equal(counts, [2, 2, 1])
+    np.testing.assert_array_equal(rim, [[0, 2], [1, 4], [-1, 3], [-1, -1]])
+    np.testing.assert_array_equal(s2f, [0, 2, 1, 5, 3, -1, -1, -1])
