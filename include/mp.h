@@ -112,6 +112,22 @@ mp_status_t mp_build_map(const int32_t *idx, int64_t T, int32_t K, int32_t E,
                          int32_t *dev_status, mp_stream_t stream);
 
 /*
+ * mp_build_map with an expert capacity (token dropping).  Expert e keeps at
+ * most `capacity` routes -- the first ones in (token, slot) order -- and the
+ * others are dropped like empty slots (row_id_map = -1).  counts[e] is the
+ * number kept and offsets its exclusive scan, so offsets[E] is the effective
+ * output row count, the "num_out_tokens" of [d9d moe_permute_with_probs]
+ * ("the number of tokens not dropped"); sorted_to_flat is -1 from offsets[E]
+ * on.  capacity < 0 means no limit (the same result as mp_build_map).  Other
+ * arguments, workspace and errors as mp_build_map.
+ */
+mp_status_t mp_build_map_capacity(const int32_t *idx, int64_t T, int32_t K, int32_t E,
+                                  int32_t capacity, int32_t *row_id_map,
+                                  int32_t *sorted_to_flat, int32_t *counts, int32_t *offsets,
+                                  void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                  mp_stream_t stream);
+
+/*
  * Allocation-free mp_build_map.  The pages have no counterpart: this entry
  * point exists for callers that cannot call cudaMalloc -- an inference
  * runtime or plugin that plans all device memory at start-up and forbids

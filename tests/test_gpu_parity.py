@@ -301,3 +301,46 @@ def test_full_size_sampled(name):
     g_x, _ = mp.mp_permute_bwd(rows, rim)
     o_gx, _ = oracle.permute_bwd(rows_s, None, local, len(sample), H)
     np.testing.assert_array_equal(h(g_x)[sample], o_gx)
+
+
+# --------------------------------------------------------------------------
+# expert capacity (token dropping)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,T,cap", [
+    ("skewed", None, 1024),       # hot experts overflow, cold ones keep all
+    ("skewed", 3000, 0),          # everything dropped
+    ("mid", None, 300),
+    ("large", None, 700),         # 2 sub-tiles per tile
+    ("mid", 2000, -1),            # no limit: the plain map
+])
+def test_build_map_capacity(name, T, cap):
+    idx, probs, E = wl.routing(name, T=T)
+    st = status_word()
+    got = mp.mp_build_map_capacity(d(idx), E, cap, status=st)
+    want = oracle.build_map_capacity(idx, E, cap)
+    for a, b in zip(got, want[:4]):
+        np.testing.assert_array_equal(h(a), b)
+    assert int(h(st)[0]) == 0
+    if cap >= 0:
+        assert h(got[2]).max(initial=0) <= cap
+
+
+def test_build_map_capacity_three_launch_path_and_dropped_rows_downstream():
+    rng = np.random.default_rng(12)
+    T, K, E, H = 25600, 8, 1024, 64               # count matrix above the fused limit
+    idx = rng.integers(-1, E, size=(T, K)).astype(np.int32)
+    idx[:, 0] = 3                                   # one very hot expert
+    got = mp.mp_build_map_capacity(d(idx), E, 5000)
+    want = oracle.build_map_capacity(idx, E, 5000)
+    for a, b in zip(got, want[:4]):
+        np.testing.assert_array_equal(h(a), b)
+    # dropped slots behave as empty slots in the row ops
+    x = wl.random_rows(T, H, 3)
+    probs = rng.random((T, K)).astype(np.float32)
+    R = int(want[3][-1])
+    out, _ = mp.mp_permute(d(x), got[0], d(probs), num_out_rows=R)
+    o_out, _ = oracle.permute(x, probs, want[0], out_rows=R)
+    np.testing.assert_array_equal(h(out), o_out)
+    y = mp.mp_unpermute(out, got[0], d(probs))
+    np.testing.assert_array_equal(h(y), oracle.unpermute(o_out, probs, want[0], T, H))

@@ -18,7 +18,8 @@ import torch
 from . import _lib
 
 __all__ = [
-    "MPError", "mp_build_map", "mp_build_map_workspace_size", "mp_permute", "mp_unpermute",
+    "MPError", "mp_build_map", "mp_build_map_capacity", "mp_build_map_workspace_size",
+    "mp_permute", "mp_unpermute",
     "mp_permute_bwd", "mp_unpermute_bwd", "mp_sort_chunks_pad", "mp_unpad_restore",
     "mp_sort_chunks_pad_bwd", "mp_unpad_restore_bwd", "status_bits", "library_path",
 ]
@@ -102,6 +103,23 @@ def mp_build_map(idx, num_experts: int, *, with_sorted_to_flat: bool = True,
                  workspace=None, status=None):
     """idx int32 [T,K] (-1 = empty slot) -> (row_id_map [T,K], sorted_to_flat [T*K]
     or None, counts [E], offsets [E+1]), all int32 on idx's device."""
+    return _build_map("mp_build_map", idx, num_experts, None, with_sorted_to_flat, row_id_map,
+                      sorted_to_flat, counts, offsets, workspace, status)
+
+
+def mp_build_map_capacity(idx, num_experts: int, capacity: int, *,
+                          with_sorted_to_flat: bool = True, row_id_map=None,
+                          sorted_to_flat=None, counts=None, offsets=None, workspace=None,
+                          status=None):
+    """mp_build_map keeping at most `capacity` routes per expert (the earliest in
+    token, slot order); dropped routes get row -1 and offsets[E] is the row count."""
+    return _build_map("mp_build_map_capacity", idx, num_experts, int(capacity),
+                      with_sorted_to_flat, row_id_map, sorted_to_flat, counts, offsets,
+                      workspace, status)
+
+
+def _build_map(fn, idx, num_experts, capacity, with_sorted_to_flat, row_id_map, sorted_to_flat,
+               counts, offsets, workspace, status):
     lib = _lib.load()
     _need(idx, "idx", torch.int32, 2)
     dev = idx.device
@@ -128,9 +146,16 @@ def mp_build_map(idx, num_experts: int, *, with_sorted_to_flat: bool = True,
         _need(workspace, "workspace", torch.uint8, 1, dev)
     _opt(status, "status", torch.int32, 1, dev)
     with torch.cuda.device(dev):
-        _check("mp_build_map", lib.mp_build_map(
-            _ptr(idx), T, K, E, _ptr(row_id_map), _ptr(sorted_to_flat), _ptr(counts),
-            _ptr(offsets), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev)))
+        if capacity is None:
+            code = lib.mp_build_map(
+                _ptr(idx), T, K, E, _ptr(row_id_map), _ptr(sorted_to_flat), _ptr(counts),
+                _ptr(offsets), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
+        else:
+            code = lib.mp_build_map_capacity(
+                _ptr(idx), T, K, E, capacity, _ptr(row_id_map), _ptr(sorted_to_flat),
+                _ptr(counts), _ptr(offsets), _ptr(workspace), workspace.numel(), _ptr(status),
+                _stream(dev))
+        _check(fn, code)
     return row_id_map, sorted_to_flat, counts, offsets
 
 

@@ -19,6 +19,7 @@ SIGNATURES = {
     "mp_last_cuda_error": (I32, []),
     "mp_build_map_workspace_size": (SZ, [I64, I32, I32]),
     "mp_build_map": (I32, [P, I64, I32, I32, P, P, P, P, P, SZ, P, P]),
+    "mp_build_map_capacity": (I32, [P, I64, I32, I32, I32, P, P, P, P, P, SZ, P, P]),
     "mp_build_map_noalloc": (I32, [P, I64, I32, I32, P, P, P, P, P, P]),
     "mp_permute": (I32, [P, P, P, I64, I32, I32, P, P, P]),
     "mp_unpermute": (I32, [P, P, P, I64, I32, I32, P, P]),

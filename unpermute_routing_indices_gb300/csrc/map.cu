@@ -24,8 +24,9 @@
 //                (the exclusive scan, done redundantly by every CTA with warp
 //                reductions over the count matrix in L2), seeds per-warp
 //                counters with a scan across its warps, and walks its routes
-//                again to write row_id_map and sorted_to_flat.  CTA 0 writes
-//                counts and offsets.
+//                again: a route's rank within its expert, below the expert's
+//                capacity, gives row = offsets[e] + rank, else the route is
+//                dropped (-1).  CTA 0 writes counts and offsets.
 // When the count matrix is large (every rank CTA would read too much), a single-CTA
 // k_map_scan turns it into bases first and k_map_rank reads them (3 launches).
 // No atomics whose order reaches the result: the map is deterministic.
@@ -143,10 +144,13 @@ __global__ void __launch_bounds__(MAP_THREADS)
 __device__ __forceinline__ int spad(int i) { return i + (i >> 5); }
 
 // Single-CTA exclusive scan of the expert-major count matrix (3-launch path,
-// and the T == 0 case where it only writes zero counts and offsets).
+// and the T == 0 case where it only writes zero counts and offsets).  Entry
+// [b][tile] becomes the routes of buckets before b plus the bucket-b routes of
+// earlier tiles; counts / offsets get the capacity-capped expert totals and
+// their exclusive scan.
 __global__ void __launch_bounds__(SCAN_THREADS)
-    k_map_scan(int32_t *__restrict__ tile_counts, int E, int ntiles, int32_t *__restrict__ counts,
-               int32_t *__restrict__ offsets)
+    k_map_scan(int32_t *__restrict__ tile_counts, int E, int ntiles, int cap,
+               int32_t *__restrict__ counts, int32_t *__restrict__ offsets)
 {
     __shared__ int32_t s_val[SCAN_PASS + SCAN_PASS / 32];
     __shared__ int32_t s_warp[SCAN_THREADS / 32];
@@ -208,14 +212,36 @@ __global__ void __launch_bounds__(SCAN_THREADS)
         __syncthreads();
     }
 
-    for (int e = tid; e <= E; e += SCAN_THREADS) {
-        const int32_t start = ntiles > 0 ? tile_counts[(int64_t)e * ntiles] : 0;
-        offsets[e] = start;
-        if (e < E) {
-            const int32_t next = ntiles > 0 ? tile_counts[(int64_t)(e + 1) * ntiles] : 0;
-            counts[e] = next - start;
-        }
+    // Capped expert totals (one expert per thread, E <= 1024) and their scan.
+    int32_t c = 0;
+    if (tid < E && ntiles > 0) {
+        const int32_t start = tile_counts[(int64_t)tid * ntiles];
+        const int32_t next = tile_counts[(int64_t)(tid + 1) * ntiles];
+        c = min(next - start, cap);
     }
+    if (tid < E) counts[tid] = c;
+    int32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int32_t w = s_warp[lane];
+        int32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(FULL_MASK, wi, o);
+            if (lane >= o) wi += y;
+        }
+        s_warp[lane] = wi - w;
+    }
+    __syncthreads();
+    const int32_t excl = s_warp[warp] + incl - c;
+    if (tid < E) offsets[tid] = excl;
+    if (tid == SCAN_THREADS - 1) offsets[E] = excl + c;
 }
 
 // In-place exclusive scan of a[0..n), n <= 5 * MAP_THREADS, in shared memory;
@@ -255,17 +281,11 @@ __device__ int32_t cta_exclusive_scan(int32_t *a, int n, int32_t *s_warp)
     return total;
 }
 
-inline size_t rank_smem(int E, int64_t ntiles, bool fused)
-{
-    size_t words = (size_t)(MAP_WARPS + 1) * (E + 1) + MAP_WARPS;
-    if (fused) words += (size_t)(E + 1);
-    (void)ntiles;
-    return words * sizeof(int32_t);
-}
+inline size_t rank_smem(int E) { return ((size_t)(MAP_WARPS + 2) * (E + 1) + MAP_WARPS) * sizeof(int32_t); }
 
 template <bool FUSED>
 __global__ void __launch_bounds__(MAP_THREADS)
-    k_map_rank(const int32_t *__restrict__ idx, int64_t n, int E, int f, int ntiles,
+    k_map_rank(const int32_t *__restrict__ idx, int64_t n, int E, int f, int ntiles, int cap,
                const int32_t *__restrict__ tile_counts, int32_t *__restrict__ row_id_map,
                int32_t *__restrict__ sorted_to_flat, int32_t *__restrict__ counts,
                int32_t *__restrict__ offsets)
@@ -273,9 +293,9 @@ __global__ void __launch_bounds__(MAP_THREADS)
     extern __shared__ int32_t sm[];
     const int stride = E + 1;
     int32_t *s_cnt = sm;                              // [MAP_WARPS][E+1] per-warp counters
-    int32_t *s_base = s_cnt + MAP_WARPS * stride;     // [E+1] first row of each bucket here
+    int32_t *s_base = s_cnt + MAP_WARPS * stride;     // [E+1] bucket routes in earlier tiles
     int32_t *s_warp = s_base + stride;                // [MAP_WARPS]
-    int32_t *s_tot = s_warp + MAP_WARPS;              // [E+1] bucket totals (FUSED)
+    int32_t *s_off = s_warp + MAP_WARPS;              // [E+1] first row of each expert
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tile = blockIdx.x;
     int32_t *mine = s_cnt + warp * stride;
@@ -298,6 +318,7 @@ __global__ void __launch_bounds__(MAP_THREADS)
 
     griddep_wait();   // the tile counts of every tile are complete from here on
 
+    int32_t kept;     // rows of the permuted tensor (routes kept), offsets[E]
     if (FUSED) {
         // Warp w sums buckets w, w+8, ...: its lanes read the bucket's row of
         // the expert-major count matrix (consecutive tiles, coalesced) and
@@ -327,24 +348,27 @@ __global__ void __launch_bounds__(MAP_THREADS)
                 const int32_t T_ = __reduce_add_sync(FULL_MASK, tot);
                 const int32_t P_ = __reduce_add_sync(FULL_MASK, pre);
                 if (lane == 0 && b <= E) {
-                    s_tot[b] = T_;
+                    s_off[b] = (b < E) ? min(T_, cap) : 0;   // rows the expert keeps
                     s_base[b] = P_;
-                    if (tile == 0 && b < E) counts[b] = T_;
+                    if (tile == 0 && b < E) counts[b] = min(T_, cap);
                 }
             }
         }
         __syncthreads();
-        cta_exclusive_scan(s_tot, stride, s_warp);   // s_tot: offsets of the buckets
-        for (int b = tid; b <= E; b += MAP_THREADS) {
-            s_base[b] += s_tot[b];
-            if (tile == 0) offsets[b] = s_tot[b];
-        }
+        kept = cta_exclusive_scan(s_off, stride, s_warp);  // s_off: first row of each expert
+        if (tile == 0)
+            for (int b = tid; b <= E; b += MAP_THREADS) offsets[b] = s_off[b];
     } else {
-        for (int b = tid; b <= E; b += MAP_THREADS) s_base[b] = tile_counts[(int64_t)b * ntiles + tile];
+        for (int b = tid; b <= E; b += MAP_THREADS) {
+            s_base[b] = tile_counts[(int64_t)b * ntiles + tile] - tile_counts[(int64_t)b * ntiles];
+            s_off[b] = offsets[b];
+        }
+        kept = offsets[E];
     }
     __syncthreads();
 
-    // Per bucket: exclusive scan over the warps, seeded with the tile's base row.
+    // Per bucket: exclusive scan over the warps, seeded with the routes of the
+    // bucket in earlier tiles, so the counters hold ranks within the expert.
     for (int b = tid; b <= E; b += MAP_THREADS) {
         int32_t run = s_base[b];
 #pragma unroll
@@ -365,18 +389,28 @@ __global__ void __launch_bounds__(MAP_THREADS)
         for (int c = 0; c < MAP_CHUNKS; ++c) {
             const int b = bk[c];
             const unsigned peers = __match_any_sync(FULL_MASK, b);
-            int32_t row = 0;
-            if (b >= 0) row = mine[b] + __popc(peers & lt);
+            int32_t rank = 0;
+            if (b >= 0) rank = mine[b] + __popc(peers & lt);
             __syncwarp();
             if (b >= 0 && lane == __ffs(peers) - 1) mine[b] += __popc(peers);
             __syncwarp();
             if (b >= 0) {
                 const int64_t i = gbase + c * 32 + lane;
-                const bool routed = b < E;
-                row_id_map[i] = routed ? row : -1;
-                if (sorted_to_flat != nullptr) sorted_to_flat[row] = routed ? (int32_t)i : -1;
+                const bool keep = b < E && rank < cap;
+                const int32_t row = keep ? s_off[b] + rank : -1;
+                row_id_map[i] = row;
+                if (keep && sorted_to_flat != nullptr) sorted_to_flat[row] = (int32_t)i;
             }
         }
+    }
+
+    // Rows past the kept ones hold no route: each CTA clears a share.
+    if (sorted_to_flat != nullptr) {
+        const int64_t tail = n - kept;
+        const int64_t per = (tail + ntiles - 1) / ntiles;
+        const int64_t lo = kept + (int64_t)tile * per;
+        const int64_t hi = min(n, lo + per);
+        for (int64_t i = lo + tid; i < hi; i += MAP_THREADS) sorted_to_flat[i] = -1;
     }
 }
 
@@ -393,19 +427,19 @@ inline size_t map_workspace_bytes(int64_t n, int E)
 }
 
 // Enqueues the map kernels; tile_counts holds (E+1) * plan.ntiles words.
-mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int32_t *row_id_map,
+mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *row_id_map,
                        int32_t *sorted_to_flat, int32_t *counts, int32_t *offsets,
                        int32_t *tile_counts, int32_t *dev_status, cudaStream_t s)
 {
     const MapPlan p = map_plan(n, E);
     if (p.ntiles == 0) {
-        k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, 0, counts, offsets);
+        k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, 0, cap, counts, offsets);
         return check_launch();
     }
     const unsigned grid = (unsigned)p.ntiles;
     k_map_count<<<grid, MAP_THREADS, (E + 1) * sizeof(int32_t), s>>>(idx, n, E, p.f, (int)p.ntiles,
                                                                      tile_counts, dev_status);
-    const size_t smem = rank_smem(E, p.ntiles, p.fused);
+    const size_t smem = rank_smem(E);
     cudaError_t err = cudaSuccess;
     if (p.fused) {
         if (smem > 48 * 1024)
@@ -422,15 +456,15 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int32_t *row_id_map
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            err = cudaLaunchKernelEx(&cfg, k_map_rank<true>, idx, n, E, p.f, (int)p.ntiles,
+            err = cudaLaunchKernelEx(&cfg, k_map_rank<true>, idx, n, E, p.f, (int)p.ntiles, cap,
                                      (const int32_t *)tile_counts, row_id_map, sorted_to_flat,
                                      counts, offsets);
         }
     } else {
-        k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)p.ntiles, counts, offsets);
-        k_map_rank<false><<<grid, MAP_THREADS, smem, s>>>(idx, n, E, p.f, (int)p.ntiles, tile_counts,
-                                                          row_id_map, sorted_to_flat, counts,
-                                                          offsets);
+        k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)p.ntiles, cap, counts, offsets);
+        k_map_rank<false><<<grid, MAP_THREADS, smem, s>>>(idx, n, E, p.f, (int)p.ntiles, cap,
+                                                          tile_counts, row_id_map, sorted_to_flat,
+                                                          counts, offsets);
     }
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -481,8 +515,30 @@ extern "C" mp_status_t mp_build_map(const int32_t *idx, int64_t T, int32_t K, in
             (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
             return MP_ERR_WORKSPACE;
     }
-    return launch_map(idx, n, E, row_id_map, sorted_to_flat, counts, offsets,
+    return launch_map(idx, n, E, INT32_MAX, row_id_map, sorted_to_flat, counts, offsets,
                       static_cast<int32_t *>(workspace), dev_status, as_stream(stream));
+}
+
+extern "C" mp_status_t mp_build_map_capacity(const int32_t *idx, int64_t T, int32_t K, int32_t E,
+                                             int32_t capacity, int32_t *row_id_map,
+                                             int32_t *sorted_to_flat, int32_t *counts,
+                                             int32_t *offsets, void *workspace,
+                                             size_t workspace_bytes, int32_t *dev_status,
+                                             mp_stream_t stream)
+{
+    if (T < 0 || K < 1 || E < 1) return MP_ERR_INVALID_ARG;
+    if (!map_sizes_ok(T, K, E)) return MP_ERR_UNSUPPORTED;
+    if (counts == nullptr || offsets == nullptr) return MP_ERR_INVALID_ARG;
+    const int64_t n = T * (int64_t)K;
+    if (n > 0 && (idx == nullptr || row_id_map == nullptr)) return MP_ERR_INVALID_ARG;
+    if (n > 0) {
+        if (workspace == nullptr || workspace_bytes < map_workspace_bytes(n, E) ||
+            (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+            return MP_ERR_WORKSPACE;
+    }
+    return launch_map(idx, n, E, capacity < 0 ? INT32_MAX : capacity, row_id_map, sorted_to_flat,
+                      counts, offsets, static_cast<int32_t *>(workspace), dev_status,
+                      as_stream(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -547,6 +603,6 @@ extern "C" mp_status_t mp_build_map_noalloc(const int32_t *idx, int64_t T, int32
     if (st != MP_OK) return st;
     // Every tile count the rank (and scan) kernels read is first written by
     // k_map_count in this call, so the array needs no clearing.
-    return launch_map(idx, n, E, row_id_map, sorted_to_flat, counts, offsets, tile_counts,
-                      dev_status, as_stream(stream));
+    return launch_map(idx, n, E, INT32_MAX, row_id_map, sorted_to_flat, counts, offsets,
+                      tile_counts, dev_status, as_stream(stream));
 }
