@@ -59,6 +59,10 @@ def _load():
         lib.orc_build_map.restype = i64
         lib.orc_build_map_capacity.argtypes = [P, i64, i32, i32, i32, P, P, P, P]
         lib.orc_build_map_capacity.restype = i64
+        lib.orc_bf16_from_f64.argtypes = [ctypes.c_double]
+        lib.orc_bf16_from_f64.restype = ctypes.c_uint16
+        lib.orc_unpermute_ep.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P]
+        lib.orc_unpermute_ep.restype = None
         lib.orc_permute.argtypes = [P, P, P, i64, i32, i32, P, P]
         lib.orc_permute.restype = None
         lib.orc_unpermute.argtypes = [P, P, P, i64, i32, i32, P]
@@ -98,6 +102,15 @@ def bf16_from_f32(values) -> np.ndarray:
     lib = _load()
     v = np.asarray(values, dtype=np.float32).ravel()
     out = np.fromiter((lib.orc_bf16_from_f32(float(f)) for f in v), dtype=np.uint16,
+                      count=v.size)
+    return out.reshape(np.shape(values))
+
+
+def bf16_from_f64(values) -> np.ndarray:
+    """float64 array -> uint16 bf16 bits, one round-to-nearest-even."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float64).ravel()
+    out = np.fromiter((lib.orc_bf16_from_f64(float(f)) for f in v), dtype=np.uint16,
                       count=v.size)
     return out.reshape(np.shape(values))
 
@@ -169,6 +182,21 @@ def unpermute(rows, probs, row_id_map, T, H):
     K = row_id_map.shape[1]
     out = np.empty((T, H), np.uint16)
     lib.orc_unpermute(_p(rows), _p(probs), _p(row_id_map), T, K, H, _p(out))
+    return out
+
+
+def unpermute_ep(rows, probs, row_id_map, idx, T, H, E, ep_size, bf16_partials=False,
+                 fp64_cross_rank=False):
+    """Rank-ordered combine over ep_size ranks of E/ep_size experts each."""
+    lib = _load()
+    rows = _c(rows, np.uint16)
+    probs = _c(probs, np.float32)
+    row_id_map = _c(row_id_map, np.int32)
+    idx = _c(idx, np.int32)
+    K = row_id_map.shape[1]
+    out = np.empty((T, H), np.uint16)
+    lib.orc_unpermute_ep(_p(rows), _p(probs), _p(row_id_map), _p(idx), T, K, H, E, ep_size,
+                         int(bool(bf16_partials)), int(bool(fp64_cross_rank)), _p(out))
     return out
 
 

@@ -249,6 +249,84 @@ void orc_unpermute(const uint16_t *rows, const float *probs, const int32_t *row_
     }
 }
 
+/* fp64 -> bf16, round to nearest even, in one rounding (no detour through
+ * fp32): scale by the bf16 quantum at the value's binade (2^(e-7) for normal
+ * bf16, 2^-133 below 2^-126), round to an integer with rint() (ties to even in
+ * the default rounding mode), scale back -- all exact in double -- then read
+ * the result's bits through float, where it is exactly representable.
+ * Magnitudes that round past the largest finite bf16 become +-inf. */
+uint16_t orc_bf16_from_f64(double d)
+{
+    if (isnan(d))
+        return 0x7fc0u;
+    if (isinf(d) || d == 0.0) {
+        float f = (float)d;
+        uint32_t u;
+        memcpy(&u, &f, sizeof u);
+        return (uint16_t)(u >> 16);
+    }
+    double a = fabs(d);
+    int e2;
+    frexp(a, &e2);               /* a = m * 2^e2, m in [0.5, 1): binade exponent e2-1 */
+    int binade = e2 - 1;
+    if (binade < -126)
+        binade = -126;           /* bf16 subnormals share the quantum 2^-133 */
+    double q = ldexp(1.0, binade - 7);
+    double r = rint(a / q) * q;
+    const double max_bf16 = ldexp(255.0, 120);   /* (2 - 2^-7) * 2^127 */
+    uint16_t sign = d < 0 ? 0x8000u : 0;
+    if (r > max_bf16)
+        return (uint16_t)(sign | 0x7f80u);
+    float f = (float)r;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7fffu));
+}
+
+/* The rank-ordered combine of a token over EP ranks [MBI,
+ * _rank_tree_unpermute_kernel, unpermute_with_bf16_rank_partials, unpermute]:
+ * experts are split into ep_size ranks of E/ep_size consecutive experts.  Per
+ * element, for each rank r in order, the rank's partial is the slot-order
+ * chain of FP32 fused multiply-adds of prob and row over the token's routed
+ * slots whose expert lies on r, from +0 (plain adds without probs); with
+ * bf16_partials it is then quantized to BF16.  The partials are added in rank
+ * order from zero, in fp32, or in fp64 when fp64_cross_rank is set, and the
+ * sum is rounded once to BF16.  With ep_size = 1 and neither flag this is
+ * orc_unpermute.  idx[T,K] holds each slot's expert. */
+void orc_unpermute_ep(const uint16_t *rows, const float *probs, const int32_t *row_id_map,
+                      const int32_t *idx, int64_t T, int32_t K, int32_t H, int32_t E,
+                      int32_t ep_size, int32_t bf16_partials, int32_t fp64_cross_rank,
+                      uint16_t *out)
+{
+    const int32_t per_rank = E / ep_size;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t h = 0; h < H; ++h) {
+            float acc32 = 0.0f;
+            double acc64 = 0.0;
+            for (int32_t r = 0; r < ep_size; ++r) {
+                float partial = 0.0f;
+                for (int32_t k = 0; k < K; ++k) {
+                    int32_t row = row_id_map[t * K + k];
+                    if (row < 0 || idx[t * K + k] / per_rank != r)
+                        continue;
+                    float x = orc_f32_from_bf16(rows[(int64_t)row * H + h]);
+                    if (probs)
+                        partial = fmaf(probs[t * K + k], x, partial);
+                    else
+                        partial = partial + x;
+                }
+                if (bf16_partials)
+                    partial = orc_f32_from_bf16(orc_bf16_from_f32(partial));
+                if (fp64_cross_rank)
+                    acc64 = acc64 + (double)partial;
+                else
+                    acc32 = acc32 + partial;
+            }
+            out[t * H + h] = fp64_cross_rank ? orc_bf16_from_f64(acc64) : orc_bf16_from_f32(acc32);
+        }
+    }
+}
+
 /* Backward of permute [d9d, _moe_permute_mask_map.backward]: the permuted
  * gradient is unpermuted without merging probs (a sum over the token's rows,
  * fp32 from +0 in slot order, one bf16 rounding), and the permuted-probs

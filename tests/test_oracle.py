@@ -525,3 +525,79 @@ def test_build_map_capacity_keeps_the_earliest_tokens():
     np.testing.assert_array_equal(counts, [2, 2, 1])
     np.testing.assert_array_equal(rim, [[0, 2], [1, 4], [-1, 3], [-1, -1]])
     np.testing.assert_array_equal(s2f, [0, 2, 1, 5, 3, -1, -1, -1])
+
+
+# --------------------------------------------------------------------------
+# rank-ordered combine over EP ranks
+# --------------------------------------------------------------------------
+
+def test_bf16_from_f64_against_exact_rounding():
+    rng = random.Random(8)
+    vals = [0.0, -0.0, 1.0, 1.00390625, 1.01171875, -1.00390625, 2.0**-133, 2.0**-134,
+            3 * 2.0**-134, 2.0**-126 * (1 - 2.0**-9), 3.3895313892515355e38,
+            3.3961775292304e38, 3.4e38, 1e300, -1e300, 1e-300, 1.0 + 2.0**-8 + 2.0**-40]
+    vals += [rng.uniform(-1, 1) * 2.0 ** rng.randint(-140, 130) for _ in range(3000)]
+    got = oracle.bf16_from_f64(np.array(vals))
+    for v, g in zip(vals, got):
+        if v == 0:
+            want = 0x8000 if math.copysign(1, v) < 0 else 0
+        else:
+            want = exact.round_bf16_bits(exact.Fraction(v))
+        assert int(g) == want, (v, hex(int(g)), hex(want))
+
+
+def _ep_exact(rows, probs, rim, idx, T, H, E, ep, bf16p, fp64):
+    """The same tree with every rounding done exactly (fp32 via exact rounding,
+    fp64 sums via exact rational then round to binary64)."""
+    K = rim.shape[1]
+    per = E // ep
+    out = np.zeros((T, H), np.uint16)
+    for t in range(T):
+        for h in range(H):
+            acc = exact.Fraction(0)
+            accf = 0.0
+            for r in range(ep):
+                part = 0.0
+                for k in range(K):
+                    if rim[t, k] < 0 or idx[t, k] // per != r:
+                        continue
+                    x = _bf(rows[rim[t, k], h])
+                    p = 1.0 if probs is None else float(probs[t, k])
+                    part = exact.fma_f32(p, x, part)
+                if bf16p:
+                    part = float(exact.frac_of_bf16(exact.bf16_of_f32(part)))
+                if fp64:
+                    acc = exact.Fraction(float(acc + exact.Fraction(part)))  # binary64 add
+                else:
+                    accf = exact.fma_f32(1.0, part, accf)
+            if fp64:
+                out[t, h] = 0 if acc == 0 else exact.round_bf16_bits(acc)
+            else:
+                out[t, h] = exact.bf16_of_f32(accf)
+    return out
+
+
+@pytest.mark.parametrize("ep,bf16p,fp64", [(1, False, False), (2, True, False),
+                                            (4, False, True), (4, True, True), (8, True, False)])
+def test_unpermute_ep_exact_tree(ep, bf16p, fp64):
+    T, K, E, H = 6, 4, 8, 7
+    idx, probs, _ = _case(70 + ep, T, K, E, H, empty=True)
+    rng = np.random.default_rng(90 + ep)
+    rim, *_ = oracle.build_map(idx, E)
+    rows = _rand_bf16(rng, (T * K, H))
+    for p in (probs, None):
+        got = oracle.unpermute_ep(rows, p, rim, idx, T, H, E, ep, bf16p, fp64)
+        np.testing.assert_array_equal(got, _ep_exact(rows, p, rim, idx, T, H, E, ep, bf16p, fp64))
+
+
+def test_unpermute_ep_with_one_rank_is_unpermute():
+    T, K, E, H = 30, 4, 8, 16
+    idx, probs, _ = _case(77, T, K, E, H, empty=True)
+    rng = np.random.default_rng(78)
+    rim, *_ = oracle.build_map(idx, E)
+    rows = _rand_bf16(rng, (T * K, H))
+    np.testing.assert_array_equal(oracle.unpermute_ep(rows, probs, rim, idx, T, H, E, 1),
+                                  oracle.unpermute(rows, probs, rim, T, H))
+    # bf16 partials with one rank: bf16(bf16(x)) == bf16(x)
+    np.testing.assert_array_equal(oracle.unpermute_ep(rows, probs, rim, idx, T, H, E, 1, True),
+                                  oracle.unpermute(rows, probs, rim, T, H))
