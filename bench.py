@@ -380,6 +380,36 @@ def run_gpu(args):
     if rank == 0 and not args.no_chunks:
         sort_pad = bench_chunks(mp, wl, dev, flush, args)
 
+    # ---- the widened rows, on the same batch: capacity map, EP-rank combine
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        cap = -(-5 * routed // (4 * E))                   # capacity factor 1.25
+        ep = 8
+        ep_bytes = nbytes["unpermute"] + 4 * T * K        # + the slot experts
+        rim_c, s2f_c = torch.empty_like(rim), torch.empty_like(s2f)
+        counts_c, offsets_c = torch.empty_like(counts), torch.empty_like(offsets)
+        extra_ops = {
+            f"build_map_capacity(cap={cap})": (
+                lambda: mp.mp_build_map_capacity(idx, E, cap, row_id_map=rim_c,
+                                                 sorted_to_flat=s2f_c, counts=counts_c,
+                                                 offsets=offsets_c, workspace=ws),
+                nbytes["build_map"]),
+            f"unpermute_ep(ep={ep})": (
+                lambda: mp.mp_unpermute_ep(rows, rim, idx, E, ep, probs, out=y), ep_bytes),
+            f"unpermute_ep(ep={ep},bf16_partials)": (
+                lambda: mp.mp_unpermute_ep(rows, rim, idx, E, ep, probs, bf16_partials=True,
+                                           out=y), ep_bytes),
+            f"unpermute_ep(ep={ep},bf16_partials,fp64_cross_rank)": (
+                lambda: mp.mp_unpermute_ep(rows, rim, idx, E, ep, probs, bf16_partials=True,
+                                           fp64_cross_rank=True, out=y), ep_bytes),
+        }
+        call("build_map")
+        call("permute")
+        for name, (fn, b) in extra_ops.items():
+            us = time_op(fn, flush, stream, max(30, min(args.steps, 100)))
+            extras[name] = {"us": round(us, 2), "GB/s": round(b / (us * 1e-6) / 1e9, 1),
+                            "frac_of_measured": round(b / (us * 1e-6) / 1e9 / peak, 4)}
+
     out = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -409,6 +439,8 @@ def run_gpu(args):
     }
     if sort_pad:
         out["sort_pad_roundtrip"] = sort_pad
+    if extras:
+        out["extras"] = extras
     if rank == 0 and not args.no_cpu:
         v, it, dt, sample = oracle_step_rate(args.cpu_seconds)
         out["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": 1,
@@ -416,6 +448,24 @@ def run_gpu(args):
     if world > 1:
         dist.destroy_process_group()
     return out if rank == 0 else None
+
+
+def time_op(fn, flush, stream, n):
+    """Mean device time (us) of fn over n launches, L2 flushed before each."""
+    import torch
+
+    for _ in range(3):
+        fn()
+    evs = []
+    for i in range(n):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return 1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs)
 
 
 def bench_chunks(mp, wl, dev, flush, args):
@@ -515,6 +565,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-chunks", action="store_true", help="skip the sort+pad roundtrip")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the capacity-map and EP-combine timings")
     ap.add_argument("--tokens", type=int, default=None,
                     help="smaller T of the same workload (profiling captures only)")
     args = ap.parse_args()

@@ -195,6 +195,30 @@ mp_status_t mp_unpermute(const mp_bf16_t *rows, const float *probs,
                          const int32_t *row_id_map, int64_t T, int32_t K, int32_t H,
                          mp_bf16_t *out, mp_stream_t stream);
 
+/* Flags of mp_unpermute_ep. */
+#define MP_EP_BF16_PARTIALS 0x1   /* quantize each rank's partial to BF16     */
+#define MP_EP_FP64_CROSS_RANK 0x2 /* add the rank partials in FP64 (else FP32) */
+
+/*
+ * Rank-ordered combine over expert-parallel ranks, simulated on one GPU
+ * [MBI _rank_tree_unpermute_kernel, unpermute_with_bf16_rank_partials,
+ * unpermute]: rank r owns experts [r*E/ep_size, (r+1)*E/ep_size).  For each
+ * token and element: for every rank r in increasing order, the rank's partial
+ * is the slot-order chain fmaf(probs[t,k], row, partial) from +0 over the
+ * token's routed slots whose expert idx[t,k] lies on r (plain adds when probs
+ * is NULL), rounded to BF16 if MP_EP_BF16_PARTIALS; the partials are added in
+ * rank order from zero in FP32, or FP64 with MP_EP_FP64_CROSS_RANK; the sum
+ * is rounded once (RNE, from FP64 directly) to BF16.  ep_size = 1 without
+ * flags gives exactly mp_unpermute.
+ *   idx        device int32 [T,K]: the expert of each slot (the routing input
+ *              of mp_build_map); other arguments as mp_unpermute.
+ * Limits: K <= 8, E % ep_size == 0.
+ */
+mp_status_t mp_unpermute_ep(const mp_bf16_t *rows, const float *probs,
+                            const int32_t *row_id_map, const int32_t *idx, int64_t T, int32_t K,
+                            int32_t H, int32_t E, int32_t ep_size, int32_t flags, mp_bf16_t *out,
+                            mp_stream_t stream);
+
 /*
  * Backward of mp_permute [d9d _moe_permute_mask_map.backward; mops
  * permute_backward]:

@@ -344,3 +344,100 @@ def test_build_map_capacity_three_launch_path_and_dropped_rows_downstream():
     np.testing.assert_array_equal(h(out), o_out)
     y = mp.mp_unpermute(out, got[0], d(probs))
     np.testing.assert_array_equal(h(y), oracle.unpermute(o_out, probs, want[0], T, H))
+
+
+# --------------------------------------------------------------------------
+# rank-ordered combine over EP ranks
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,T,H,ep", [("mid", 2000, None, 8), ("skewed", 3000, 264, 16),
+                                          ("tiny", None, None, 4), ("mid", 1500, 37, 2)])
+@pytest.mark.parametrize("bf16p,fp64", [(False, False), (True, False), (False, True),
+                                         (True, True)])
+def test_unpermute_ep(name, T, H, ep, bf16p, fp64):
+    w = _full_case(name, T=T, H=H, empty=(name == "mid"))
+    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+    rim, *_ = mp.mp_build_map(d(w["idx"]), E)
+    o_rim, *_ = oracle.build_map(w["idx"], E)
+    rows = d(w["rows_in"])
+    for probs in (w["probs"], None):
+        got = mp.mp_unpermute_ep(rows, rim, d(w["idx"]), E, ep,
+                                 None if probs is None else d(probs),
+                                 bf16_partials=bf16p, fp64_cross_rank=fp64)
+        want = oracle.unpermute_ep(w["rows_in"], probs, o_rim, w["idx"], T, H, E, ep, bf16p, fp64)
+        np.testing.assert_array_equal(h(got), want)
+
+
+def test_unpermute_ep_one_rank_is_unpermute():
+    w = _full_case("mid", T=1000)
+    rim, *_ = mp.mp_build_map(d(w["idx"]), w["E"])
+    rows, probs = d(w["rows_in"]), d(w["probs"])
+    a = mp.mp_unpermute_ep(rows, rim, d(w["idx"]), w["E"], 1, probs)
+    assert torch.equal(a, mp.mp_unpermute(rows, rim, probs))
+
+
+def test_unpermute_ep_full_size_sampled():
+    w = wl.routed("large")
+    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+    rim, *_ = mp.mp_build_map(d(w["idx"]), E)
+    o_rim, *_ = oracle.build_map(w["idx"], E)
+    seed = 91
+    rows = wl.hashed_rows_torch(T * K, H, seed, DEV)
+    sample = np.unique(np.random.default_rng(3).choice(T, 64, replace=False))
+    rim_s = o_rim[sample]
+    rows_s = wl.hashed_rows(rim_s.ravel(), H, seed)
+    local = np.arange(rim_s.size, dtype=np.int32).reshape(rim_s.shape)
+    for bf16p, fp64 in ((True, False), (True, True)):
+        got = mp.mp_unpermute_ep(rows, rim, d(w["idx"]), E, 8, d(w["probs"]),
+                                 bf16_partials=bf16p, fp64_cross_rank=fp64)
+        want = oracle.unpermute_ep(rows_s, w["probs"][sample], local, w["idx"][sample],
+                                   len(sample), H, E, 8, bf16p, fp64)
+        np.testing.assert_array_equal(h(got)[sample], want)
+
+
+def test_unpermute_ep_wide_ranging_partials():
+    """Rows whose values span ~130 binades, so the per-element rank partials
+    often range past what an fp32 sum holds exactly: the fp64 cross-rank sum
+    must still match the oracle bit for bit."""
+    rng = np.random.default_rng(31)
+    T, K, E, H, ep = 700, 8, 64, 64, 8
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    probs = rng.dirichlet(np.ones(K), size=T).astype(np.float32)
+    ex = rng.integers(60, 191, size=(T * K, H)).astype(np.uint16)
+    rows = ((rng.integers(0, 2, size=(T * K, H)) << 15) | (ex << 7) |
+            rng.integers(0, 128, size=(T * K, H))).astype(np.uint16)
+    rim, *_ = mp.mp_build_map(d(idx), E)
+    o_rim, *_ = oracle.build_map(idx, E)
+    for bf16p, fp64 in ((True, True), (False, True), (True, False)):
+        got = mp.mp_unpermute_ep(d(rows), rim, d(idx), E, ep, d(probs), bf16_partials=bf16p,
+                                 fp64_cross_rank=fp64)
+        want = oracle.unpermute_ep(rows, probs, o_rim, idx, T, H, E, ep, bf16p, fp64)
+        np.testing.assert_array_equal(h(got), want)
+
+
+def test_unpermute_ep_fp64_sum_on_bf16_ties():
+    """Rank partials 1, 2^-8 (together exactly halfway between two bf16 values)
+    and +-2^-30 or +-2^-40 on a third rank: the tiny partial decides the
+    rounding, both on the fp32-pair path (span 30 binades) and on the fp64
+    path (span 40)."""
+    E, ep, K, H = 8, 4, 3, 8
+    vals = [(1.0, 2.0**-8, 2.0**-30), (1.0, 2.0**-8, -2.0**-30), (1.0, 2.0**-8, 2.0**-40),
+            (1.0, 2.0**-8, -2.0**-40), (1.0, 2.0**-8, 0.0), (-1.0, -(2.0**-8), -(2.0**-30)),
+            (3.0, 2.0**-7, 2.0**-33), (2.0**-30, 1.0, 2.0**-8)]
+    T = len(vals)
+    idx = np.tile(np.array([[0, 2, 4]], np.int32), (T, 1))      # ranks 0, 1, 2
+    rows_f = np.zeros((T * K, H), np.float32)
+    rim, *_ = oracle.build_map(idx, E)
+    for t, v in enumerate(vals):
+        for k in range(K):
+            rows_f[rim[t, k]] = v[k]
+    rows = torch.from_numpy(rows_f).to(torch.bfloat16)
+    assert torch.equal(rows.float(), torch.from_numpy(rows_f))   # all bf16 values
+    rows_bits = rows.view(torch.int16).numpy().view(np.uint16)
+    g_rim, *_ = mp.mp_build_map(d(idx), E)
+    got = mp.mp_unpermute_ep(d(rows_bits), g_rim, d(idx), E, ep, None, bf16_partials=True,
+                             fp64_cross_rank=True)
+    want = oracle.unpermute_ep(rows_bits, None, rim, idx, T, H, E, ep, True, True)
+    np.testing.assert_array_equal(h(got), want)
+    up = oracle.bf16_from_f32(np.float32(1.0078125))
+    assert want[0, 0] == up and want[1, 0] == oracle.bf16_from_f32(np.float32(1.0))

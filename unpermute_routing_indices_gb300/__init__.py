@@ -19,7 +19,7 @@ from . import _lib
 
 __all__ = [
     "MPError", "mp_build_map", "mp_build_map_capacity", "mp_build_map_workspace_size",
-    "mp_permute", "mp_unpermute",
+    "mp_permute", "mp_unpermute", "mp_unpermute_ep", "EP_BF16_PARTIALS", "EP_FP64_CROSS_RANK",
     "mp_permute_bwd", "mp_unpermute_bwd", "mp_sort_chunks_pad", "mp_unpad_restore",
     "mp_sort_chunks_pad_bwd", "mp_unpad_restore_bwd", "status_bits", "library_path",
 ]
@@ -28,6 +28,10 @@ STATUS_BITS = {
     "bad_expert": 0x1, "bad_split": 0x2, "bad_order": 0x4, "split_overflow": 0x8,
     "rows_overflow": 0x10, "bad_row": 0x20,
 }
+
+
+EP_BF16_PARTIALS = 0x1
+EP_FP64_CROSS_RANK = 0x2
 
 
 class MPError(RuntimeError):
@@ -206,6 +210,34 @@ def mp_unpermute(rows, row_id_map, probs=None, *, out=None):
     with torch.cuda.device(dev):
         _check("mp_unpermute", lib.mp_unpermute(
             _ptr(rows), _ptr(probs), _ptr(row_id_map), T, K, H, _ptr(out), _stream(dev)))
+    return out
+
+
+def mp_unpermute_ep(rows, row_id_map, idx, num_experts: int, ep_size: int, probs=None, *,
+                    bf16_partials: bool = False, fp64_cross_rank: bool = False, out=None):
+    """Rank-ordered combine over `ep_size` expert-parallel ranks: per-rank
+    slot-order FMA partials (optionally rounded to bf16), added in rank order
+    (fp32, or fp64), one bf16 rounding.  idx int32 [T,K] holds each slot's expert."""
+    lib = _lib.load()
+    _need(rows, "rows", torch.bfloat16, 2)
+    dev = rows.device
+    _need(row_id_map, "row_id_map", torch.int32, 2, dev)
+    T, K = row_id_map.shape
+    _need(idx, "idx", torch.int32, 2, dev)
+    _shape(idx, "idx", (T, K))
+    H = rows.shape[1]
+    if probs is not None:
+        _need(probs, "probs", torch.float32, 2, dev)
+        _shape(probs, "probs", (T, K))
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if out is None \
+        else _need(out, "out", torch.bfloat16, 2, dev)
+    _shape(out, "out", (T, H))
+    flags = (EP_BF16_PARTIALS if bf16_partials else 0) | \
+        (EP_FP64_CROSS_RANK if fp64_cross_rank else 0)
+    with torch.cuda.device(dev):
+        _check("mp_unpermute_ep", lib.mp_unpermute_ep(
+            _ptr(rows), _ptr(probs), _ptr(row_id_map), _ptr(idx), T, K, H, int(num_experts),
+            int(ep_size), flags, _ptr(out), _stream(dev)))
     return out
 
 

@@ -23,6 +23,7 @@ SIGNATURES = {
     "mp_build_map_noalloc": (I32, [P, I64, I32, I32, P, P, P, P, P, P]),
     "mp_permute": (I32, [P, P, P, I64, I32, I32, P, P, P]),
     "mp_unpermute": (I32, [P, P, P, I64, I32, I32, P, P]),
+    "mp_unpermute_ep": (I32, [P, P, P, P, I64, I32, I32, I32, I32, I32, P, P]),
     "mp_permute_bwd": (I32, [P, P, P, I64, I32, I32, P, P, P]),
     "mp_unpermute_bwd": (I32, [P, P, P, P, I64, I32, I32, P, P, P]),
     "mp_sort_chunks_pad": (I32, [P, P, P, P, I32, I32, I32, I64, I64, I32, P, P, P, P, P, P]),

@@ -1,0 +1,343 @@
+// Rank-ordered combine over expert-parallel ranks, on one GPU.
+//
+// "core.transformer.moe.batch_invariant" (Megatron-Core API docs) defines the
+// batch-invariant unpermute over EP ranks: accumulation is token-owned and
+// adds contributions by EP rank, then top-k slot (unpermute); each rank's
+// partial is the slot-order chain of FP32 fused multiply-adds of probability
+// and row from zero, optionally quantized to BF16 (BF16_RANK_PARTIALS,
+// unpermute_with_bf16_rank_partials), and the ranks are added in rank order,
+// optionally in FP64 (CROSS_RANK_FP64, _rank_tree_unpermute_kernel).  Here the
+// EP ranks are simulated: rank r owns experts [r*E/ep, (r+1)*E/ep).
+//
+// k_unpermute_ep: one group of tpt threads per token, one 16-byte vector (8
+// elements) per thread per pass.  Each thread sorts the token's K (<= 8)
+// slots by (rank, slot) once, with a fixed sorting network on registers, then
+// per pass loads the rows in that order and runs one fused multiply-add chain
+// that hands the rank's partial to the cross-rank sum at each rank's last
+// slot: K FMAs per element whatever the number of ranks.  A rank with no
+// routed slot would add +0 to an accumulator that is never -0, so skipping it
+// changes no bit.  GB300 runs FP64 at a small fraction of its FP32 rate, so
+// bf16 partials whose fp64 sum is provably exact are summed exactly as an
+// fp32 pair (same bits); only partials spanning more than 34 binades take the
+// fp64 additions.
+#include <climits>
+
+#include "common.cuh"
+
+namespace mp {
+namespace {
+
+constexpr int EP_THREADS = 128;
+constexpr int EP_KMAX = 8;
+
+// fp64 -> bf16, round to nearest even, in a single rounding, from the binary64
+// fields: keep the top 8 significant bits (1 + 7) for normal bf16 results, or
+// the bits at or above the 2^-133 quantum for subnormal ones; a carry out of
+// the kept bits moves to the next binade (and to +-inf past 2^128).
+__device__ __forceinline__ uint16_t bf16_from_f64(double d)
+{
+    const uint64_t u = static_cast<uint64_t>(__double_as_longlong(d));
+    const uint16_t sign = static_cast<uint16_t>((u >> 48) & 0x8000u);
+    const int ex = static_cast<int>((u >> 52) & 0x7ff);
+    const uint64_t mant = u & 0xFFFFFFFFFFFFFull;
+    if (ex == 0x7ff) return mant ? 0x7fc0 : static_cast<uint16_t>(sign | 0x7f80u);
+    if (ex == 0) return sign;  // zero, or far below half the smallest bf16 subnormal
+    const int e = ex - 1023;   // value = 1.mant * 2^e
+    if (e > 127) return static_cast<uint16_t>(sign | 0x7f80u);
+    const uint64_t full = (1ull << 52) | mant;
+    if (e >= -126) {
+        uint64_t keep = full >> 45;
+        const uint64_t rest = full & ((1ull << 45) - 1), half = 1ull << 44;
+        if (rest > half || (rest == half && (keep & 1u))) keep += 1;
+        return static_cast<uint16_t>(sign | (((uint32_t)(e + 127) << 7) + (uint32_t)(keep - 128)));
+    }
+    const int s = -81 - e;  // shift to the 2^-133 quantum (>= 46 here)
+    if (s >= 54) return sign;
+    uint64_t keep = full >> s;
+    const uint64_t rest = full & ((1ull << s) - 1), half = 1ull << (s - 1);
+    if (rest > half || (rest == half && (keep & 1u))) keep += 1;
+    return static_cast<uint16_t>(sign | keep);
+}
+
+// bf16 (round to nearest even) of the exact value a + b of two floats.  After
+// TwoSum, hi = fl(a + b) and lo = the exact error; bf16 rounding of hi is right
+// unless hi lies exactly halfway between two bf16 values, where the sign of lo
+// (the side of the tie the exact value is on) decides.
+__device__ __forceinline__ uint16_t bf16_from_pair(float a, float b)
+{
+    const float hi = __fadd_rn(a, b);
+    const float bb = __fsub_rn(hi, a);
+    const float lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
+    const uint32_t u = __float_as_uint(hi);
+    if ((u & 0xffffu) == 0x8000u && lo != 0.0f && (u & 0x7f800000u) != 0x7f800000u) {
+        const bool away = (lo > 0.0f) == (hi > 0.0f);   // exact value beyond the tie
+        return static_cast<uint16_t>((u >> 16) + (away ? 1u : 0u));
+    }
+    __nv_bfloat16 h = __float2bfloat16_rn(hi);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 pack_bits(const uint16_t (&b)[8])
+{
+    return make_uint4((uint32_t)b[0] | ((uint32_t)b[1] << 16), (uint32_t)b[2] | ((uint32_t)b[3] << 16),
+                      (uint32_t)b[4] | ((uint32_t)b[5] << 16), (uint32_t)b[6] | ((uint32_t)b[7] << 16));
+}
+
+__device__ __forceinline__ uint16_t pack_bits(const uint16_t (&b)[1]) { return b[0]; }
+
+template <bool FP64> struct AccT;
+template <> struct AccT<false> { using type = float; };
+template <> struct AccT<true> { using type = double; };
+
+template <typename V, bool FP64> struct PackAcc;
+template <> struct PackAcc<uint4, false> {
+    static __device__ __forceinline__ uint4 run(const float (&a)[8]) { return pack(a); }
+};
+template <> struct PackAcc<uint16_t, false> {
+    static __device__ __forceinline__ uint16_t run(const float (&a)[1]) { return pack(a); }
+};
+template <> struct PackAcc<uint4, true> {
+    static __device__ __forceinline__ uint4 run(const double (&a)[8])
+    {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = (uint32_t)bf16_from_f64(a[2 * i]) | ((uint32_t)bf16_from_f64(a[2 * i + 1]) << 16);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+template <> struct PackAcc<uint16_t, true> {
+    static __device__ __forceinline__ uint16_t run(const double (&a)[1]) { return bf16_from_f64(a[0]); }
+};
+
+// Compare-exchange on (key, row, prob) triples, smaller key first.
+__device__ __forceinline__ void cx(int32_t &ka, int32_t &ra, float &pa, int32_t &kb, int32_t &rb,
+                                   float &pb)
+{
+    const bool sw = kb < ka;
+    const int32_t k0 = sw ? kb : ka, k1 = sw ? ka : kb;
+    const int32_t r0 = sw ? rb : ra, r1 = sw ? ra : rb;
+    const float p0 = sw ? pb : pa, p1 = sw ? pa : pb;
+    ka = k0; kb = k1; ra = r0; rb = r1; pa = p0; pb = p1;
+}
+
+// Batcher's odd-even merge sort of 8 keys (19 comparators, fixed indices).
+__device__ __forceinline__ void sort8(int32_t (&k)[EP_KMAX], int32_t (&r)[EP_KMAX],
+                                      float (&p)[EP_KMAX])
+{
+#define MP_CX(a, b) cx(k[a], r[a], p[a], k[b], r[b], p[b])
+    MP_CX(0, 1); MP_CX(2, 3); MP_CX(4, 5); MP_CX(6, 7);
+    MP_CX(0, 2); MP_CX(1, 3); MP_CX(4, 6); MP_CX(5, 7);
+    MP_CX(1, 2); MP_CX(5, 6);
+    MP_CX(0, 4); MP_CX(1, 5); MP_CX(2, 6); MP_CX(3, 7);
+    MP_CX(2, 4); MP_CX(3, 5);
+    MP_CX(1, 2); MP_CX(3, 4); MP_CX(5, 6);
+#undef MP_CX
+}
+
+// Walks the token's slots sorted by (rank, slot): a slot-order chain of fused
+// multiply-adds (plain adds without probs) from +0 per rank, and add(e, p) at
+// each rank's last slot with the rank's partial p for element e (rounded to
+// bf16 if BF16P).  `valid` / `last` are bit masks over the sorted positions.
+template <bool PROBS, bool BF16P, int L, typename V, typename Add>
+__device__ __forceinline__ void walk_ranks(const V (&r)[EP_KMAX], const float (&p)[EP_KMAX],
+                                           unsigned valid, unsigned last, Add add)
+{
+    float part[L];
+#pragma unroll
+    for (int e = 0; e < L; ++e) part[e] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < EP_KMAX; ++j) {
+        if (!(valid >> j & 1u)) continue;
+        float f[L];
+        unpack(r[j], f);
+#pragma unroll
+        for (int e = 0; e < L; ++e)
+            part[e] = PROBS ? __fmaf_rn(p[j], f[e], part[e]) : __fadd_rn(part[e], f[e]);
+        if (last >> j & 1u) {
+#pragma unroll
+            for (int e = 0; e < L; ++e) {
+                add(e, BF16P ? __bfloat162float(__float2bfloat16_rn(part[e])) : part[e]);
+                part[e] = 0.0f;
+            }
+        }
+    }
+}
+
+template <typename V, bool PROBS, bool BF16P, bool FP64>
+__global__ void __launch_bounds__(EP_THREADS)
+    k_unpermute_ep(const V *__restrict__ rows, const float *__restrict__ probs,
+                   const int32_t *__restrict__ map, const int32_t *__restrict__ idx, int64_t T,
+                   int K, int nvec, int tpt_log2, int per_rank, V *__restrict__ out)
+{
+    constexpr int L = Lanes<V>::N;
+    using Acc = typename AccT<FP64>::type;
+    const int tpt = 1 << tpt_log2;
+    const int lane = threadIdx.x & (tpt - 1);
+    const int64_t t = (int64_t)blockIdx.x * (EP_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
+    if (t >= T) return;
+
+    // The token's routed slots sorted by (rank, slot); unrouted slots last.
+    int32_t key[EP_KMAX], rk[EP_KMAX];
+    float pk[EP_KMAX];
+#pragma unroll
+    for (int i = 0; i < EP_KMAX; ++i) {
+        const bool in = i < K;
+        const int32_t row = in ? __ldg(map + t * K + i) : -1;
+        int32_t rank = in ? __ldg(idx + t * K + i) / per_rank : 0;
+        rank = rank < -(1 << 20) ? -(1 << 20) : (rank > (1 << 20) ? (1 << 20) : rank);
+        key[i] = row >= 0 ? rank * EP_KMAX + i : INT_MAX;
+        rk[i] = row;
+        pk[i] = (PROBS && in) ? __ldg(probs + t * K + i) : 1.0f;
+    }
+    sort8(key, rk, pk);
+    unsigned valid = 0, last = 0;
+#pragma unroll
+    for (int j = 0; j < EP_KMAX; ++j) {
+        if (key[j] == INT_MAX) continue;
+        valid |= 1u << j;
+        const bool next_same = j + 1 < EP_KMAX && key[j + 1] != INT_MAX &&
+                               (key[j + 1] - (key[j + 1] & (EP_KMAX - 1))) ==
+                                   (key[j] - (key[j] & (EP_KMAX - 1)));
+        if (!next_same) last |= 1u << j;
+    }
+    for (int c0 = 0; c0 < nvec; c0 += tpt) {
+        const int c = c0 + lane;
+        V r[EP_KMAX];
+#pragma unroll
+        for (int i = 0; i < EP_KMAX; ++i)
+            r[i] = ((valid >> i & 1u) && c < nvec) ? ld_stream(rows + (int64_t)rk[i] * nvec + c)
+                                                   : zero_vec<V>();
+        Acc acc[L];
+        if (FP64 && BF16P) {
+            // Cross-rank sum of bf16 partials in fp64.  Every partial is a
+            // multiple of the smallest partial's quantum Q.  The sum runs as an
+            // fp32 pair (hi, lo): TwoSum makes each addition's error exact, and
+            // while the nonzero partials span at most 34 binades (below 2^124)
+            // the errors add up in lo without rounding, so hi + lo is the exact
+            // sum -- which the fp64 additions also produce, every partial sum
+            // having at most 45 significant bits.  Wider spans take the fp64
+            // additions (the rows are still in registers).
+            float shi[L], slo[L];
+            int lo[L], hi[L];
+#pragma unroll
+            for (int e = 0; e < L; ++e) {
+                shi[e] = 0.0f;
+                slo[e] = 0.0f;
+                lo[e] = 255;
+                hi[e] = 0;
+            }
+            walk_ranks<PROBS, true, L>(r, pk, valid, last, [&](int e, float p) {
+                const float s = __fadd_rn(shi[e], p);
+                const float bb = __fsub_rn(s, shi[e]);
+                const float err = __fadd_rn(__fsub_rn(shi[e], __fsub_rn(s, bb)), __fsub_rn(p, bb));
+                shi[e] = s;
+                slo[e] = __fadd_rn(slo[e], err);
+                if (p != 0.0f) {
+                    int ex = (__float_as_int(p) >> 23) & 0xff;
+                    ex = ex < 1 ? 1 : ex;
+                    lo[e] = min(lo[e], ex);
+                    hi[e] = max(hi[e], ex);
+                }
+            });
+            bool any_wide = false;
+#pragma unroll
+            for (int e = 0; e < L; ++e) {
+                const bool wide = !(hi[e] - lo[e] <= 34 && hi[e] <= 250);
+                any_wide |= wide;
+                lo[e] = wide;   // reuse: 1 = needs the fp64 pass
+                acc[e] = 0.0;
+            }
+            if (any_wide)
+                walk_ranks<PROBS, true, L>(r, pk, valid, last, [&](int e, float p) {
+                    if (lo[e]) acc[e] = __dadd_rn(acc[e], (double)p);
+                });
+            if (c < nvec) {
+                uint16_t bits[L];
+#pragma unroll
+                for (int e = 0; e < L; ++e)
+                    bits[e] = lo[e] ? bf16_from_f64(acc[e]) : bf16_from_pair(shi[e], slo[e]);
+                st_row(out + t * nvec + c, pack_bits(bits));
+            }
+            continue;
+        } else {
+#pragma unroll
+            for (int e = 0; e < L; ++e) acc[e] = 0;
+            walk_ranks<PROBS, BF16P, L>(r, pk, valid, last, [&](int e, float p) {
+                if (FP64)
+                    acc[e] = __dadd_rn(acc[e], (double)p);
+                else
+                    acc[e] = __fadd_rn(acc[e], p);
+            });
+        }
+        if (c < nvec) st_row(out + t * nvec + c, PackAcc<V, FP64>::run(acc));
+    }
+}
+
+template <typename V, bool PROBS, bool BF16P, bool FP64>
+void launch_ep(const void *rows, const float *probs, const int32_t *map, const int32_t *idx,
+               int64_t T, int K, int nvec, int per_rank, void *out, cudaStream_t s)
+{
+    int l = ceil_log2(nvec < 1 ? 1 : nvec);
+    const int lmax = ceil_log2(EP_THREADS);
+    if (l > lmax) l = lmax;
+    const int64_t per_block = EP_THREADS >> l;
+    const unsigned blocks = (unsigned)((T + per_block - 1) / per_block);
+    k_unpermute_ep<V, PROBS, BF16P, FP64><<<blocks, EP_THREADS, 0, s>>>(
+        (const V *)rows, probs, map, idx, T, K, nvec, l, per_rank, (V *)out);
+}
+
+template <typename V, bool PROBS>
+void launch_ep_flags(int flags, const void *rows, const float *probs, const int32_t *map,
+                     const int32_t *idx, int64_t T, int K, int nvec, int per_rank, void *out,
+                     cudaStream_t s)
+{
+    const bool b = flags & MP_EP_BF16_PARTIALS, d = flags & MP_EP_FP64_CROSS_RANK;
+    if (b && d)
+        launch_ep<V, PROBS, true, true>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
+    else if (b)
+        launch_ep<V, PROBS, true, false>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
+    else if (d)
+        launch_ep<V, PROBS, false, true>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
+    else
+        launch_ep<V, PROBS, false, false>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
+}
+
+}  // namespace
+}  // namespace mp
+
+using namespace mp;
+
+extern "C" mp_status_t mp_unpermute_ep(const mp_bf16_t *rows, const float *probs,
+                                       const int32_t *row_id_map, const int32_t *idx, int64_t T,
+                                       int32_t K, int32_t H, int32_t E, int32_t ep_size,
+                                       int32_t flags, mp_bf16_t *out, mp_stream_t stream)
+{
+    if (T < 0 || K < 1 || H < 1 || E < 1 || ep_size < 1 || T * (int64_t)K > INT32_MAX)
+        return MP_ERR_INVALID_ARG;
+    if (E % ep_size != 0 || (flags & ~(MP_EP_BF16_PARTIALS | MP_EP_FP64_CROSS_RANK)) != 0)
+        return MP_ERR_INVALID_ARG;
+    if (K > EP_KMAX) return MP_ERR_UNSUPPORTED;
+    if (T == 0) return MP_OK;
+    if (rows == nullptr || row_id_map == nullptr || idx == nullptr || out == nullptr)
+        return MP_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    const int per_rank = E / ep_size;
+    const bool vec = H % 8 == 0 && aligned16(rows) && aligned16(out);
+    if (vec) {
+        if (probs)
+            launch_ep_flags<uint4, true>(flags, rows, probs, row_id_map, idx, T, K, H / 8, per_rank,
+                                         out, s);
+        else
+            launch_ep_flags<uint4, false>(flags, rows, nullptr, row_id_map, idx, T, K, H / 8,
+                                          per_rank, out, s);
+    } else {
+        if (probs)
+            launch_ep_flags<uint16_t, true>(flags, rows, probs, row_id_map, idx, T, K, H, per_rank,
+                                            out, s);
+        else
+            launch_ep_flags<uint16_t, false>(flags, rows, nullptr, row_id_map, idx, T, K, H,
+                                             per_rank, out, s);
+    }
+    return check_launch();
+}
