@@ -63,6 +63,10 @@ def _load():
         lib.orc_bf16_from_f64.restype = ctypes.c_uint16
         lib.orc_unpermute_ep.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P]
         lib.orc_unpermute_ep.restype = None
+        lib.orc_topk_softmax.argtypes = [P, i64, i32, i32, i32, i32, P, P]
+        lib.orc_topk_softmax.restype = None
+        lib.orc_topk_softmax_bwd.argtypes = [P, P, P, i64, i32, i32, P]
+        lib.orc_topk_softmax_bwd.restype = None
         lib.orc_permute.argtypes = [P, P, P, i64, i32, i32, P, P]
         lib.orc_permute.restype = None
         lib.orc_unpermute.argtypes = [P, P, P, i64, i32, i32, P]
@@ -229,6 +233,32 @@ def unpermute_bwd(g_y, rows, probs, row_id_map, out_rows=None):
     lib.orc_unpermute_bwd(_p(g_y), _p(rows), _p(probs), _p(row_id_map), T, K, H,
                           _p(g_rows), _p(g_probs))
     return g_rows, g_probs
+
+
+# --------------------------------------------------------------------------
+# router
+# --------------------------------------------------------------------------
+
+def topk_softmax(logits, K, n_groups=1, topk_groups=1):
+    """logits f32 [T,E] -> (idx int32 [T,K], probs f32 [T,K])."""
+    lib = _load()
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    idx = np.empty((T, K), np.int32)
+    probs = np.empty((T, K), np.float32)
+    lib.orc_topk_softmax(_p(logits), T, E, K, n_groups, topk_groups, _p(idx), _p(probs))
+    return idx, probs
+
+
+def topk_softmax_bwd(g_probs, probs, idx, E):
+    lib = _load()
+    g_probs = _c(g_probs, np.float32)
+    probs = _c(probs, np.float32)
+    idx = _c(idx, np.int32)
+    T, K = idx.shape
+    g_logits = np.empty((T, E), np.float32)
+    lib.orc_topk_softmax_bwd(_p(g_probs), _p(probs), _p(idx), T, E, K, _p(g_logits))
+    return g_logits
 
 
 # --------------------------------------------------------------------------

@@ -387,6 +387,96 @@ void orc_unpermute_bwd(const uint16_t *g_y, const uint16_t *rows, const float *p
 }
 
 /* ------------------------------------------------------------------------ */
+/* Router: fused top-k softmax  [mops "Operators: fused_topk_softmax"]       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Per token: optionally keep only the topk_groups best of n_groups equal
+ * groups of consecutive experts (a group's score is its largest logit; equal
+ * scores favour the lower group), then pick the K largest logits among the
+ * kept experts one at a time (equal logits favour the lower expert), so slot
+ * 0 holds the largest.  probs are the fp32 softmax over the K picked logits:
+ * z_k = l_k - l_0, e_k = expf(z_k), s = e_0 + ... + e_{K-1} in slot order,
+ * p_k = e_k / s.  n_groups = topk_groups = 1 is plain top-K.
+ */
+void orc_topk_softmax(const float *logits, int64_t T, int32_t E, int32_t K,
+                      int32_t n_groups, int32_t topk_groups, int32_t *idx, float *probs)
+{
+    const int32_t per_group = E / n_groups;
+    char *kept = (char *)malloc((size_t)E);
+    char *taken = (char *)malloc((size_t)E);
+    char *gtaken = (char *)malloc((size_t)n_groups);
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        for (int32_t g = 0; g < n_groups; ++g)
+            gtaken[g] = 0;
+        for (int32_t e = 0; e < E; ++e)
+            kept[e] = (n_groups == 1);
+        if (n_groups > 1) {
+            for (int32_t j = 0; j < topk_groups; ++j) {
+                int32_t best = -1;
+                float best_score = 0.0f;
+                for (int32_t g = 0; g < n_groups; ++g) {
+                    if (gtaken[g])
+                        continue;
+                    float score = l[g * per_group];
+                    for (int32_t e = g * per_group + 1; e < (g + 1) * per_group; ++e)
+                        if (l[e] > score)
+                            score = l[e];
+                    if (best < 0 || score > best_score) {
+                        best = g;
+                        best_score = score;
+                    }
+                }
+                gtaken[best] = 1;
+                for (int32_t e = best * per_group; e < (best + 1) * per_group; ++e)
+                    kept[e] = 1;
+            }
+        }
+        for (int32_t e = 0; e < E; ++e)
+            taken[e] = 0;
+        for (int32_t k = 0; k < K; ++k) {
+            int32_t best = -1;
+            for (int32_t e = 0; e < E; ++e)
+                if (kept[e] && !taken[e] && (best < 0 || l[e] > l[best]))
+                    best = e;
+            taken[best] = 1;
+            idx[t * K + k] = best;
+        }
+        float s = 0.0f;
+        const float m = l[idx[t * K]];
+        for (int32_t k = 0; k < K; ++k) {
+            float z = l[idx[t * K + k]] - m;
+            probs[t * K + k] = expf(z);
+            s = s + probs[t * K + k];
+        }
+        for (int32_t k = 0; k < K; ++k)
+            probs[t * K + k] = probs[t * K + k] / s;
+    }
+    free(kept);
+    free(taken);
+    free(gtaken);
+}
+
+/* Gradient of the router w.r.t. the logits: the picked logits get the softmax
+ * gradient g_l_k = p_k * (g_k - d) with d = sum_j p_j * g_j (fused
+ * multiply-adds in slot order from +0); every other logit gets 0 (the choice
+ * itself is piecewise constant). */
+void orc_topk_softmax_bwd(const float *g_probs, const float *probs, const int32_t *idx,
+                          int64_t T, int32_t E, int32_t K, float *g_logits)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t e = 0; e < E; ++e)
+            g_logits[t * E + e] = 0.0f;
+        float d = 0.0f;
+        for (int32_t k = 0; k < K; ++k)
+            d = fmaf(probs[t * K + k], g_probs[t * K + k], d);
+        for (int32_t k = 0; k < K; ++k)
+            g_logits[t * E + idx[t * K + k]] = probs[t * K + k] * (g_probs[t * K + k] - d);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Chunk sort + pad, unpad + restore  [TE-PR]                                */
 /* ------------------------------------------------------------------------ */
 

@@ -601,3 +601,62 @@ def test_unpermute_ep_with_one_rank_is_unpermute():
     # bf16 partials with one rank: bf16(bf16(x)) == bf16(x)
     np.testing.assert_array_equal(oracle.unpermute_ep(rows, probs, rim, idx, T, H, E, 1, True),
                                   oracle.unpermute(rows, probs, rim, T, H))
+
+
+# --------------------------------------------------------------------------
+# router: fused top-k softmax
+# --------------------------------------------------------------------------
+
+def test_topk_softmax_selection_matches_stable_argsort():
+    rng = np.random.default_rng(4)
+    logits = rng.integers(-3, 4, size=(200, 24)).astype(np.float32)   # many ties
+    idx, probs = oracle.topk_softmax(logits, 5)
+    want = np.argsort(-logits, axis=1, kind="stable")[:, :5]
+    np.testing.assert_array_equal(idx, want)
+
+
+def test_topk_softmax_probs_within_fp32_bound_of_fp64():
+    rng = np.random.default_rng(5)
+    T, E, K = 300, 64, 8
+    logits = (3 * rng.standard_normal((T, E))).astype(np.float32)
+    idx, probs = oracle.topk_softmax(logits, K)
+    sel = np.take_along_axis(logits, idx, axis=1).astype(np.float64)
+    z = sel - sel[:, :1]
+    p64 = np.exp(z) / np.exp(z).sum(1, keepdims=True)
+    # each term: z rounding (|z| ulp/2), expf (<= 1 ulp), sum (K ulp), divide
+    bound = (np.abs(z).max(1, keepdims=True) * 2.0**-24 + (K + 4) * 2.0**-24) * p64 * 2
+    assert np.all(np.abs(probs - p64) <= bound)
+    np.testing.assert_allclose(probs.sum(1), 1.0, rtol=K * 2.0**-23)
+
+
+def test_topk_softmax_group_limited_brute_force():
+    rng = np.random.default_rng(6)
+    T, E, K, G, TG = 120, 32, 4, 8, 3
+    logits = rng.integers(-4, 5, size=(T, E)).astype(np.float32)
+    idx, _ = oracle.topk_softmax(logits, K, G, TG)
+    per = E // G
+    for t in range(T):
+        score = [max(logits[t, g * per:(g + 1) * per]) for g in range(G)]
+        groups = sorted(range(G), key=lambda g: (-score[g], g))[:TG]
+        cand = [e for e in range(E) if e // per in groups]
+        best = sorted(cand, key=lambda e: (-logits[t, e], e))[:K]
+        assert list(idx[t]) == best
+
+
+def test_topk_softmax_bwd_is_the_softmax_jacobian():
+    rng = np.random.default_rng(7)
+    T, E, K = 50, 16, 4
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    idx, probs = oracle.topk_softmax(logits, K)
+    g = rng.standard_normal((T, K)).astype(np.float32)
+    gl = oracle.topk_softmax_bwd(g, probs, idx, E)
+    p = probs.astype(np.float64)
+    for t in range(T):
+        J = np.diag(p[t]) - np.outer(p[t], p[t])          # d p / d z, symmetric
+        want = J @ g[t].astype(np.float64)
+        got = gl[t, idx[t]].astype(np.float64)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-6)
+        mask = np.ones(E, bool)
+        mask[idx[t]] = False
+        assert np.all(gl[t, mask] == 0)
+        assert abs(got.sum()) < 1e-6
