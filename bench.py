@@ -386,6 +386,8 @@ def run_gpu(args):
         cap = -(-5 * routed // (4 * E))                   # capacity factor 1.25
         ep = 8
         ep_bytes = nbytes["unpermute"] + 4 * T * K        # + the slot experts
+        logits = dev_t(wl.router_logits(WORKLOAD, T=T, seed=base_seed))
+        r_idx, r_probs = torch.empty_like(idx), torch.empty_like(probs)
         rim_c, s2f_c = torch.empty_like(rim), torch.empty_like(s2f)
         counts_c, offsets_c = torch.empty_like(counts), torch.empty_like(offsets)
         extra_ops = {
@@ -394,6 +396,9 @@ def run_gpu(args):
                                                  sorted_to_flat=s2f_c, counts=counts_c,
                                                  offsets=offsets_c, workspace=ws),
                 nbytes["build_map"]),
+            "topk_softmax(router)": (
+                lambda: mp.mp_topk_softmax(logits, K, idx=r_idx, probs=r_probs),
+                4 * T * E + 8 * T * K),
             f"unpermute_ep(ep={ep})": (
                 lambda: mp.mp_unpermute_ep(rows, rim, idx, E, ep, probs, out=y), ep_bytes),
             f"unpermute_ep(ep={ep},bf16_partials)": (

@@ -162,6 +162,37 @@ mp_status_t mp_build_map_noalloc(const int32_t *idx, int64_t T, int32_t K, int32
                                  mp_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Router  [mops "Operators: fused_topk_softmax"]                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Fused top-k softmax: the routing input of mp_build_map from router logits.
+ * Per token: if n_groups > 1, keep only the topk_groups best of n_groups equal
+ * groups of consecutive experts (score = the group's largest logit; equal
+ * scores favour the lower group); then pick the K largest logits among the
+ * kept experts (equal logits favour the lower expert), slot 0 the largest.
+ * probs = fp32 softmax over the K picked logits: z_k = l_k - l_0, expf
+ * (CUDA's full-accuracy expf), sum in slot order, IEEE division.
+ *   logits  device fp32 [T,E];  idx device int32 [T,K];  probs device fp32 [T,K]
+ * Limits: E <= MP_MAX_EXPERTS, K <= 32, n_groups <= 32, E % n_groups == 0,
+ * topk_groups * E / n_groups >= K.
+ */
+mp_status_t mp_topk_softmax(const float *logits, int64_t T, int32_t E, int32_t K,
+                            int32_t n_groups, int32_t topk_groups, int32_t *idx, float *probs,
+                            mp_stream_t stream);
+
+/*
+ * Backward of mp_topk_softmax: g_logits[t,e] = p_k * (g_probs[t,k] - d) at
+ * the picked expert e = idx[t,k], with d = sum_k p_k * g_probs[t,k] (fused
+ * multiply-adds in slot order from +0), and 0 for every other expert.
+ *   g_probs, probs device fp32 [T,K];  idx device int32 [T,K];
+ *   g_logits device fp32 [T,E] (every element written).
+ */
+mp_status_t mp_topk_softmax_bwd(const float *g_probs, const float *probs, const int32_t *idx,
+                                int64_t T, int32_t E, int32_t K, float *g_logits,
+                                mp_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Permute / unpermute  [d9d _permute_kernel, _unpermute_kernel; MBI]        */
 /* ------------------------------------------------------------------------ */
 

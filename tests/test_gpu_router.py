@@ -1,0 +1,88 @@
+"""Parity of the fused top-k softmax router with the oracle: expert choices
+bit-exact; probabilities within 8 fp32 ulps (CUDA's expf and the C library's
+expf may differ by a few ulps; the rest of the arithmetic is the same IEEE
+sequence); the backward bit-exact from the same forward probabilities."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import unpermute_routing_indices_gb300 as mp
+from unpermute_routing_indices_gb300 import workloads as wl
+from tests.gpu_util import DEV, d, h
+
+pytestmark = pytest.mark.gpu
+
+ULP_TOL = 8
+
+
+def _logits(T, E, seed, ties=False, skew=False):
+    rng = np.random.default_rng(seed)
+    if ties:
+        return rng.integers(-3, 4, size=(T, E)).astype(np.float32)
+    x = rng.standard_normal((T, E), dtype=np.float32)
+    if skew:
+        x = x + wl.zipf_bias(rng, E)[None, :]
+    return x.astype(np.float32)
+
+
+def _check_probs(got, want):
+    assert np.all(np.abs(got - want) <= ULP_TOL * np.spacing(np.abs(want).astype(np.float32)))
+
+
+@pytest.mark.parametrize("T,E,K,G,TG,kind", [
+    (16, 32, 4, 1, 1, "normal"),        # tiny workload shape
+    (4096, 64, 6, 1, 1, "normal"),      # mid
+    (16384, 128, 8, 1, 1, "skew"),      # skewed (Zipf-biased) router
+    (32768, 256, 8, 8, 4, "normal"),    # large: 8 groups, top-4 groups
+    (3001, 40, 5, 1, 1, "ties"),        # integer logits: many ties, odd sizes
+    (2000, 96, 3, 6, 2, "ties"),
+    (777, 1024, 32, 32, 8, "normal"),   # limits
+    (500, 8, 8, 1, 1, "normal"),        # K = E
+])
+def test_topk_softmax_parity(T, E, K, G, TG, kind):
+    logits = _logits(T, E, T + E, ties=(kind == "ties"), skew=(kind == "skew"))
+    idx, probs = mp.mp_topk_softmax(d(logits), K, n_groups=G, topk_groups=TG)
+    o_idx, o_probs = oracle.topk_softmax(logits, K, G, TG)
+    np.testing.assert_array_equal(h(idx), o_idx)
+    _check_probs(h(probs), o_probs)
+
+
+def test_topk_softmax_matches_the_workload_router():
+    """The router in the input generator (numpy) chooses the same experts."""
+    for name, G, TG in (("mid", 1, 1), ("large", 8, 4)):
+        cfg = wl.ROUTED[name]
+        rng = np.random.default_rng(cfg["seed"])
+        logits = rng.standard_normal((cfg["T"], cfg["E"]), dtype=np.float32)
+        want_idx, want_probs = wl.routing(name)[:2]
+        idx, probs = mp.mp_topk_softmax(d(logits), cfg["K"], n_groups=G, topk_groups=TG)
+        np.testing.assert_array_equal(h(idx), want_idx)
+        np.testing.assert_allclose(h(probs), want_probs, rtol=1e-5, atol=0)
+
+
+def test_topk_softmax_bwd_parity():
+    T, E, K = 5000, 128, 8
+    logits = _logits(T, E, 9)
+    idx, probs = mp.mp_topk_softmax(d(logits), K)
+    g = np.random.default_rng(10).standard_normal((T, K)).astype(np.float32)
+    g_logits = mp.mp_topk_softmax_bwd(d(g), probs, idx, E)
+    want = oracle.topk_softmax_bwd(g, h(probs), h(idx), E)
+    np.testing.assert_array_equal(h(g_logits), want)
+
+
+def test_router_feeds_the_map():
+    """logits -> router -> map -> permute, all on the device, equals the oracle chain."""
+    T, E, K, H = 4096, 64, 6, 256
+    logits = _logits(T, E, 11)
+    x = wl.random_rows(T, H, 12)
+    idx, probs = mp.mp_topk_softmax(d(logits), K)
+    rim, *_ = mp.mp_build_map(idx, E)
+    out, out_p = mp.mp_permute(d(x), rim, probs)
+    o_idx, _ = oracle.topk_softmax(logits, K)
+    o_rim, *_ = oracle.build_map(o_idx, E)
+    np.testing.assert_array_equal(h(rim), o_rim)
+    o_out, _ = oracle.permute(x, None, o_rim)
+    np.testing.assert_array_equal(h(out), o_out)
+    np.testing.assert_array_equal(h(out_p)[o_rim.ravel()], h(probs).ravel())

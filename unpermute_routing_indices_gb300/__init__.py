@@ -19,7 +19,7 @@ from . import _lib
 
 __all__ = [
     "MPError", "mp_build_map", "mp_build_map_capacity", "mp_build_map_workspace_size",
-    "mp_permute", "mp_unpermute", "mp_unpermute_ep", "EP_BF16_PARTIALS", "EP_FP64_CROSS_RANK",
+    "mp_topk_softmax", "mp_topk_softmax_bwd", "mp_permute", "mp_unpermute", "mp_unpermute_ep", "EP_BF16_PARTIALS", "EP_FP64_CROSS_RANK",
     "mp_permute_bwd", "mp_unpermute_bwd", "mp_sort_chunks_pad", "mp_unpad_restore",
     "mp_sort_chunks_pad_bwd", "mp_unpad_restore_bwd", "status_bits", "library_path",
 ]
@@ -161,6 +161,53 @@ def _build_map(fn, idx, num_experts, capacity, with_sorted_to_flat, row_id_map, 
                 _stream(dev))
         _check(fn, code)
     return row_id_map, sorted_to_flat, counts, offsets
+
+
+# --------------------------------------------------------------------------
+# router
+# --------------------------------------------------------------------------
+
+def mp_topk_softmax(logits, topk: int, *, n_groups: int = 1, topk_groups: int = 1, idx=None,
+                    probs=None):
+    """logits fp32 [T,E] -> (idx int32 [T,K], probs fp32 [T,K]): top-K experts
+    (optionally within the best `topk_groups` of `n_groups` expert groups) and
+    the fp32 softmax over the K picked logits."""
+    lib = _lib.load()
+    _need(logits, "logits", torch.float32, 2)
+    dev = logits.device
+    T, E = logits.shape
+    K = int(topk)
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev) if idx is None \
+        else _need(idx, "idx", torch.int32, 2, dev)
+    probs = torch.empty((T, K), dtype=torch.float32, device=dev) if probs is None \
+        else _need(probs, "probs", torch.float32, 2, dev)
+    _shape(idx, "idx", (T, K))
+    _shape(probs, "probs", (T, K))
+    with torch.cuda.device(dev):
+        _check("mp_topk_softmax", lib.mp_topk_softmax(
+            _ptr(logits), T, E, K, int(n_groups), int(topk_groups), _ptr(idx), _ptr(probs),
+            _stream(dev)))
+    return idx, probs
+
+
+def mp_topk_softmax_bwd(g_probs, probs, idx, num_experts: int, *, g_logits=None):
+    """Gradient of mp_topk_softmax w.r.t. the logits: fp32 [T,E]."""
+    lib = _lib.load()
+    _need(g_probs, "g_probs", torch.float32, 2)
+    dev = g_probs.device
+    T, K = g_probs.shape
+    _need(probs, "probs", torch.float32, 2, dev)
+    _need(idx, "idx", torch.int32, 2, dev)
+    _shape(probs, "probs", (T, K))
+    _shape(idx, "idx", (T, K))
+    E = int(num_experts)
+    g_logits = torch.empty((T, E), dtype=torch.float32, device=dev) if g_logits is None \
+        else _need(g_logits, "g_logits", torch.float32, 2, dev)
+    _shape(g_logits, "g_logits", (T, E))
+    with torch.cuda.device(dev):
+        _check("mp_topk_softmax_bwd", lib.mp_topk_softmax_bwd(
+            _ptr(g_probs), _ptr(probs), _ptr(idx), T, E, K, _ptr(g_logits), _stream(dev)))
+    return g_logits
 
 
 # --------------------------------------------------------------------------

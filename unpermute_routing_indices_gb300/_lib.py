@@ -21,6 +21,8 @@ SIGNATURES = {
     "mp_build_map": (I32, [P, I64, I32, I32, P, P, P, P, P, SZ, P, P]),
     "mp_build_map_capacity": (I32, [P, I64, I32, I32, I32, P, P, P, P, P, SZ, P, P]),
     "mp_build_map_noalloc": (I32, [P, I64, I32, I32, P, P, P, P, P, P]),
+    "mp_topk_softmax": (I32, [P, I64, I32, I32, I32, I32, P, P, P]),
+    "mp_topk_softmax_bwd": (I32, [P, P, P, I64, I32, I32, P, P]),
     "mp_permute": (I32, [P, P, P, I64, I32, I32, P, P, P]),
     "mp_unpermute": (I32, [P, P, P, I64, I32, I32, P, P]),
     "mp_unpermute_ep": (I32, [P, P, P, P, I64, I32, I32, I32, I32, I32, P, P]),

@@ -82,22 +82,27 @@ ROUTED = {
 }
 
 
+def router_logits(name: str, T: int | None = None, seed: int | None = None) -> np.ndarray:
+    """The fp32 router logits [T,E] a named routed workload draws its routing from."""
+    cfg = ROUTED[name]
+    T = cfg["T"] if T is None else T
+    rng = _rng(cfg["seed"] if seed is None else seed)
+    E = cfg["E"]
+    if cfg["kind"] == "zipf":
+        bias = zipf_bias(rng, E)
+        return (rng.standard_normal((T, E), dtype=np.float32) + bias[None, :]).astype(np.float32)
+    return rng.standard_normal((T, E), dtype=np.float32)
+
+
 def routing(name: str, T: int | None = None, seed: int | None = None):
     """(idx[T,K] int32, probs[T,K] f32, E) for a named routed workload.
     T may be overridden (a leading slice of the same distribution)."""
     cfg = ROUTED[name]
-    T = cfg["T"] if T is None else T
-    rng = _rng(cfg["seed"] if seed is None else seed)
     E, K = cfg["E"], cfg["K"]
-    if cfg["kind"] == "zipf":
-        bias = zipf_bias(rng, E)
-        logits = rng.standard_normal((T, E), dtype=np.float32) + bias[None, :]
-        idx, probs = topk_softmax(logits, K)
-    elif cfg["kind"] == "grouped":
-        logits = rng.standard_normal((T, E), dtype=np.float32)
+    logits = router_logits(name, T=T, seed=seed)
+    if cfg["kind"] == "grouped":
         idx, probs = group_limited_topk(logits, K, cfg["n_groups"], cfg["topk_groups"])
     else:
-        logits = rng.standard_normal((T, E), dtype=np.float32)
         idx, probs = topk_softmax(logits, K)
     return idx, probs, E
 
