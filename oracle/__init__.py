@@ -40,7 +40,8 @@ def build(force: bool = False) -> str:
 
 class _Flags(ctypes.Structure):
     _fields_ = [("bad_split", ctypes.c_int32), ("bad_order", ctypes.c_int32),
-                ("split_overflow", ctypes.c_int32), ("rows_overflow", ctypes.c_int32)]
+                ("split_overflow", ctypes.c_int32), ("rows_overflow", ctypes.c_int32),
+                ("bad_padded", ctypes.c_int32)]
 
 
 def _load():
@@ -75,7 +76,7 @@ def _load():
         lib.orc_permute_bwd.restype = None
         lib.orc_unpermute_bwd.argtypes = [P, P, P, P, i64, i32, i32, P, P]
         lib.orc_unpermute_bwd.restype = None
-        lib.orc_sort_chunks_pad.argtypes = [P, P, P, P, i32, i32, i32, i64, i64, i32,
+        lib.orc_sort_chunks_pad.argtypes = [P, P, P, P, P, i32, i32, i32, i64, i64, i32,
                                             P, P, P, P, ctypes.POINTER(_Flags)]
         lib.orc_sort_chunks_pad.restype = None
         for name in ("orc_unpad_restore", "orc_sort_chunks_pad_bwd",
@@ -265,42 +266,54 @@ def topk_softmax_bwd(g_probs, probs, idx, E):
 # chunk sort + pad, unpad + restore
 # --------------------------------------------------------------------------
 
-def sort_chunks_pad(x, probs, split_sizes, chunk_order, G, align, out_rows):
-    """Returns (out, out_probs, row_map, group_off[G+1] int64, flags dict)."""
+def as_units(rows: np.ndarray) -> np.ndarray:
+    """A [N, ...] array of 2- or 4-byte elements as [N, W] uint16 units (the
+    chunk functions only move bits)."""
+    a = np.ascontiguousarray(rows)
+    return a.reshape(a.shape[0], -1).view(np.uint16)
+
+
+def sort_chunks_pad(x, probs, split_sizes, chunk_order, G, align, out_rows, padded_sizes=None):
+    """Returns (out, out_probs, row_map, group_off[G+1] int64, flags dict).
+    x may be bf16 / fp16 bits (uint16) or float32 rows; out has x's dtype."""
     lib = _load()
-    x = _c(x, np.uint16)
+    dtype = np.asarray(x).dtype
+    xu = as_units(x)
     probs = _c(probs, np.float32)
     split_sizes = _c(split_sizes, np.int32)
     chunk_order = _c(chunk_order, np.int32)
-    N, H = x.shape
+    padded_sizes = _c(padded_sizes, np.int32)
+    N, W = xu.shape
     C = split_sizes.shape[0]
-    out = np.empty((out_rows, H), np.uint16)
+    out = np.empty((out_rows, W), np.uint16)
     out_probs = np.empty(out_rows, np.float32) if probs is not None else None
     row_map = np.empty(out_rows, np.int32)
     group_off = np.empty(G + 1, np.int64)
     flags = _Flags()
-    lib.orc_sort_chunks_pad(_p(x), _p(probs), _p(split_sizes), _p(chunk_order), C, G,
-                            align, N, out_rows, H, _p(out), _p(out_probs), _p(row_map),
-                            _p(group_off), ctypes.byref(flags))
+    lib.orc_sort_chunks_pad(_p(xu), _p(probs), _p(split_sizes), _p(chunk_order),
+                            _p(padded_sizes), C, G, align, N, out_rows, W, _p(out),
+                            _p(out_probs), _p(row_map), _p(group_off), ctypes.byref(flags))
     fl = {name: int(getattr(flags, name)) for name, _ in _Flags._fields_}
-    return out, out_probs, row_map, group_off, fl
+    return out.view(dtype).reshape((out_rows,) + np.asarray(x).shape[1:]), out_probs, \
+        row_map, group_off, fl
 
 
 def _rowmap_call(name, src, src_probs, row_map, N, out_shape_rows, init):
     lib = _load()
-    src = _c(src, np.uint16)
+    dtype = np.asarray(src).dtype
+    su = as_units(src)
     src_probs = _c(src_probs, np.float32)
     row_map = _c(row_map, np.int32)
-    H = src.shape[1]
-    out = np.array(init[0], dtype=np.uint16, copy=True) if init is not None else \
-        np.zeros((out_shape_rows, H), np.uint16)
+    W = su.shape[1]
+    out = as_units(np.array(init[0], copy=True)).copy() if init is not None else \
+        np.zeros((out_shape_rows, W), np.uint16)
     out_probs = None
     if src_probs is not None:
         out_probs = np.array(init[1], dtype=np.float32, copy=True) if init is not None \
             else np.zeros(out_shape_rows, np.float32)
-    getattr(lib, name)(_p(src), _p(src_probs), _p(row_map), row_map.shape[0], N, H,
+    getattr(lib, name)(_p(su), _p(src_probs), _p(row_map), row_map.shape[0], N, W,
                        _p(out), _p(out_probs))
-    return out, out_probs
+    return out.view(dtype).reshape((out_shape_rows,) + np.asarray(src).shape[1:]), out_probs
 
 
 def unpad_restore(padded, padded_probs, row_map, N, init=None):
@@ -315,13 +328,15 @@ def sort_chunks_pad_bwd(g_out, g_out_probs, row_map, N, init=None):
 
 def unpad_restore_bwd(g_y, g_y_probs, row_map, N):
     lib = _load()
-    g_y = _c(g_y, np.uint16)
+    dtype = np.asarray(g_y).dtype
+    gu = as_units(g_y)
     g_y_probs = _c(g_y_probs, np.float32)
     row_map = _c(row_map, np.int32)
     out_rows = row_map.shape[0]
-    H = g_y.shape[1]
-    g_padded = np.empty((out_rows, H), np.uint16)
+    W = gu.shape[1]
+    g_padded = np.empty((out_rows, W), np.uint16)
     g_padded_probs = np.empty(out_rows, np.float32) if g_y_probs is not None else None
-    lib.orc_unpad_restore_bwd(_p(g_y), _p(g_y_probs), _p(row_map), out_rows, N, H,
+    lib.orc_unpad_restore_bwd(_p(gu), _p(g_y_probs), _p(row_map), out_rows, N, W,
                               _p(g_padded), _p(g_padded_probs))
-    return g_padded, g_padded_probs
+    return g_padded.view(dtype).reshape((out_rows,) + np.asarray(g_y).shape[1:]), \
+        g_padded_probs

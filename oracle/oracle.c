@@ -487,9 +487,13 @@ typedef struct {
     int32_t bad_order;      /* some chunk_order entry outside [0,C) (skipped)  */
     int32_t split_overflow; /* sum of split sizes > N (rows >= N not read)     */
     int32_t rows_overflow;  /* sum of padded group sizes > out_rows (dropped)  */
+    int32_t bad_padded;     /* a given padded size below its group's rows      */
 } orc_chunk_flags;
 
 /*
+ * Rows here are W 16-bit units wide: H for bf16 / fp16 tokens, 2H for fp32
+ * (the copies only move bits, so the element type does not matter).
+ *
  * Fused sort + pad: input rows arrive as C consecutive chunks whose sizes are
  * split_sizes (input order).  The output holds G groups; group g is made of
  * the chunks chunk_order[g*C/G .. (g+1)*C/G) in that order, each chunk's rows
@@ -499,15 +503,19 @@ typedef struct {
  * group_off[G] the padded total.  row_map[d] is the input row placed at output
  * row d, or -1 for a padding row; output rows from group_off[G] to out_rows
  * are padding too.  Padding rows are zero and their probabilities 0.
- * probs / out_probs may be NULL together.
+ * probs / out_probs may be NULL together.  With padded_sizes given ("padded
+ * sizes are explicit", [TE-PR, Description]), group g takes exactly
+ * padded_sizes[g] rows instead (negative counts as 0); a group with more rows
+ * than that keeps its first padded_sizes[g] rows and is flagged.
  */
 void orc_sort_chunks_pad(const uint16_t *x, const float *probs,
                          const int32_t *split_sizes, const int32_t *chunk_order,
-                         int32_t C, int32_t G, int32_t align, int64_t N,
-                         int64_t out_rows, int32_t H, uint16_t *out, float *out_probs,
-                         int32_t *row_map, int64_t *group_off, orc_chunk_flags *flags)
+                         const int32_t *padded_sizes, int32_t C, int32_t G, int32_t align,
+                         int64_t N, int64_t out_rows, int32_t H, uint16_t *out,
+                         float *out_probs, int32_t *row_map, int64_t *group_off,
+                         orc_chunk_flags *flags)
 {
-    orc_chunk_flags f = {0, 0, 0, 0};
+    orc_chunk_flags f = {0, 0, 0, 0, 0};
     int64_t *in_start = (int64_t *)malloc(sizeof(int64_t) * (size_t)(C > 0 ? C : 1));
     int64_t total = 0;
     for (int32_t c = 0; c < C; ++c) {
@@ -535,7 +543,21 @@ void orc_sort_chunks_pad(const uint16_t *x, const float *probs,
     int64_t d = 0;
     for (int32_t g = 0; g < G; ++g) {
         group_off[g] = d;
+        /* rows the group holds before padding */
         int64_t rows_in_group = 0;
+        for (int32_t j = 0; j < per_group; ++j) {
+            int32_t c = chunk_order[g * per_group + j];
+            if (c >= 0 && c < C && split_sizes[c] > 0)
+                rows_in_group += split_sizes[c];
+        }
+        int64_t padded = ((rows_in_group + align - 1) / align) * align;
+        if (padded_sizes) {
+            padded = padded_sizes[g] < 0 ? 0 : padded_sizes[g];
+            if (padded < rows_in_group)
+                f.bad_padded = 1;
+        }
+        /* place the rows in order, as many as the padded size holds */
+        int64_t placed = 0;
         for (int32_t j = 0; j < per_group; ++j) {
             int32_t c = chunk_order[g * per_group + j];
             if (c < 0 || c >= C) {
@@ -543,21 +565,20 @@ void orc_sort_chunks_pad(const uint16_t *x, const float *probs,
                 continue;
             }
             int64_t s = split_sizes[c] < 0 ? 0 : split_sizes[c];
-            for (int64_t i = 0; i < s; ++i) {
+            for (int64_t i = 0; i < s && placed < padded; ++i) {
                 int64_t src = in_start[c] + i;
-                if (d < out_rows && src < N) {
-                    row_map[d] = (int32_t)src;
+                int64_t dd = d + placed;
+                if (dd < out_rows && src < N) {
+                    row_map[dd] = (int32_t)src;
                     for (int32_t h = 0; h < H; ++h)
-                        out[d * H + h] = x[src * H + h];
+                        out[dd * H + h] = x[src * H + h];
                     if (probs && out_probs)
-                        out_probs[d] = probs[src];
+                        out_probs[dd] = probs[src];
                 }
-                d += 1;
-                rows_in_group += 1;
+                placed += 1;
             }
         }
-        int64_t padded = ((rows_in_group + align - 1) / align) * align;
-        d += padded - rows_in_group;
+        d += padded;
     }
     group_off[G] = d;
     if (d > out_rows)

@@ -660,3 +660,65 @@ def test_topk_softmax_bwd_is_the_softmax_jacobian():
         mask[idx[t]] = False
         assert np.all(gl[t, mask] == 0)
         assert abs(got.sum()) < 1e-6
+
+
+# --------------------------------------------------------------------------
+# chunk sort + pad: explicit padded sizes, other token types
+# --------------------------------------------------------------------------
+
+def _brute_sort_pad_sizes(x, probs, sizes, order, G, padded_sizes, out_rows):
+    N = x.shape[0]
+    C = len(sizes)
+    starts = np.concatenate([[0], np.cumsum(np.maximum(sizes, 0))])
+    rows, offs = [], []
+    for g in range(G):
+        offs.append(len(rows))
+        grp = []
+        for c in order[g * (C // G):(g + 1) * (C // G)]:
+            grp += list(range(starts[c], starts[c] + max(sizes[c], 0)))
+        ps = max(int(padded_sizes[g]), 0)
+        grp = grp[:ps]
+        rows += grp + [-1] * (ps - len(grp))
+    offs.append(len(rows))
+    rows = [r if r < N else -1 for r in rows]
+    row_map = np.array((rows + [-1] * out_rows)[:out_rows], np.int32)
+    out = np.zeros((out_rows,) + x.shape[1:], x.dtype)
+    ok = row_map >= 0
+    out[ok] = x[row_map[ok]]
+    return out, row_map, np.array(offs, np.int64)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_sort_chunks_pad_explicit_sizes_brute_force(seed):
+    rng = np.random.default_rng(200 + seed)
+    G, R = int(rng.integers(1, 5)), int(rng.integers(1, 4))
+    C = G * R
+    sizes = rng.integers(0, 6, size=C).astype(np.int32)
+    order = rng.permutation(C).astype(np.int32)
+    N = int(sizes.sum())
+    x = rng.standard_normal((N, 3)).astype(np.float32)          # fp32 tokens
+    probs = rng.random(N).astype(np.float32)
+    grows = np.array([sizes[order[g * R:(g + 1) * R]].sum() for g in range(G)])
+    padded = (grows + rng.integers(-2, 5, size=G)).astype(np.int32)   # some too small
+    out_rows = int(np.maximum(padded, 0).sum() + rng.integers(0, 3))
+    out, out_p, rm, off, fl = oracle.sort_chunks_pad(x, probs, sizes, order, G, 1, out_rows,
+                                                     padded_sizes=padded)
+    want_out, want_rm, want_off = _brute_sort_pad_sizes(x, probs, sizes, order, G, padded,
+                                                        out_rows)
+    np.testing.assert_array_equal(out.view(np.uint32), want_out.view(np.uint32))
+    np.testing.assert_array_equal(rm, want_rm)
+    np.testing.assert_array_equal(off, want_off)
+    assert fl["bad_padded"] == int(np.any(padded < grows))
+
+
+def test_sort_chunks_pad_is_dtype_agnostic():
+    rng = np.random.default_rng(9)
+    sizes = np.array([3, 0, 4, 2], np.int32)
+    order = np.array([2, 0, 3, 1], np.int32)
+    x32 = rng.standard_normal((9, 5)).astype(np.float32)
+    x16 = x32.view(np.uint16)                                   # same bits, 2x wider
+    a = oracle.sort_chunks_pad(x32, None, sizes, order, 2, 4, 16)
+    b = oracle.sort_chunks_pad(x16, None, sizes, order, 2, 4, 16)
+    np.testing.assert_array_equal(a[0].view(np.uint16), b[0])
+    y, _ = oracle.unpad_restore(a[0], None, a[2], 9)
+    np.testing.assert_array_equal(y.view(np.uint32), x32.view(np.uint32))
