@@ -478,7 +478,7 @@ def bench_chunks(mp, wl, dev, flush, args):
 
     res = {}
     stream = torch.cuda.current_stream(dev)
-    for N in (8192, 32768):
+    for N, tdt in ((8192, torch.bfloat16), (32768, torch.bfloat16), (32768, torch.float32)):
         c = wl.chunks(N)
         G, align, H = c["G"], c["align"], c["H"]
         out_rows = wl.padded_rows_bound(N, G, align)
@@ -490,11 +490,13 @@ def bench_chunks(mp, wl, dev, flush, args):
             return tt.to(dev)
 
         x, p, sz, od = t(c["x"]), t(c["probs"]), t(c["split_sizes"]), t(c["chunk_order"])
-        out = torch.empty((out_rows, H), dtype=torch.bfloat16, device=dev)
+        x = x.to(tdt)
+        esize = x.element_size()
+        out = torch.empty((out_rows, H), dtype=tdt, device=dev)
         out_p = torch.empty(out_rows, dtype=torch.float32, device=dev)
         row_map = torch.empty(out_rows, dtype=torch.int32, device=dev)
         goff = torch.empty(G + 1, dtype=torch.int64, device=dev)
-        y = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        y = torch.empty((N, H), dtype=tdt, device=dev)
         y_p = torch.empty(N, dtype=torch.float32, device=dev)
 
         def roundtrip():
@@ -520,13 +522,15 @@ def bench_chunks(mp, wl, dev, flush, args):
         ur = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
         rt = statistics.median(e[0].elapsed_time(e[2]) for e in evs)
         padded = int(goff[-1].item())
-        b = chunk_bytes(N, H, padded, out_rows)
-        res[str(N)] = {"roundtrip_ms": round(rt, 4), "sort_pad_us": round(sp * 1e3, 2),
-                       "unpad_restore_us": round(ur * 1e3, 2),
-                       "roundtrip_GB/s": round((b["sort_chunks_pad"] + b["unpad_restore"])
-                                               / (rt * 1e-3) / 1e9, 1),
-                       "out_rows": out_rows, "padded_rows": padded,
-                       "published_b200_fused_ms": {8192: 0.1717, 32768: 0.2029}[N]}
+        b = chunk_bytes(N, H * esize // 2, padded, out_rows)
+        key = str(N) if tdt == torch.bfloat16 else f"{N} fp32"
+        res[key] = {"roundtrip_ms": round(rt, 4), "sort_pad_us": round(sp * 1e3, 2),
+                    "unpad_restore_us": round(ur * 1e3, 2),
+                    "roundtrip_GB/s": round((b["sort_chunks_pad"] + b["unpad_restore"])
+                                            / (rt * 1e-3) / 1e9, 1),
+                    "out_rows": out_rows, "padded_rows": padded}
+        if tdt == torch.bfloat16:
+            res[key]["published_b200_fused_ms"] = {8192: 0.1717, 32768: 0.2029}[N]
     return res
 
 

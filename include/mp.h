@@ -70,6 +70,12 @@ typedef void *mp_stream_t;    /* a cudaStream_t                             */
 #define MP_STATUS_SPLIT_OVERFLOW 0x8 /* sum of split sizes > N: rows >= N unread */
 #define MP_STATUS_ROWS_OVERFLOW 0x10 /* padded total > out_rows: excess dropped  */
 #define MP_STATUS_BAD_ROW 0x20       /* row_map entry outside [-1,N): skipped    */
+#define MP_STATUS_BAD_PADDED 0x40    /* a padded size below its group's rows     */
+
+/* Token types of the chunk entry points with a dtype argument. */
+#define MP_DTYPE_BF16 0
+#define MP_DTYPE_FP16 1
+#define MP_DTYPE_FP32 2
 
 #define MP_MAX_EXPERTS 1024
 #define MP_MAX_CHUNKS 1024
@@ -331,6 +337,35 @@ mp_status_t mp_unpad_restore_bwd(const mp_bf16_t *g_y, const float *g_y_probs,
                                  const int32_t *row_map, int64_t out_rows, int64_t N,
                                  int32_t H, mp_bf16_t *g_padded, float *g_padded_probs,
                                  int32_t *dev_status, mp_stream_t stream);
+
+/*
+ * The chunk entry points for FP32, FP16 and BF16 tokens ([TE-PR Changes]):
+ * `dtype` is an MP_DTYPE_*, rows are H elements of that type, and the other
+ * arguments are those of the bf16 entry points above.  mp_sort_chunks_pad_ex
+ * also takes padded_sizes, device int32 [G] or NULL ("Chunk order and padded
+ * sizes are explicit", [TE-PR Description]): when given, group g occupies
+ * exactly padded_sizes[g] output rows (a negative size counts as 0; `align`
+ * is then unused), and a group with more rows keeps its first
+ * padded_sizes[g] rows and sets MP_STATUS_BAD_PADDED.
+ */
+mp_status_t mp_sort_chunks_pad_ex(const void *x, int32_t dtype, const float *probs,
+                                  const int32_t *split_sizes, const int32_t *chunk_order,
+                                  const int32_t *padded_sizes, int32_t C, int32_t G,
+                                  int32_t align, int64_t N, int64_t out_rows, int32_t H,
+                                  void *out, float *out_probs, int32_t *row_map,
+                                  int64_t *group_off, int32_t *dev_status, mp_stream_t stream);
+mp_status_t mp_unpad_restore_ex(const void *padded, int32_t dtype, const float *padded_probs,
+                                const int32_t *row_map, int64_t out_rows, int64_t N, int32_t H,
+                                void *y, float *y_probs, int32_t *dev_status,
+                                mp_stream_t stream);
+mp_status_t mp_sort_chunks_pad_bwd_ex(const void *g_out, int32_t dtype,
+                                      const float *g_out_probs, const int32_t *row_map,
+                                      int64_t out_rows, int64_t N, int32_t H, void *g_x,
+                                      float *g_probs, int32_t *dev_status, mp_stream_t stream);
+mp_status_t mp_unpad_restore_bwd_ex(const void *g_y, int32_t dtype, const float *g_y_probs,
+                                    const int32_t *row_map, int64_t out_rows, int64_t N,
+                                    int32_t H, void *g_padded, float *g_padded_probs,
+                                    int32_t *dev_status, mp_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -145,3 +145,71 @@ def test_bulk_engine_many_rounds_per_cta():
     np.testing.assert_array_equal(h(y_p), probs)
     g_pad, _ = mp.mp_unpad_restore_bwd(d(x), row_map)
     np.testing.assert_array_equal(h(g_pad), h(out))
+
+
+# --------------------------------------------------------------------------
+# fp16 / fp32 tokens and caller-supplied padded sizes
+# --------------------------------------------------------------------------
+
+def _dev_tokens(x_np):
+    t = torch.from_numpy(np.ascontiguousarray(x_np))
+    return t.to(DEV)
+
+
+@pytest.mark.parametrize("dtype,H", [(np.float32, 2048), (np.float16, 2048), (np.float32, 5),
+                                     (np.float16, 37)])
+def test_sort_pad_roundtrip_other_token_types(dtype, H):
+    N = 8192 if H > 64 else 3000
+    c = wl.chunks(N, H=8)                               # sizes and order only
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal((N, H)).astype(dtype)
+    G, align = c["G"], c["align"]
+    out_rows = wl.padded_rows_bound(N, G, align)
+    st = status_word()
+    out, out_p, row_map, goff = mp.mp_sort_chunks_pad(
+        _dev_tokens(x), d(c["split_sizes"]), d(c["chunk_order"]), G, align, out_rows,
+        d(c["probs"]), status=st)
+    o_out, o_p, o_map, o_goff, _ = oracle.sort_chunks_pad(x, c["probs"], c["split_sizes"],
+                                                          c["chunk_order"], G, align, out_rows)
+    got = out.cpu().numpy()
+    np.testing.assert_array_equal(got.view(np.uint16), o_out.view(np.uint16))
+    np.testing.assert_array_equal(h(row_map), o_map)
+    np.testing.assert_array_equal(h(goff), o_goff)
+    assert int(h(st)[0]) == 0
+    y, _ = mp.mp_unpad_restore(out, row_map, N, out_p)
+    np.testing.assert_array_equal(y.cpu().numpy().view(np.uint16), x.view(np.uint16))
+    g_pad, _ = mp.mp_unpad_restore_bwd(_dev_tokens(x), row_map)
+    np.testing.assert_array_equal(g_pad.cpu().numpy().view(np.uint16), got.view(np.uint16))
+    g_x, _ = mp.mp_sort_chunks_pad_bwd(out, row_map, N)
+    np.testing.assert_array_equal(g_x.cpu().numpy().view(np.uint16), x.view(np.uint16))
+
+
+@pytest.mark.parametrize("slack", ["exact", "larger", "smaller"])
+def test_sort_pad_explicit_padded_sizes(slack):
+    N, H = 8192, 2048
+    c = wl.chunks(N)
+    G, R = c["G"], c["C"] // c["G"]
+    sizes, order = c["split_sizes"], c["chunk_order"]
+    grows = np.array([sizes[order[g * R:(g + 1) * R]].sum() for g in range(G)])
+    rng = np.random.default_rng(23)
+    if slack == "exact":
+        padded = grows
+    elif slack == "larger":
+        padded = grows + rng.integers(0, 300, size=G)
+    else:
+        padded = grows - rng.integers(0, 40, size=G)
+        padded[3] = -5                                   # negative: an empty group
+    padded = padded.astype(np.int32)
+    out_rows = int(np.maximum(padded, 0).sum()) + 10
+    st = status_word()
+    out, out_p, row_map, goff = mp.mp_sort_chunks_pad(
+        d(c["x"]), d(sizes), d(order), G, 1, out_rows, d(c["probs"]), padded_sizes=d(padded),
+        status=st)
+    o_out, o_p, o_map, o_goff, fl = oracle.sort_chunks_pad(c["x"], c["probs"], sizes, order, G,
+                                                           1, out_rows, padded_sizes=padded)
+    np.testing.assert_array_equal(h(out), o_out)
+    np.testing.assert_array_equal(h(out_p), o_p)
+    np.testing.assert_array_equal(h(row_map), o_map)
+    np.testing.assert_array_equal(h(goff), o_goff)
+    assert mp.status_bits(int(h(st)[0])) == {k for k, v in fl.items() if v}
+    assert (slack == "smaller") == bool(fl["bad_padded"])

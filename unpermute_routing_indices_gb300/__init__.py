@@ -26,10 +26,11 @@ __all__ = [
 
 STATUS_BITS = {
     "bad_expert": 0x1, "bad_split": 0x2, "bad_order": 0x4, "split_overflow": 0x8,
-    "rows_overflow": 0x10, "bad_row": 0x20,
+    "rows_overflow": 0x10, "bad_row": 0x20, "bad_padded": 0x40,
 }
 
 
+DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}   # MP_DTYPE_*
 EP_BF16_PARTIALS = 0x1
 EP_FP64_CROSS_RANK = 0x2
 
@@ -349,22 +350,33 @@ def mp_unpermute_bwd(g_y, row_id_map, rows=None, probs=None, *, num_out_rows=Non
 # chunk sort + pad, unpad + restore
 # --------------------------------------------------------------------------
 
+def _token_dtype(t, name):
+    if not isinstance(t, torch.Tensor) or t.dtype not in DTYPES:
+        raise TypeError(f"{name} must be a bf16, fp16 or fp32 tensor")
+    return DTYPES[t.dtype]
+
+
 def mp_sort_chunks_pad(x, split_sizes, chunk_order, num_groups: int, align: int,
-                       out_rows: int, probs=None, *, out=None, out_probs=None, row_map=None,
-                       group_off=None, status=None):
-    """x bf16 [N,H] -> (out [out_rows,H], out_probs or None, row_map int32 [out_rows],
-    group_off int64 [G+1])."""
+                       out_rows: int, probs=None, *, padded_sizes=None, out=None,
+                       out_probs=None, row_map=None, group_off=None, status=None):
+    """x [N,H] (bf16, fp16 or fp32) -> (out [out_rows,H], out_probs or None,
+    row_map int32 [out_rows], group_off int64 [G+1]).  padded_sizes (int32 [G])
+    fixes each group's row count instead of rounding up to `align`."""
     lib = _lib.load()
-    _need(x, "x", torch.bfloat16, 2)
+    dt = _token_dtype(x, "x")
+    _need(x, "x", x.dtype, 2)
     dev = x.device
     N, H = x.shape
     _need(split_sizes, "split_sizes", torch.int32, 1, dev)
     _need(chunk_order, "chunk_order", torch.int32, 1, dev)
     C, G = split_sizes.shape[0], int(num_groups)
     _shape(chunk_order, "chunk_order", (C,))
+    if padded_sizes is not None:
+        _need(padded_sizes, "padded_sizes", torch.int32, 1, dev)
+        _shape(padded_sizes, "padded_sizes", (G,))
     _opt(probs, "probs", torch.float32, 1, dev)
-    out = torch.empty((out_rows, H), dtype=torch.bfloat16, device=dev) if out is None \
-        else _need(out, "out", torch.bfloat16, 2, dev)
+    out = torch.empty((out_rows, H), dtype=x.dtype, device=dev) if out is None \
+        else _need(out, "out", x.dtype, 2, dev)
     if probs is not None and out_probs is None:
         out_probs = torch.empty(out_rows, dtype=torch.float32, device=dev)
     if probs is None:
@@ -375,22 +387,30 @@ def mp_sort_chunks_pad(x, split_sizes, chunk_order, num_groups: int, align: int,
         else _need(group_off, "group_off", torch.int64, 1, dev)
     _opt(status, "status", torch.int32, 1, dev)
     with torch.cuda.device(dev):
-        _check("mp_sort_chunks_pad", lib.mp_sort_chunks_pad(
-            _ptr(x), _ptr(probs), _ptr(split_sizes), _ptr(chunk_order), C, G, int(align), N,
-            int(out_rows), H, _ptr(out), _ptr(out_probs), _ptr(row_map), _ptr(group_off),
-            _ptr(status), _stream(dev)))
+        if dt == 0 and padded_sizes is None:
+            code = lib.mp_sort_chunks_pad(
+                _ptr(x), _ptr(probs), _ptr(split_sizes), _ptr(chunk_order), C, G, int(align), N,
+                int(out_rows), H, _ptr(out), _ptr(out_probs), _ptr(row_map), _ptr(group_off),
+                _ptr(status), _stream(dev))
+        else:
+            code = lib.mp_sort_chunks_pad_ex(
+                _ptr(x), dt, _ptr(probs), _ptr(split_sizes), _ptr(chunk_order),
+                _ptr(padded_sizes), C, G, int(align), N, int(out_rows), H, _ptr(out),
+                _ptr(out_probs), _ptr(row_map), _ptr(group_off), _ptr(status), _stream(dev))
+        _check("mp_sort_chunks_pad", code)
     return out, out_probs, row_map, group_off
 
 
 def _remap(name, src, row_map, n_rows, src_probs, out, out_probs, status, gather):
     lib = _lib.load()
-    _need(src, "input", torch.bfloat16, 2)
+    dt = _token_dtype(src, "input")
+    _need(src, "input", src.dtype, 2)
     dev = src.device
     _need(row_map, "row_map", torch.int32, 1, dev)
     H = src.shape[1]
     rows_out = row_map.shape[0] if gather else n_rows
-    out = torch.empty((rows_out, H), dtype=torch.bfloat16, device=dev) if out is None \
-        else _need(out, "out", torch.bfloat16, 2, dev)
+    out = torch.empty((rows_out, H), dtype=src.dtype, device=dev) if out is None \
+        else _need(out, "out", src.dtype, 2, dev)
     _opt(src_probs, "probs", torch.float32, 1, dev)
     if src_probs is not None and out_probs is None:
         out_probs = torch.empty(rows_out, dtype=torch.float32, device=dev)
@@ -398,9 +418,15 @@ def _remap(name, src, row_map, n_rows, src_probs, out, out_probs, status, gather
         out_probs = None
     _opt(status, "status", torch.int32, 1, dev)
     with torch.cuda.device(dev):
-        _check(name, getattr(lib, name)(
-            _ptr(src), _ptr(src_probs), _ptr(row_map), row_map.shape[0], int(n_rows), H,
-            _ptr(out), _ptr(out_probs), _ptr(status), _stream(dev)))
+        if dt == 0:
+            code = getattr(lib, name)(
+                _ptr(src), _ptr(src_probs), _ptr(row_map), row_map.shape[0], int(n_rows), H,
+                _ptr(out), _ptr(out_probs), _ptr(status), _stream(dev))
+        else:
+            code = getattr(lib, name + "_ex")(
+                _ptr(src), dt, _ptr(src_probs), _ptr(row_map), row_map.shape[0], int(n_rows), H,
+                _ptr(out), _ptr(out_probs), _ptr(status), _stream(dev))
+        _check(name, code)
     return out, out_probs
 
 

@@ -32,6 +32,11 @@ SIGNATURES = {
     "mp_unpad_restore": (I32, [P, P, P, I64, I64, I32, P, P, P, P]),
     "mp_sort_chunks_pad_bwd": (I32, [P, P, P, I64, I64, I32, P, P, P, P]),
     "mp_unpad_restore_bwd": (I32, [P, P, P, I64, I64, I32, P, P, P, P]),
+    "mp_sort_chunks_pad_ex": (I32, [P, I32, P, P, P, P, I32, I32, I32, I64, I64, I32, P, P, P, P,
+                                    P, P]),
+    "mp_unpad_restore_ex": (I32, [P, I32, P, P, I64, I64, I32, P, P, P, P]),
+    "mp_sort_chunks_pad_bwd_ex": (I32, [P, I32, P, P, I64, I64, I32, P, P, P, P]),
+    "mp_unpad_restore_bwd_ex": (I32, [P, I32, P, P, I64, I64, I32, P, P, P, P]),
 }
 
 

@@ -108,7 +108,8 @@ __device__ __forceinline__ void copy_rows(const V *__restrict__ in, V *__restric
 template <typename V>
 __global__ void __launch_bounds__(CH_THREADS)
     k_sort_pad(const V *__restrict__ x, const float *__restrict__ probs,
-               const int32_t *__restrict__ split, const int32_t *__restrict__ order, int C, int G,
+               const int32_t *__restrict__ split, const int32_t *__restrict__ order,
+               const int32_t *__restrict__ padded_sizes, int C, int G,
                int align, int64_t N, int64_t out_rows, int nvec, V *__restrict__ out,
                float *__restrict__ out_probs, int32_t *__restrict__ row_map,
                int64_t *__restrict__ group_off, int32_t *status)
@@ -152,7 +153,13 @@ __global__ void __launch_bounds__(CH_THREADS)
     for (int g = tid; g < G; g += CH_THREADS) {
         const int64_t rows = s_cum[(g + 1) * per_group] - s_cum[g * per_group];
         s_grows[g] = rows;
-        s_goff[g] = (rows + align - 1) / align * align;
+        int64_t padded = (rows + align - 1) / align * align;
+        if (padded_sizes != nullptr) {   // explicit padded sizes
+            const int32_t ps = padded_sizes[g];
+            padded = ps < 0 ? 0 : ps;
+            if (padded < rows) atomicOr(&s_flags, MP_STATUS_BAD_PADDED);
+        }
+        s_goff[g] = padded;
     }
     __syncthreads();
     const int64_t total_pad = cta_exclusive_scan(s_goff, G, s_warp);
@@ -238,6 +245,7 @@ inline size_t sort_pad_smem(int C, int G)
            sizeof(int32_t) * (size_t)(C + CH_ROWS);
 }
 
+// Rows are H 16-bit units wide.
 mp_status_t remap(const void *in, const float *in_probs, const int32_t *map, int64_t out_rows,
                   int64_t N, int32_t H, void *out, float *out_probs, int32_t *status,
                   cudaStream_t s, bool scatter)
@@ -272,6 +280,56 @@ mp_status_t remap(const void *in, const float *in_probs, const int32_t *map, int
     return check_launch();
 }
 
+inline int elem_units(int32_t dtype)
+{
+    switch (dtype) {
+    case MP_DTYPE_BF16:
+    case MP_DTYPE_FP16: return 1;
+    case MP_DTYPE_FP32: return 2;
+    default: return 0;
+    }
+}
+
+// Rows are W 16-bit units wide (H for 2-byte types, 2H for fp32).
+mp_status_t sort_pad_impl(const void *x, const float *probs, const int32_t *split_sizes,
+                          const int32_t *chunk_order, const int32_t *padded_sizes, int32_t C,
+                          int32_t G, int32_t align, int64_t N, int64_t out_rows, int64_t W,
+                          void *out, float *out_probs, int32_t *row_map, int64_t *group_off,
+                          int32_t *dev_status, cudaStream_t s)
+{
+    if (C < 1 || G < 1 || align < 1 || N < 0 || out_rows < 0 || W < 1) return MP_ERR_INVALID_ARG;
+    if (C % G != 0) return MP_ERR_INVALID_ARG;
+    if (C > MP_MAX_CHUNKS || N > INT32_MAX || out_rows > INT32_MAX || W > INT32_MAX)
+        return MP_ERR_UNSUPPORTED;
+    if (split_sizes == nullptr || chunk_order == nullptr || group_off == nullptr)
+        return MP_ERR_INVALID_ARG;
+    if ((probs == nullptr) != (out_probs == nullptr)) return MP_ERR_INVALID_ARG;
+    if (out_rows > 0 && (out == nullptr || row_map == nullptr)) return MP_ERR_INVALID_ARG;
+    if (N > 0 && x == nullptr) return MP_ERR_INVALID_ARG;
+    const unsigned blocks = out_rows > 0 ? (unsigned)((out_rows + CH_ROWS - 1) / CH_ROWS) : 1u;
+    const size_t smem = sort_pad_smem(C, G);
+    const int32_t w = (int32_t)W;
+    if (chunk_vec_ok(w, {x, out}))
+        k_sort_pad<uint4><<<blocks, CH_THREADS, smem, s>>>(
+            (const uint4 *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N,
+            out_rows, w / 8, (uint4 *)out, out_probs, row_map, group_off, dev_status);
+    else
+        k_sort_pad<uint16_t><<<blocks, CH_THREADS, smem, s>>>(
+            (const uint16_t *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N,
+            out_rows, w, (uint16_t *)out, out_probs, row_map, group_off, dev_status);
+    return check_launch();
+}
+
+mp_status_t remap_ex(const void *in, int32_t dtype, const float *in_probs, const int32_t *map,
+                     int64_t out_rows, int64_t N, int32_t H, void *out, float *out_probs,
+                     int32_t *status, cudaStream_t s, bool scatter)
+{
+    const int u = elem_units(dtype);
+    if (u == 0 || H < 1) return MP_ERR_INVALID_ARG;
+    if ((int64_t)H * u > INT32_MAX) return MP_ERR_UNSUPPORTED;
+    return remap(in, in_probs, map, out_rows, N, H * u, out, out_probs, status, s, scatter);
+}
+
 }  // namespace
 }  // namespace mp
 
@@ -284,26 +342,25 @@ extern "C" mp_status_t mp_sort_chunks_pad(const mp_bf16_t *x, const float *probs
                                           float *out_probs, int32_t *row_map, int64_t *group_off,
                                           int32_t *dev_status, mp_stream_t stream)
 {
-    if (C < 1 || G < 1 || align < 1 || N < 0 || out_rows < 0 || H < 1) return MP_ERR_INVALID_ARG;
-    if (C % G != 0) return MP_ERR_INVALID_ARG;
-    if (C > MP_MAX_CHUNKS || N > INT32_MAX || out_rows > INT32_MAX) return MP_ERR_UNSUPPORTED;
-    if (split_sizes == nullptr || chunk_order == nullptr || group_off == nullptr)
-        return MP_ERR_INVALID_ARG;
-    if ((probs == nullptr) != (out_probs == nullptr)) return MP_ERR_INVALID_ARG;
-    if (out_rows > 0 && (out == nullptr || row_map == nullptr)) return MP_ERR_INVALID_ARG;
-    if (N > 0 && x == nullptr) return MP_ERR_INVALID_ARG;
-    cudaStream_t s = as_stream(stream);
-    const unsigned blocks = out_rows > 0 ? (unsigned)((out_rows + CH_ROWS - 1) / CH_ROWS) : 1u;
-    const size_t smem = sort_pad_smem(C, G);
-    if (chunk_vec_ok(H, {x, out}))
-        k_sort_pad<uint4><<<blocks, CH_THREADS, smem, s>>>(
-            (const uint4 *)x, probs, split_sizes, chunk_order, C, G, align, N, out_rows, H / 8,
-            (uint4 *)out, out_probs, row_map, group_off, dev_status);
-    else
-        k_sort_pad<uint16_t><<<blocks, CH_THREADS, smem, s>>>(
-            (const uint16_t *)x, probs, split_sizes, chunk_order, C, G, align, N, out_rows, H,
-            (uint16_t *)out, out_probs, row_map, group_off, dev_status);
-    return check_launch();
+    if (H < 1) return MP_ERR_INVALID_ARG;
+    return sort_pad_impl(x, probs, split_sizes, chunk_order, nullptr, C, G, align, N, out_rows, H,
+                         out, out_probs, row_map, group_off, dev_status, as_stream(stream));
+}
+
+extern "C" mp_status_t mp_sort_chunks_pad_ex(const void *x, int32_t dtype, const float *probs,
+                                             const int32_t *split_sizes,
+                                             const int32_t *chunk_order,
+                                             const int32_t *padded_sizes, int32_t C, int32_t G,
+                                             int32_t align, int64_t N, int64_t out_rows, int32_t H,
+                                             void *out, float *out_probs, int32_t *row_map,
+                                             int64_t *group_off, int32_t *dev_status,
+                                             mp_stream_t stream)
+{
+    const int u = elem_units(dtype);
+    if (u == 0 || H < 1) return MP_ERR_INVALID_ARG;
+    return sort_pad_impl(x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N,
+                         out_rows, (int64_t)H * u, out, out_probs, row_map, group_off, dev_status,
+                         as_stream(stream));
 }
 
 extern "C" mp_status_t mp_unpad_restore(const mp_bf16_t *padded, const float *padded_probs,
@@ -315,6 +372,15 @@ extern "C" mp_status_t mp_unpad_restore(const mp_bf16_t *padded, const float *pa
                  as_stream(stream), true);
 }
 
+extern "C" mp_status_t mp_unpad_restore_ex(const void *padded, int32_t dtype,
+                                           const float *padded_probs, const int32_t *row_map,
+                                           int64_t out_rows, int64_t N, int32_t H, void *y,
+                                           float *y_probs, int32_t *dev_status, mp_stream_t stream)
+{
+    return remap_ex(padded, dtype, padded_probs, row_map, out_rows, N, H, y, y_probs, dev_status,
+                    as_stream(stream), true);
+}
+
 extern "C" mp_status_t mp_sort_chunks_pad_bwd(const mp_bf16_t *g_out, const float *g_out_probs,
                                               const int32_t *row_map, int64_t out_rows, int64_t N,
                                               int32_t H, mp_bf16_t *g_x, float *g_probs,
@@ -324,6 +390,16 @@ extern "C" mp_status_t mp_sort_chunks_pad_bwd(const mp_bf16_t *g_out, const floa
                  as_stream(stream), true);
 }
 
+extern "C" mp_status_t mp_sort_chunks_pad_bwd_ex(const void *g_out, int32_t dtype,
+                                                 const float *g_out_probs, const int32_t *row_map,
+                                                 int64_t out_rows, int64_t N, int32_t H, void *g_x,
+                                                 float *g_probs, int32_t *dev_status,
+                                                 mp_stream_t stream)
+{
+    return remap_ex(g_out, dtype, g_out_probs, row_map, out_rows, N, H, g_x, g_probs, dev_status,
+                    as_stream(stream), true);
+}
+
 extern "C" mp_status_t mp_unpad_restore_bwd(const mp_bf16_t *g_y, const float *g_y_probs,
                                             const int32_t *row_map, int64_t out_rows, int64_t N,
                                             int32_t H, mp_bf16_t *g_padded, float *g_padded_probs,
@@ -331,4 +407,14 @@ extern "C" mp_status_t mp_unpad_restore_bwd(const mp_bf16_t *g_y, const float *g
 {
     return remap(g_y, g_y_probs, row_map, out_rows, N, H, g_padded, g_padded_probs, dev_status,
                  as_stream(stream), false);
+}
+
+extern "C" mp_status_t mp_unpad_restore_bwd_ex(const void *g_y, int32_t dtype,
+                                               const float *g_y_probs, const int32_t *row_map,
+                                               int64_t out_rows, int64_t N, int32_t H,
+                                               void *g_padded, float *g_padded_probs,
+                                               int32_t *dev_status, mp_stream_t stream)
+{
+    return remap_ex(g_y, dtype, g_y_probs, row_map, out_rows, N, H, g_padded, g_padded_probs,
+                    dev_status, as_stream(stream), false);
 }
