@@ -273,7 +273,9 @@ def run_gpu(args):
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
 
     ops = ["build_map", "permute", "unpermute", "unpermute_bwd", "permute_bwd"]
-    launches = {"build_map": 3, "permute": 1, "unpermute": 1, "unpermute_bwd": 1,
+    # kernels each op launches (the map: count + rank; a third, the single-CTA
+    # scan, only when the count matrix exceeds what the rank CTAs read)
+    launches = {"build_map": 2, "permute": 1, "unpermute": 1, "unpermute_bwd": 1,
                 "permute_bwd": 1}
 
     def call(op):
