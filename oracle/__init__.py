@@ -11,6 +11,7 @@ page it follows, is documented in ``oracle.c``.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -25,15 +26,16 @@ _lock = threading.Lock()
 _lib = None
 
 
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
 def build(force: bool = False) -> str:
     """Compile ``oracle.c`` into ``liboracle.so`` (in place) if it is stale."""
     if (not force and os.path.exists(_LIB)
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
-           _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, _LIB)
     return _LIB
 
@@ -47,45 +49,62 @@ class _Flags(ctypes.Structure):
 def _load():
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
-        P = ctypes.c_void_p
-        i64, i32 = ctypes.c_int64, ctypes.c_int32
-        lib.orc_f32_from_bf16.argtypes = [ctypes.c_uint16]
-        lib.orc_f32_from_bf16.restype = ctypes.c_float
-        lib.orc_bf16_from_f32.argtypes = [ctypes.c_float]
-        lib.orc_bf16_from_f32.restype = ctypes.c_uint16
-        lib.orc_build_map.argtypes = [P, i64, i32, i32, P, P, P, P]
-        lib.orc_build_map.restype = i64
-        lib.orc_build_map_capacity.argtypes = [P, i64, i32, i32, i32, P, P, P, P]
-        lib.orc_build_map_capacity.restype = i64
-        lib.orc_bf16_from_f64.argtypes = [ctypes.c_double]
-        lib.orc_bf16_from_f64.restype = ctypes.c_uint16
-        lib.orc_unpermute_ep.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P]
-        lib.orc_unpermute_ep.restype = None
-        lib.orc_topk_softmax.argtypes = [P, i64, i32, i32, i32, i32, P, P]
-        lib.orc_topk_softmax.restype = None
-        lib.orc_topk_softmax_bwd.argtypes = [P, P, P, i64, i32, i32, P]
-        lib.orc_topk_softmax_bwd.restype = None
-        lib.orc_permute.argtypes = [P, P, P, i64, i32, i32, P, P]
-        lib.orc_permute.restype = None
-        lib.orc_unpermute.argtypes = [P, P, P, i64, i32, i32, P]
-        lib.orc_unpermute.restype = None
-        lib.orc_permute_bwd.argtypes = [P, P, P, i64, i32, i32, P, P]
-        lib.orc_permute_bwd.restype = None
-        lib.orc_unpermute_bwd.argtypes = [P, P, P, P, i64, i32, i32, P, P]
-        lib.orc_unpermute_bwd.restype = None
-        lib.orc_sort_chunks_pad.argtypes = [P, P, P, P, P, i32, i32, i32, i64, i64, i32,
-                                            P, P, P, P, ctypes.POINTER(_Flags)]
-        lib.orc_sort_chunks_pad.restype = None
-        for name in ("orc_unpad_restore", "orc_sort_chunks_pad_bwd",
-                     "orc_unpad_restore_bwd"):
-            fn = getattr(lib, name)
-            fn.argtypes = [P, P, P, i64, i64, i32, P, P]
-            fn.restype = None
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = _configure(ctypes.CDLL(build()))
+        return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Routes every oracle call to another build of oracle.c for the duration
+    (the tests that plant a mistake in a copy of the oracle use this)."""
+    global _lib
+    with _lock:
+        saved = _lib
+        _lib = _configure(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = saved
+
+
+def _configure(lib):
+    P = ctypes.c_void_p
+    i64, i32 = ctypes.c_int64, ctypes.c_int32
+    lib.orc_f32_from_bf16.argtypes = [ctypes.c_uint16]
+    lib.orc_f32_from_bf16.restype = ctypes.c_float
+    lib.orc_bf16_from_f32.argtypes = [ctypes.c_float]
+    lib.orc_bf16_from_f32.restype = ctypes.c_uint16
+    lib.orc_build_map.argtypes = [P, i64, i32, i32, P, P, P, P]
+    lib.orc_build_map.restype = i64
+    lib.orc_build_map_capacity.argtypes = [P, i64, i32, i32, i32, P, P, P, P]
+    lib.orc_build_map_capacity.restype = i64
+    lib.orc_bf16_from_f64.argtypes = [ctypes.c_double]
+    lib.orc_bf16_from_f64.restype = ctypes.c_uint16
+    lib.orc_unpermute_ep.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P]
+    lib.orc_unpermute_ep.restype = None
+    lib.orc_topk_softmax.argtypes = [P, i64, i32, i32, i32, i32, P, P]
+    lib.orc_topk_softmax.restype = None
+    lib.orc_topk_softmax_bwd.argtypes = [P, P, P, i64, i32, i32, P]
+    lib.orc_topk_softmax_bwd.restype = None
+    lib.orc_permute.argtypes = [P, P, P, i64, i32, i32, P, P]
+    lib.orc_permute.restype = None
+    lib.orc_unpermute.argtypes = [P, P, P, i64, i32, i32, P]
+    lib.orc_unpermute.restype = None
+    lib.orc_permute_bwd.argtypes = [P, P, P, i64, i32, i32, P, P]
+    lib.orc_permute_bwd.restype = None
+    lib.orc_unpermute_bwd.argtypes = [P, P, P, P, i64, i32, i32, P, P]
+    lib.orc_unpermute_bwd.restype = None
+    lib.orc_sort_chunks_pad.argtypes = [P, P, P, P, P, i32, i32, i32, i64, i64, i32,
+                                        P, P, P, P, ctypes.POINTER(_Flags)]
+    lib.orc_sort_chunks_pad.restype = None
+    for name in ("orc_unpad_restore", "orc_sort_chunks_pad_bwd",
+                 "orc_unpad_restore_bwd"):
+        fn = getattr(lib, name)
+        fn.argtypes = [P, P, P, i64, i64, i32, P, P]
+        fn.restype = None
+    return lib
 
 
 def _p(a):
