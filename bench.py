@@ -224,6 +224,134 @@ def oracle_step_rate(seconds: float, sample_tokens: int = 256):
     return nbytes / dt / 1e9, it, dt, sample
 
 
+def cpu_model() -> str:
+    """A one-line description of the host CPU (model name where the kernel
+    reports one, else the architecture)."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_step_sharded(w, rim, routed, pool, n_shards):
+    """One fwd+bwd step of the oracle with the row work split over token
+    ranges on a thread pool: the map is built once for the whole batch (its
+    scan is global), then permute, unpermute, unpermute_bwd and permute_bwd
+    each run on disjoint token ranges (the oracle's C calls release the GIL).
+    Every token's outputs depend on that token alone, so the result is
+    bit-identical to the single-thread oracle."""
+    import oracle
+
+    T, H, K = w["T"], w["H"], w["K"]
+    edges = [T * i // n_shards for i in range(n_shards + 1)]
+    shards = [(a, b) for a, b in zip(edges[:-1], edges[1:]) if b > a]
+    R = T * K
+    rows = np.zeros((R, H), np.uint16)
+    rows_p = np.zeros(R, np.float32)
+    g_rows = np.zeros((R, H), np.uint16)
+    y = np.empty((T, H), np.uint16)
+    g_x = np.empty((T, H), np.uint16)
+    g_probs = np.empty((T, K), np.float64)
+    x, probs, g_y = w["x"], w["probs"], w["g_y"]
+
+    def fwd_perm(s):
+        a, b = s
+        oracle.permute(x[a:b], probs[a:b], rim[a:b], out=rows, out_probs=rows_p)
+
+    def fwd_unperm(s):
+        a, b = s
+        y[a:b] = oracle.unpermute(rows, probs[a:b], rim[a:b], b - a, H)
+
+    def bwd_unperm(s):
+        a, b = s
+        _, gp = oracle.unpermute_bwd(g_y[a:b], rows, probs[a:b], rim[a:b], g_rows=g_rows)
+        g_probs[a:b] = gp
+
+    def bwd_perm(s):
+        a, b = s
+        g_x[a:b] = oracle.permute_bwd(g_rows, None, rim[a:b], b - a, H)[0]
+
+    for phase in (fwd_perm, fwd_unperm, bwd_unperm, bwd_perm):
+        list(pool.map(phase, shards))
+    return {"rows": rows[:routed], "rows_probs": rows_p[:routed], "y": y,
+            "g_rows": g_rows[:routed], "g_probs": g_probs, "g_x": g_x}
+
+
+class ShardedOracle:
+    """The oracle's fwd+bwd step on n_threads * tokens_per_thread tokens of the
+    workload, its row work over token ranges on a pool of n_threads threads.
+    The first step is checked bit-identical to the single-thread oracle."""
+
+    def __init__(self, n_threads: int, tokens_per_thread: int):
+        from concurrent.futures import ThreadPoolExecutor
+
+        import oracle
+        from unpermute_routing_indices_gb300 import workloads as wl
+
+        self.n = n_threads
+        self.w = w = wl.routed(WORKLOAD, T=n_threads * tokens_per_thread)
+        T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+        self.rim, _, _, offsets, _ = oracle.build_map(w["idx"], E)
+        self.routed = int(offsets[-1])
+        self.step_bytes = sum(routed_bytes(T, H, K, E, self.routed).values())
+        self.pool = ThreadPoolExecutor(max_workers=n_threads)
+        got = oracle_step_sharded(w, self.rim, self.routed, self.pool, n_threads)
+        want = oracle_step_sharded(w, self.rim, self.routed, _Serial(), 1)
+        if not all(np.array_equal(got[k], want[k]) for k in got):
+            raise RuntimeError("threaded oracle differs from the single-thread oracle")
+
+    def step(self) -> float:
+        """One whole step (map + row work); returns its wall time in seconds."""
+        import oracle
+
+        t0 = time.perf_counter()
+        oracle.build_map(self.w["idx"], self.w["E"])
+        oracle_step_sharded(self.w, self.rim, self.routed, self.pool, self.n)
+        return time.perf_counter() - t0
+
+    def describe(self, steps: int, seconds: float) -> str:
+        w = self.w
+        return (f"{w['T']} tokens of the skewed workload (T={w['T']}, H={w['H']}, E={w['E']}, "
+                f"K={w['K']}), whole fwd+bwd step, row work over {self.n} token ranges on "
+                f"{self.n} threads ({cpu_model()}), bit-identical to one thread; "
+                f"{steps} steps in {seconds:.1f} s")
+
+    def close(self):
+        self.pool.shutdown()
+
+
+def oracle_threads_rate(seconds: float, n_threads: int, tokens_per_thread: int = 256):
+    """ShardedOracle steps until `seconds` have passed; returns
+    (GB/s, steps, seconds, sample description)."""
+    so = ShardedOracle(n_threads, tokens_per_thread)
+    it, dt = 0, 0.0
+    while dt < seconds:
+        dt += so.step()
+        it += 1
+    so.close()
+    return it * so.step_bytes / dt / 1e9, it, dt, so.describe(it, dt)
+
+
+class _Serial:
+    """The map() of a pool, run on the calling thread."""
+
+    @staticmethod
+    def map(fn, items):
+        return [fn(i) for i in items]
+
+
 # --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
@@ -321,15 +449,29 @@ def run_gpu(args):
         barrier()
     clocks = clk.summary(t0, t1)
 
-    per_op = {op: 0.0 for op in ops}
+    samples = {op: [] for op in ops}
     step_ms = []
     for e in evs:
         step_ms.append(e[0].elapsed_time(e[-1]))
         for j, op in enumerate(ops):
-            per_op[op] += e[j].elapsed_time(e[j + 1])
+            samples[op].append(e[j].elapsed_time(e[j + 1]))
     ms = sum(step_ms) / len(step_ms)
-    per_op = {op: v / args.steps for op, v in per_op.items()}
+    per_op = {op: statistics.mean(v) for op, v in samples.items()}
+    med_op = {op: statistics.median(v) for op, v in samples.items()}
     ms = max_over_ranks(ms, world, dev)
+
+    # warm numbers: the same steps back to back, no L2 flush in between
+    warm_n = max(3, min(args.steps, 100))
+    torch.cuda.synchronize()
+    wev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(warm_n)]
+    for i in range(warm_n):
+        wev[i][0].record(stream)
+        for j, op in enumerate(ops):
+            call(op)
+            wev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    warm_op = {op: statistics.median(wev[i][j].elapsed_time(wev[i][j + 1]) for i in range(warm_n))
+               for j, op in enumerate(ops)}
 
     peak, peak_kind = measured_peaks()
     gbs = job_throughput(step_bytes, world, ms)
@@ -430,10 +572,16 @@ def run_gpu(args):
         "pct_of_nominal_peak": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_peak": round(100 * gbs / world / peak, 2),
         "tokens_per_s": round(world * T / (ms * 1e-3), 1),
-        "ops": {op: {"us": round(per_op[op] * 1e3, 2), "bytes": nbytes[op],
+        "ops": {op: {"us": round(per_op[op] * 1e3, 2), "us_median": round(med_op[op] * 1e3, 2),
+                     "us_warm_median": round(warm_op[op] * 1e3, 2), "bytes": nbytes[op],
                      "GB/s": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9, 1),
                      "frac_of_measured": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9 / peak, 4)}
                 for op in ops},
+        "permute_incl_map": {
+            "us": round((per_op["build_map"] + per_op["permute"]) * 1e3, 2),
+            "GB/s": round((nbytes["build_map"] + nbytes["permute"])
+                          / ((per_op["build_map"] + per_op["permute"]) * 1e-3) / 1e9, 1),
+            "tokens_per_s": round(T / ((per_op["build_map"] + per_op["permute"]) * 1e-3), 1)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -452,6 +600,10 @@ def run_gpu(args):
         v, it, dt, sample = oracle_step_rate(args.cpu_seconds)
         out["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": 1,
                                "kind": "oracle", "sample": sample}
+        n = host_threads()
+        v, it, dt, sample = oracle_threads_rate(args.cpu_seconds * 2 / 3, n)
+        out["cpu_baseline_threads"] = {"value": round(v, 4), "unit": "GB/s", "cores": n,
+                                       "kind": "oracle", "sample": sample}
     if world > 1:
         dist.destroy_process_group()
     return out if rank == 0 else None
@@ -537,32 +689,35 @@ def bench_chunks(mp, wl, dev, flush, args):
 
 
 def run_reference(args):
+    """The oracle as it stands, on the host cores: each step is one whole
+    fwd+bwd step over a bounded sample of the workload (64 tokens per host
+    thread), the row work split over token ranges on all host threads."""
     world, rank, _ = dist_env()
     if rank != 0:
         return None
+    n = host_threads()
+    so = ShardedOracle(n, 64)
+    for _ in range(args.warmup):
+        so.step()
+    secs = [so.step() for _ in range(args.steps)]
+    so.close()
+    mean_s = statistics.mean(secs)
+    v = so.step_bytes / mean_s / 1e9
     from unpermute_routing_indices_gb300 import workloads as wl
 
-    cfg = wl.ROUTED[WORKLOAD]
-    T, H, E, K = cfg["T"], cfg["H"], cfg["E"], cfg["K"]
-    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        oracle_step_rate(per_step)
-    vals, secs = [], 0.0
-    sample = ""
-    for _ in range(args.steps):
-        v, it, dt, sample = oracle_step_rate(per_step)
-        vals.append(v)
-        secs += dt
-    v = statistics.mean(vals)
+    full = wl.ROUTED[WORKLOAD]
+    T, H, E, K = full["T"], full["H"], full["E"], full["K"]
+    cfg = {"workload": f"{WORKLOAD} dispatch T={T} H={H} E={E} K={K}, fwd+bwd step",
+           "T": T, "H": H, "E": E, "K": K,
+           "sample": f"{so.w['T']} tokens per step ({so.routed} routed rows, "
+                     f"{so.step_bytes} bytes)"}
     return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * secs / max(1, args.steps), 3),
+            "ms_per_step": round(1e3 * mean_s, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded numpy)",
-            "config": {"workload": f"{WORKLOAD} dispatch T={T} H={H} E={E} K={K}, fwd+bwd step",
-                       "T": T, "H": H, "E": E, "K": K},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "data": "synthetic (seeded numpy)", "config": cfg,
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+                             "sample": so.describe(args.steps, sum(secs))},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

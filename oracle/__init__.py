@@ -179,11 +179,22 @@ def build_map_capacity(idx: np.ndarray, E: int, capacity: int):
     return row_id_map, s2f, counts, offsets, int(bad)
 
 
-def permute(x, probs, row_id_map, out_rows=None):
+def _out(a, shape, dtype):
+    """A caller-supplied output array, checked to be a C-contiguous array the
+    C code may write through."""
+    if a.dtype != dtype or a.shape[1:] != shape[1:] or not a.flags.c_contiguous \
+            or not a.flags.writeable:
+        raise ValueError("output array of the wrong type, shape or layout")
+    return a
+
+
+def permute(x, probs, row_id_map, out_rows=None, out=None, out_probs=None):
     """x[T,H] uint16, probs[T,K] f32 or None -> (out[out_rows,H], out_probs or None).
 
     Rows no slot maps to are left at zero here (the CUDA path leaves them
-    unwritten; the tests compare only mapped rows)."""
+    unwritten; the tests compare only mapped rows).  With `out` (and
+    `out_probs`) given, only the mapped rows of those arrays are written, so
+    calls on disjoint token ranges can share them."""
     lib = _load()
     x = _c(x, np.uint16)
     row_id_map = _c(row_id_map, np.int32)
@@ -191,9 +202,16 @@ def permute(x, probs, row_id_map, out_rows=None):
     T, H = x.shape
     K = row_id_map.shape[1]
     if out_rows is None:
-        out_rows = T * K
-    out = np.zeros((out_rows, H), np.uint16)
-    out_probs = np.zeros(out_rows, np.float32) if probs is not None else None
+        out_rows = T * K if out is None else out.shape[0]
+    if out is None:
+        out = np.zeros((out_rows, H), np.uint16)
+    out = _out(out, (out_rows, H), np.uint16)
+    if probs is not None and out_probs is None:
+        out_probs = np.zeros(out_rows, np.float32)
+    if probs is None:
+        out_probs = None
+    elif out_probs.shape != (out.shape[0],):
+        raise ValueError("out_probs must have one entry per row of out")
     lib.orc_permute(_p(x), _p(probs), _p(row_id_map), T, K, H, _p(out), _p(out_probs))
     return out, out_probs
 
@@ -237,8 +255,10 @@ def permute_bwd(g_out, g_out_probs, row_id_map, T, H):
     return g_x, g_probs
 
 
-def unpermute_bwd(g_y, rows, probs, row_id_map, out_rows=None):
-    """Returns (g_rows[out_rows,H] uint16, g_probs[T,K] float64 or None)."""
+def unpermute_bwd(g_y, rows, probs, row_id_map, out_rows=None, g_rows=None):
+    """Returns (g_rows[out_rows,H] uint16, g_probs[T,K] float64 or None).
+
+    With `g_rows` given, only the rows the map names are written into it."""
     lib = _load()
     g_y = _c(g_y, np.uint16)
     rows = _c(rows, np.uint16)
@@ -247,8 +267,10 @@ def unpermute_bwd(g_y, rows, probs, row_id_map, out_rows=None):
     T, H = g_y.shape
     K = row_id_map.shape[1]
     if out_rows is None:
-        out_rows = T * K
-    g_rows = np.zeros((out_rows, H), np.uint16)
+        out_rows = T * K if g_rows is None else g_rows.shape[0]
+    if g_rows is None:
+        g_rows = np.zeros((out_rows, H), np.uint16)
+    g_rows = _out(g_rows, (out_rows, H), np.uint16)
     g_probs = np.empty((T, K), np.float64) if probs is not None else None
     lib.orc_unpermute_bwd(_p(g_y), _p(rows), _p(probs), _p(row_id_map), T, K, H,
                           _p(g_rows), _p(g_probs))
