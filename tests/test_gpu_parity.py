@@ -415,15 +415,21 @@ def test_unpermute_ep_wide_ranging_partials():
         np.testing.assert_array_equal(h(got), want)
 
 
-def test_unpermute_ep_fp64_sum_on_bf16_ties():
+@pytest.mark.parametrize("bf16p", [True, False])
+def test_unpermute_ep_fp64_sum_on_bf16_ties(bf16p):
     """Rank partials 1, 2^-8 (together exactly halfway between two bf16 values)
-    and +-2^-30 or +-2^-40 on a third rank: the tiny partial decides the
-    rounding, both on the fp32-pair path (span 30 binades) and on the fp64
-    path (span 40)."""
+    and a small third partial on a third rank that decides the rounding.  The
+    spans (sum of magnitudes over the smallest) reach each way the kernel
+    forms the exact sum: plain fp32 adds up to 2^15 (bf16 partials), an fp32
+    TwoSum pair up to 2^36 (bf16) or 2^20 (fp32 partials), fp64 adds beyond,
+    and a zero partial."""
     E, ep, K, H = 8, 4, 3, 8
     vals = [(1.0, 2.0**-8, 2.0**-30), (1.0, 2.0**-8, -2.0**-30), (1.0, 2.0**-8, 2.0**-40),
             (1.0, 2.0**-8, -2.0**-40), (1.0, 2.0**-8, 0.0), (-1.0, -(2.0**-8), -(2.0**-30)),
-            (3.0, 2.0**-7, 2.0**-33), (2.0**-30, 1.0, 2.0**-8)]
+            (3.0, 2.0**-7, 2.0**-33), (2.0**-30, 1.0, 2.0**-8),
+            (1.0, 2.0**-8, 2.0**-12), (1.0, 2.0**-8, -2.0**-12), (1.0, 2.0**-8, 2.0**-14),
+            (1.0, 2.0**-8, -2.0**-15), (1.0, 2.0**-8, 2.0**-15), (1.0, 2.0**-8, 2.0**-19),
+            (1.0, 2.0**-8, -2.0**-21), (-(2.0**-14), -1.0, -(2.0**-8))]
     T = len(vals)
     idx = np.tile(np.array([[0, 2, 4]], np.int32), (T, 1))      # ranks 0, 1, 2
     rows_f = np.zeros((T * K, H), np.float32)
@@ -435,9 +441,11 @@ def test_unpermute_ep_fp64_sum_on_bf16_ties():
     assert torch.equal(rows.float(), torch.from_numpy(rows_f))   # all bf16 values
     rows_bits = rows.view(torch.int16).numpy().view(np.uint16)
     g_rim, *_ = mp.mp_build_map(d(idx), E)
-    got = mp.mp_unpermute_ep(d(rows_bits), g_rim, d(idx), E, ep, None, bf16_partials=True,
+    got = mp.mp_unpermute_ep(d(rows_bits), g_rim, d(idx), E, ep, None, bf16_partials=bf16p,
                              fp64_cross_rank=True)
-    want = oracle.unpermute_ep(rows_bits, None, rim, idx, T, H, E, ep, True, True)
+    want = oracle.unpermute_ep(rows_bits, None, rim, idx, T, H, E, ep, bf16p, True)
     np.testing.assert_array_equal(h(got), want)
     up = oracle.bf16_from_f32(np.float32(1.0078125))
-    assert want[0, 0] == up and want[1, 0] == oracle.bf16_from_f32(np.float32(1.0))
+    one = oracle.bf16_from_f32(np.float32(1.0))
+    assert want[0, 0] == up and want[1, 0] == one
+    assert want[8, 0] == up and want[9, 0] == one and want[11, 0] == one

@@ -17,9 +17,9 @@
 // slot: K FMAs per element whatever the number of ranks.  A rank with no
 // routed slot would add +0 to an accumulator that is never -0, so skipping it
 // changes no bit.  GB300 runs FP64 at a small fraction of its FP32 rate, so
-// bf16 partials whose fp64 sum is provably exact are summed exactly as an
-// fp32 pair (same bits); only partials spanning more than 34 binades take the
-// fp64 additions.
+// where the fp64 sum of the partials is provably exact (their magnitudes span
+// few enough binades) the same exact sum is formed in fp32 -- by plain adds,
+// or as a TwoSum pair -- and only wider spans take the fp64 additions.
 #include <climits>
 
 #include "common.cuh"
@@ -85,31 +85,6 @@ __device__ __forceinline__ uint4 pack_bits(const uint16_t (&b)[8])
 
 __device__ __forceinline__ uint16_t pack_bits(const uint16_t (&b)[1]) { return b[0]; }
 
-template <bool FP64> struct AccT;
-template <> struct AccT<false> { using type = float; };
-template <> struct AccT<true> { using type = double; };
-
-template <typename V, bool FP64> struct PackAcc;
-template <> struct PackAcc<uint4, false> {
-    static __device__ __forceinline__ uint4 run(const float (&a)[8]) { return pack(a); }
-};
-template <> struct PackAcc<uint16_t, false> {
-    static __device__ __forceinline__ uint16_t run(const float (&a)[1]) { return pack(a); }
-};
-template <> struct PackAcc<uint4, true> {
-    static __device__ __forceinline__ uint4 run(const double (&a)[8])
-    {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            w[i] = (uint32_t)bf16_from_f64(a[2 * i]) | ((uint32_t)bf16_from_f64(a[2 * i + 1]) << 16);
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-};
-template <> struct PackAcc<uint16_t, true> {
-    static __device__ __forceinline__ uint16_t run(const double (&a)[1]) { return bf16_from_f64(a[0]); }
-};
-
 // Compare-exchange on (key, row, prob) triples, smaller key first.
 __device__ __forceinline__ void cx(int32_t &ka, int32_t &ra, float &pa, int32_t &kb, int32_t &rb,
                                    float &pb)
@@ -165,13 +140,12 @@ __device__ __forceinline__ void walk_ranks(const V (&r)[EP_KMAX], const float (&
 }
 
 template <typename V, bool PROBS, bool BF16P, bool FP64>
-__global__ void __launch_bounds__(EP_THREADS)
+__global__ void __launch_bounds__(EP_THREADS, FP64 ? 4 : 1)
     k_unpermute_ep(const V *__restrict__ rows, const float *__restrict__ probs,
                    const int32_t *__restrict__ map, const int32_t *__restrict__ idx, int64_t T,
                    int K, int nvec, int tpt_log2, int per_rank, V *__restrict__ out)
 {
     constexpr int L = Lanes<V>::N;
-    using Acc = typename AccT<FP64>::type;
     const int tpt = 1 << tpt_log2;
     const int lane = threadIdx.x & (tpt - 1);
     const int64_t t = (int64_t)blockIdx.x * (EP_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
@@ -208,69 +182,102 @@ __global__ void __launch_bounds__(EP_THREADS)
         for (int i = 0; i < EP_KMAX; ++i)
             r[i] = ((valid >> i & 1u) && c < nvec) ? ld_stream(rows + (int64_t)rk[i] * nvec + c)
                                                    : zero_vec<V>();
-        Acc acc[L];
-        if (FP64 && BF16P) {
-            // Cross-rank sum of bf16 partials in fp64.  Every partial is a
-            // multiple of the smallest partial's quantum Q.  The sum runs as an
-            // fp32 pair (hi, lo): TwoSum makes each addition's error exact, and
-            // while the nonzero partials span at most 34 binades (below 2^124)
-            // the errors add up in lo without rounding, so hi + lo is the exact
-            // sum -- which the fp64 additions also produce, every partial sum
-            // having at most 45 significant bits.  Wider spans take the fp64
-            // additions (the rows are still in registers).
-            float shi[L], slo[L];
-            int lo[L], hi[L];
+        if constexpr (FP64) {
+            // Exact cross-rank sum, then one rounding to bf16.  The partials
+            // are bf16 (BF16P) or fp32 values, each a multiple of its own
+            // quantum, and the smallest nonzero magnitude m has the smallest
+            // quantum q, with q > m / 2^8 (bf16) or m / 2^24 (fp32).  With
+            // a = the fp32 sum of |partial| (within 2^-20 of the exact one):
+            //  * bf16 partials, a <= 2^15 m: every running sum is a multiple
+            //    of q below 2^24 q, so plain fp32 adds are exact;
+            //  * a <= 2^36 m (bf16) or 2^20 m (fp32): TwoSum makes each add's
+            //    error exact, the errors (multiples of q, together below
+            //    2^24 q) add up exactly, and hi + lo is the exact sum;
+            //  * otherwise (or a > 2^120, inf, NaN): fp64 additions in rank
+            //    order, the definition itself.
+            // In the first two cases every running sum has at most 45
+            // significant bits, so the fp64 additions are exact as well and
+            // all three give the same bits.
+            constexpr float TIER2 = BF16P ? 0x1p36f : 0x1p20f;
+            uint16_t bits[L];
+            unsigned pair = 0, dbl = 0;   // elements that take the pair / fp64 sum
+            float sa[L], sb[L], sm[L];
 #pragma unroll
             for (int e = 0; e < L; ++e) {
-                shi[e] = 0.0f;
-                slo[e] = 0.0f;
-                lo[e] = 255;
-                hi[e] = 0;
+                sa[e] = 0.0f;
+                sb[e] = 0.0f;
+                sm[e] = __int_as_float(0x7f800000);
             }
-            walk_ranks<PROBS, true, L>(r, pk, valid, last, [&](int e, float p) {
-                const float s = __fadd_rn(shi[e], p);
-                const float bb = __fsub_rn(s, shi[e]);
-                const float err = __fadd_rn(__fsub_rn(shi[e], __fsub_rn(s, bb)), __fsub_rn(p, bb));
-                shi[e] = s;
-                slo[e] = __fadd_rn(slo[e], err);
-                if (p != 0.0f) {
-                    int ex = (__float_as_int(p) >> 23) & 0xff;
-                    ex = ex < 1 ? 1 : ex;
-                    lo[e] = min(lo[e], ex);
-                    hi[e] = max(hi[e], ex);
-                }
-            });
-            bool any_wide = false;
-#pragma unroll
-            for (int e = 0; e < L; ++e) {
-                const bool wide = !(hi[e] - lo[e] <= 34 && hi[e] <= 250);
-                any_wide |= wide;
-                lo[e] = wide;   // reuse: 1 = needs the fp64 pass
-                acc[e] = 0.0;
-            }
-            if (any_wide)
+            if (BF16P) {
                 walk_ranks<PROBS, true, L>(r, pk, valid, last, [&](int e, float p) {
-                    if (lo[e]) acc[e] = __dadd_rn(acc[e], (double)p);
+                    sa[e] = __fadd_rn(sa[e], p);
+                    sb[e] = __fadd_rn(sb[e], fabsf(p));
+                    sm[e] = fminf(sm[e], fabsf(p));
                 });
-            if (c < nvec) {
-                uint16_t bits[L];
+#pragma unroll
+                for (int e = 0; e < L; ++e) {
+                    __nv_bfloat16 h = __float2bfloat16_rn(sa[e]);
+                    bits[e] = *reinterpret_cast<uint16_t *>(&h);
+                    const bool fin = sb[e] <= 0x1p120f;
+                    if (!(fin && sb[e] <= __fmul_rn(sm[e], 0x1p15f)))
+                        (fin && sb[e] <= __fmul_rn(sm[e], TIER2) ? pair : dbl) |= 1u << e;
+                }
+                if (pair) {
+#pragma unroll
+                    for (int e = 0; e < L; ++e) {
+                        sa[e] = 0.0f;
+                        sb[e] = 0.0f;
+                    }
+                    walk_ranks<PROBS, true, L>(r, pk, valid, last, [&](int e, float p) {
+                        const float s = __fadd_rn(sa[e], p);
+                        const float bb = __fsub_rn(s, sa[e]);
+                        sb[e] = __fadd_rn(sb[e], __fadd_rn(__fsub_rn(sa[e], __fsub_rn(s, bb)),
+                                                           __fsub_rn(p, bb)));
+                        sa[e] = s;
+                    });
+#pragma unroll
+                    for (int e = 0; e < L; ++e)
+                        if (pair >> e & 1u) bits[e] = bf16_from_pair(sa[e], sb[e]);
+                }
+            } else {
+                float sl[L];
+#pragma unroll
+                for (int e = 0; e < L; ++e) sl[e] = 0.0f;
+                walk_ranks<PROBS, false, L>(r, pk, valid, last, [&](int e, float p) {
+                    const float s = __fadd_rn(sa[e], p);
+                    const float bb = __fsub_rn(s, sa[e]);
+                    sl[e] = __fadd_rn(sl[e], __fadd_rn(__fsub_rn(sa[e], __fsub_rn(s, bb)),
+                                                       __fsub_rn(p, bb)));
+                    sa[e] = s;
+                    sb[e] = __fadd_rn(sb[e], fabsf(p));
+                    sm[e] = fminf(sm[e], fabsf(p));
+                });
+#pragma unroll
+                for (int e = 0; e < L; ++e) {
+                    bits[e] = bf16_from_pair(sa[e], sl[e]);
+                    if (!(sb[e] <= 0x1p120f && sb[e] <= __fmul_rn(sm[e], TIER2))) dbl |= 1u << e;
+                }
+            }
+            if (dbl) {
+                double acc[L];
+#pragma unroll
+                for (int e = 0; e < L; ++e) acc[e] = 0.0;
+                walk_ranks<PROBS, BF16P, L>(r, pk, valid, last, [&](int e, float p) {
+                    acc[e] = __dadd_rn(acc[e], (double)p);
+                });
 #pragma unroll
                 for (int e = 0; e < L; ++e)
-                    bits[e] = lo[e] ? bf16_from_f64(acc[e]) : bf16_from_pair(shi[e], slo[e]);
-                st_row(out + t * nvec + c, pack_bits(bits));
+                    if (dbl >> e & 1u) bits[e] = bf16_from_f64(acc[e]);
             }
-            continue;
+            if (c < nvec) st_row(out + t * nvec + c, pack_bits(bits));
         } else {
+            float acc[L];
 #pragma unroll
-            for (int e = 0; e < L; ++e) acc[e] = 0;
-            walk_ranks<PROBS, BF16P, L>(r, pk, valid, last, [&](int e, float p) {
-                if (FP64)
-                    acc[e] = __dadd_rn(acc[e], (double)p);
-                else
-                    acc[e] = __fadd_rn(acc[e], p);
-            });
+            for (int e = 0; e < L; ++e) acc[e] = 0.0f;
+            walk_ranks<PROBS, BF16P, L>(r, pk, valid, last,
+                                        [&](int e, float p) { acc[e] = __fadd_rn(acc[e], p); });
+            if (c < nvec) st_row(out + t * nvec + c, pack(acc));
         }
-        if (c < nvec) st_row(out + t * nvec + c, PackAcc<V, FP64>::run(acc));
     }
 }
 
