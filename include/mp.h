@@ -283,6 +283,25 @@ mp_status_t mp_unpermute_bwd(const mp_bf16_t *g_y, const mp_bf16_t *rows,
                              int32_t K, int32_t H, mp_bf16_t *g_rows, float *g_probs,
                              mp_stream_t stream);
 
+/*
+ * Zeroes rows [*first_row, rows) of a row-major device buffer.  The start row
+ * is read from device memory -- typically offsets + E of mp_build_map or
+ * mp_build_map_capacity, the routed row count, so that the rows of a
+ * permuted buffer (or of its gradient) that no slot maps to, left unwritten
+ * by mp_permute and mp_unpermute_bwd, become zero without a host round trip
+ * ["d9d 0.1.0 -- permute_with_probs.py", num_out_tokens: rows past the
+ * tokens kept].  *first_row is clamped to [0, rows]; at or past rows
+ * nothing is written.
+ *   buf        device, rows * row_bytes bytes (any alignment; 16-byte
+ *              aligned with row_bytes % 16 == 0 takes vector stores)
+ *   rows       >= 0;  row_bytes >= 0 (e.g. 2*H for bf16 rows, 4 for probs)
+ *   first_row  device int32 [1]
+ * rows == 0 or row_bytes == 0 is a no-op (NULL pointers allowed);
+ * otherwise NULL pointers or a negative size give MP_ERR_INVALID_ARG.
+ */
+mp_status_t mp_zero_rows_from(void *buf, int64_t rows, int64_t row_bytes,
+                              const int32_t *first_row, mp_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Chunk sort + pad, unpad + restore  [TE-PR]                                */
 /* ------------------------------------------------------------------------ */

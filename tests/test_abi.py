@@ -84,6 +84,16 @@ def test_row_ops_reject(lib):
     assert lib.mp_unpermute_bwd(FAKE, FAKE, FAKE, FAKE, 4, 2, 8, FAKE, None, None) == -1
 
 
+def test_zero_rows_from_rejects(lib):
+    assert lib.mp_zero_rows_from(None, 0, 64, None, None) == 0        # nothing to zero
+    assert lib.mp_zero_rows_from(None, 10, 0, None, None) == 0
+    assert lib.mp_zero_rows_from(None, 10, 64, FAKE, None) == -1
+    assert lib.mp_zero_rows_from(FAKE, 10, 64, None, None) == -1
+    assert lib.mp_zero_rows_from(FAKE, -1, 64, FAKE, None) == -1
+    assert lib.mp_zero_rows_from(FAKE, 10, -2, FAKE, None) == -1
+    assert lib.mp_zero_rows_from(FAKE, 1 << 40, 1 << 40, FAKE, None) == -1  # size overflow
+
+
 def test_chunk_ops_reject(lib):
     ok = (FAKE, None, FAKE, FAKE, 128, 16, 128, 100, 200, 64, FAKE, None, FAKE, FAKE, None, None)
     bad_cg = list(ok); bad_cg[4] = 100                  # C % G != 0

@@ -346,6 +346,25 @@ def mp_unpermute_bwd(g_y, row_id_map, rows=None, probs=None, *, num_out_rows=Non
     return g_rows, g_probs
 
 
+def mp_zero_rows_from(buf, first_row):
+    """Zeroes rows [first_row[0], buf.shape[0]) of a contiguous device tensor,
+    the start read on the device (e.g. offsets[-1:] of mp_build_map: the
+    rows of a permuted buffer no slot maps to).  Returns buf."""
+    lib = _lib.load()
+    if not isinstance(buf, torch.Tensor) or not buf.is_cuda or not buf.is_contiguous():
+        raise TypeError("buf must be a contiguous CUDA tensor")
+    dev = buf.device
+    _need(first_row, "first_row", torch.int32, 1, dev)
+    if first_row.numel() < 1:
+        raise ValueError("first_row must hold at least one element")
+    rows = buf.shape[0] if buf.dim() > 0 else 1
+    row_bytes = (buf.numel() // rows if rows else 0) * buf.element_size()
+    with torch.cuda.device(dev):
+        _check("mp_zero_rows_from", lib.mp_zero_rows_from(
+            _ptr(buf), rows, row_bytes, _ptr(first_row), _stream(dev)))
+    return buf
+
+
 # --------------------------------------------------------------------------
 # chunk sort + pad, unpad + restore
 # --------------------------------------------------------------------------

@@ -28,6 +28,7 @@ SIGNATURES = {
     "mp_unpermute_ep": (I32, [P, P, P, P, I64, I32, I32, I32, I32, I32, P, P]),
     "mp_permute_bwd": (I32, [P, P, P, I64, I32, I32, P, P, P]),
     "mp_unpermute_bwd": (I32, [P, P, P, P, I64, I32, I32, P, P, P]),
+    "mp_zero_rows_from": (I32, [P, I64, I64, P, P]),
     "mp_sort_chunks_pad": (I32, [P, P, P, P, I32, I32, I32, I64, I64, I32, P, P, P, P, P, P]),
     "mp_unpad_restore": (I32, [P, P, P, I64, I64, I32, P, P, P, P]),
     "mp_sort_chunks_pad_bwd": (I32, [P, P, P, I64, I64, I32, P, P, P, P]),
