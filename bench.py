@@ -397,8 +397,7 @@ def run_gpu(args):
     g_rows = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
     g_probs = torch.empty((T, K), dtype=torch.float32, device=dev)
     g_x = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
 
     ops = ["build_map", "permute", "unpermute", "unpermute_bwd", "permute_bwd"]
     # kernels each op launches (the map: count + rank; a third, the single-CTA
@@ -425,7 +424,7 @@ def run_gpu(args):
     def timed_steps(n, record):
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n)]
         for i in range(n):
-            flush.fill_(float(i))                       # L2 flush between steps
+            flush(i)                                    # L2 flush between steps
             evs[i][0].record(stream)
             for j, op in enumerate(ops):
                 call(op)
@@ -567,7 +566,8 @@ def run_gpu(args):
         "config": {"workload": f"{WORKLOAD} dispatch T={T} H={H} E={E} K={K}, fwd+bwd step",
                    "T": T, "H": H, "E": E, "K": K, "routed_rows": routed,
                    "bytes_per_step": step_bytes,
-                   "l2": "flushed between steps (fill of a 2xL2 buffer, outside the events)",
+                   "l2": "flushed between steps, outside the events: a 2xL2 buffer written, "
+                         "then another 2xL2 buffer read (L2 cold and clean)",
                    "parallelism": f"dp{world} (independent token batches, no collective)"},
         "pct_of_nominal_peak": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_peak": round(100 * gbs / world / peak, 2),
@@ -609,6 +609,28 @@ def run_gpu(args):
     return out if rank == 0 else None
 
 
+class L2Flush:
+    """Leaves L2 cold and clean between timed steps: a write of a buffer twice
+    the size of L2 evicts every line the last step left, then a read of a
+    second such buffer evicts the written (dirty) lines, so their write-back
+    happens here rather than inside the next timed region."""
+
+    def __init__(self, dev):
+        import torch
+
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        n = max(2 * l2, 256 << 20) // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.zeros(n, dtype=torch.float32, device=dev)
+        self.sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def __call__(self, i=0):
+        import torch
+
+        self.w.fill_(float(i))
+        torch.amax(self.r, dim=0, keepdim=True, out=self.sink)
+
+
 def time_op(fn, flush, stream, n):
     """Mean device time (us) of fn over n launches, L2 flushed before each."""
     import torch
@@ -617,7 +639,7 @@ def time_op(fn, flush, stream, n):
         fn()
     evs = []
     for i in range(n):
-        flush.fill_(float(i))
+        flush(i)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -664,7 +686,7 @@ def bench_chunks(mp, wl, dev, flush, args):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                 torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         for e in evs:
-            flush.fill_(1.0)
+            flush(1)
             e[0].record(stream)
             mp.mp_sort_chunks_pad(x, sz, od, G, align, out_rows, p, out=out, out_probs=out_p,
                                   row_map=row_map, group_off=goff)
