@@ -700,10 +700,35 @@ def bench_chunks(mp, wl, dev, flush, args):
         padded = int(goff[-1].item())
         b = chunk_bytes(N, H * esize // 2, padded, out_rows)
         key = str(N) if tdt == torch.bfloat16 else f"{N} fp32"
+
+        # each op alone after its own flush, and a plain device copy of the
+        # same N rows (torch copy_) timed the same way, for scale
+        def alone(fn):
+            ev = []
+            for i in range(n):
+                flush(i)
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                z.record(stream)
+                ev.append((a, z))
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(z) for a, z in ev) * 1e3
+
+        sp_alone = alone(lambda: mp.mp_sort_chunks_pad(x, sz, od, G, align, out_rows, p, out=out,
+                                                       out_probs=out_p, row_map=row_map,
+                                                       group_off=goff))
+        ur_alone = alone(lambda: mp.mp_unpad_restore(out, row_map, N, out_p, y=y, y_probs=y_p))
+        copy_us = alone(lambda: y.copy_(x))
         res[key] = {"roundtrip_ms": round(rt, 4), "sort_pad_us": round(sp * 1e3, 2),
                     "unpad_restore_us": round(ur * 1e3, 2),
                     "roundtrip_GB/s": round((b["sort_chunks_pad"] + b["unpad_restore"])
                                             / (rt * 1e-3) / 1e9, 1),
+                    "sort_pad_alone_us": round(sp_alone, 2),
+                    "unpad_restore_alone_us": round(ur_alone, 2),
+                    "sort_pad_alone_GB/s": round(b["sort_chunks_pad"] / sp_alone / 1e3, 1),
+                    "unpad_restore_alone_GB/s": round(b["unpad_restore"] / ur_alone / 1e3, 1),
+                    "plain_copy_us": round(copy_us, 2),
                     "out_rows": out_rows, "padded_rows": padded}
         if tdt == torch.bfloat16:
             res[key]["published_b200_fused_ms"] = {8192: 0.1717, 32768: 0.2029}[N]

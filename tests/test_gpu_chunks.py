@@ -76,14 +76,16 @@ def _meta(seed, G, R, max_size=40, empty_group=False):
 
 
 @pytest.mark.parametrize("G,R,align,H,empty_group,extra", [
-    (16, 8, 128, 2048, True, 0),
-    (4, 3, 8, 37, False, 5),        # element path, capacity tail
-    (1, 1, 1, 64, False, 0),        # one chunk, no padding
-    (32, 32, 16, 128, True, 100),   # C = MP_MAX_CHUNKS
-    (5, 2, 3, 24, False, 0),
-    (8, 4, 64, 512, True, 7),       # bulk engine, 1 KiB rows, 16 slots
-    (4, 4, 16, 7168, False, 3),     # bulk engine, 14 KiB rows
-    (2, 2, 4, 24576, True, 0),      # bulk engine, 48 KiB rows, 2 slots
+    (16, 8, 128, 2048, True, 0),    # one warp per row, one unrolled pass
+    (4, 3, 8, 37, False, 5),        # element path (37 units, warp per row), capacity tail
+    (1, 1, 1, 64, False, 0),        # one chunk, no padding; rows of 8 vectors (flat copy)
+    (32, 32, 16, 128, True, 100),   # C = MP_MAX_CHUNKS: metadata built by the whole CTA
+    (32, 8, 16, 256, False, 0),     # C = 256: the largest metadata built by one warp
+    (2, 129, 8, 256, True, 0),      # C = 258: the smallest built by the whole CTA
+    (5, 2, 3, 24, False, 0),        # rows of 3 vectors (flat copy)
+    (8, 4, 64, 512, True, 7),       # 64 vectors per row, a partial unrolled pass
+    (4, 4, 16, 7168, False, 3),     # 896 vectors per row, several passes
+    (2, 2, 4, 24576, True, 0),      # 3072 vectors per row
 ])
 def test_sort_pad_edges(G, R, align, H, empty_group, extra):
     sizes, order = _meta(G * 100 + R, G, R, empty_group=empty_group)
@@ -129,13 +131,13 @@ def test_restore_bad_row_sets_status():
     np.testing.assert_array_equal(h(y), want)
 
 
-def test_bulk_engine_many_rounds_per_cta():
-    """More output rows than CTAs x 256, so every CTA runs several rounds and
-    the slot ring wraps many times."""
+def test_sort_pad_many_rows():
+    """More than 155,000 rows of 64 vectors: thousands of CTAs, every row
+    position in a CTA and every warp's share of rows used."""
     G, R, align, H = 16, 8, 128, 512
     sizes, order = _meta(99, G, R, max_size=3600)
     N = int(sizes.sum())
-    assert N > 2 * 2 * 152 * 256                 # at least two rounds per CTA
+    assert N > 2 * 2 * 152 * 256
     x = wl.random_rows(N, H, 12)
     probs = np.random.default_rng(2).random(N).astype(np.float32)
     out_rows = N + G * (align - 1)

@@ -64,7 +64,7 @@ def test_routed_path_graph_replay():
         np.testing.assert_array_equal(h(g_x), o_gx)
 
 
-@pytest.mark.parametrize("H", [128, 1024])      # vector and bulk engines
+@pytest.mark.parametrize("H", [128, 1024])      # flat copy (16 vectors) and warp per row
 def test_sort_pad_graph_replay_with_new_sizes(H):
     N, G, align = 4096, 16, 128
     out_rows = wl.padded_rows_bound(N, G, align)

@@ -50,6 +50,21 @@ def test_topk_softmax_parity(T, E, K, G, TG, kind):
     _check_probs(h(probs), o_probs)
 
 
+@pytest.mark.parametrize("G,TG", [(1, 1), (8, 3)])
+def test_topk_softmax_special_values(G, TG):
+    """+0 and -0 compare equal (the lower expert wins), subnormals order
+    above zero, -inf loses to every finite logit."""
+    rng = np.random.default_rng(17)
+    T, E, K = 1031, 64, 6
+    vals = np.array([0.0, -0.0, 0.5, -0.5, 1e-40, -1e-40, -np.inf, 2.0], np.float32)
+    logits = vals[rng.integers(0, vals.size, size=(T, E))]
+    logits[:, :K] = rng.choice(vals[:6], size=(T, K))      # at least K finite logits
+    idx, probs = mp.mp_topk_softmax(d(logits), K, n_groups=G, topk_groups=TG)
+    o_idx, o_probs = oracle.topk_softmax(logits, K, G, TG)
+    np.testing.assert_array_equal(h(idx), o_idx)
+    _check_probs(h(probs), o_probs)
+
+
 def test_topk_softmax_matches_the_workload_router():
     """The router in the input generator (numpy) chooses the same experts."""
     for name, G, TG in (("mid", 1, 1), ("large", 8, 4)):

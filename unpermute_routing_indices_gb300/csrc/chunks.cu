@@ -6,23 +6,39 @@
 //   k_sort_pad     one launch for map + copy.  Every CTA rebuilds the small
 //                  chunk metadata in shared memory (C <= MP_MAX_CHUNKS sizes:
 //                  input starts, output-order starts, group rows, padded group
-//                  offsets), then resolves the source row of each of its
-//                  CH_ROWS output rows by two binary searches and copies the
-//                  rows (zero for padding).  CTA 0 also writes group_off and
-//                  the status bits.  Nothing is carried between CTAs, so the
-//                  grid depends on out_rows only and sizes are runtime data.
-//   k_rows_gather  out[d] = in[map[d]] or zero     (unpad+restore backward)
-//   k_rows_scatter out[map[d]] = in[d] if map[d] >= 0  (unpad+restore, and the
-//                  sort+pad backward)
+//                  offsets) -- one warp with shuffle scans for up to 256
+//                  chunks, the whole CTA beyond -- then resolves the source
+//                  row of each of its SP_ROWS output rows by two binary
+//                  searches and copies the rows (zero for padding).  CTA 0
+//                  also writes group_off and the status bits.  Nothing is
+//                  carried between CTAs, so the grid depends on out_rows only
+//                  and sizes are runtime data.
+//   k_rows_remap   through a saved row map: out[d] = in[map[d]] or zero
+//                  (gather: unpad+restore backward) or out[map[d]] = in[d]
+//                  (scatter: unpad+restore and the sort+pad backward).
+//   Rows of >= 32 vectors are copied one warp per row, lanes across the row.
 #include "common.cuh"
 
 namespace mp {
 namespace {
 
+#ifndef MP_CH_ROWS
+#define MP_CH_ROWS 16
+#endif
+#ifndef MP_CH_UNROLL
+#define MP_CH_UNROLL 8
+#endif
+
+#ifndef MP_SP_ROWS
+#define MP_SP_ROWS 32
+#endif
+
 constexpr int CH_THREADS = 256;
 constexpr int CH_WARPS = CH_THREADS / 32;
-constexpr int CH_ROWS = 16;   // output rows per CTA
-constexpr int CH_UNROLL = 8;  // vectors in flight per thread
+constexpr int CH_ROWS = MP_CH_ROWS;      // output rows per CTA (restore kernels)
+constexpr int SP_ROWS = MP_SP_ROWS;      // output rows per CTA (sort+pad)
+constexpr int CH_UNROLL = MP_CH_UNROLL;  // vectors in flight per thread
+constexpr int SP_WARP_META_MAX_C = 256;  // chunk counts whose metadata one warp builds
 
 // In-place exclusive scan of a[0..n), n <= 4 * CH_THREADS, in shared memory.
 // Returns the total.  Every thread of the CTA must call it.
@@ -60,6 +76,29 @@ __device__ int64_t cta_exclusive_scan(int64_t *a, int n, int64_t *s_warp)
     return total;
 }
 
+// In-place exclusive scan of a[0..n) in shared memory by one warp (32 entries
+// per round, carried across rounds).  Returns the total to every lane.  All 32
+// lanes must call it; entries written by other lanes must be fenced with
+// __syncwarp() before and after.
+__device__ int64_t warp_exclusive_scan(int64_t *a, int n)
+{
+    const int lane = threadIdx.x & 31;
+    int64_t carry = 0;
+    for (int base = 0; base < n; base += 32) {
+        const int i = base + lane;
+        const int64_t v = i < n ? a[i] : 0;
+        int64_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(FULL_MASK, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (i < n) a[i] = carry + incl - v;
+        carry += __shfl_sync(FULL_MASK, incl, 31);
+    }
+    return carry;
+}
+
 // Largest i in [lo, hi) with a[i] <= key (a non-decreasing, a[lo] <= key).
 __device__ __forceinline__ int last_le(const int64_t *a, int lo, int hi, int64_t key)
 {
@@ -72,10 +111,37 @@ __device__ __forceinline__ int last_le(const int64_t *a, int lo, int hi, int64_t
 
 // Copies the CTA's rows: out[row0 + r] = src[r] >= 0 ? in[src[r]] : 0 (gather)
 // or out[dst[r]] = in[row0 + r] (scatter, rows with dst < 0 skipped).
+// Rows of at least 32 vectors go one warp per row, the lanes across the row
+// (CH_UNROLL vectors in flight per lane, addresses by immediate offsets from
+// the row base); narrower rows are spread over the CTA as one flat range.
 template <typename V, bool SCATTER>
 __device__ __forceinline__ void copy_rows(const V *__restrict__ in, V *__restrict__ out,
                                           const int32_t *s_map, int64_t row0, int nrows, int nvec)
 {
+    if (nvec >= 32) {
+        const int lane = threadIdx.x & 31;
+        for (int r = threadIdx.x >> 5; r < nrows; r += CH_WARPS) {
+            const int32_t m = s_map[r];
+            if (SCATTER && m < 0) continue;
+            const bool zero = !SCATTER && m < 0;
+            const V *src = in + (SCATTER ? row0 + r : (int64_t)(zero ? 0 : m)) * nvec;
+            V *dst = out + (SCATTER ? (int64_t)m : row0 + r) * nvec;
+            for (int c0 = lane; c0 < nvec; c0 += 32 * CH_UNROLL) {
+                V v[CH_UNROLL];
+#pragma unroll
+                for (int u = 0; u < CH_UNROLL; ++u) {
+                    const int c = c0 + 32 * u;
+                    v[u] = (!zero && c < nvec) ? ld_stream(src + c) : zero_vec<V>();
+                }
+#pragma unroll
+                for (int u = 0; u < CH_UNROLL; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c < nvec) st_row(dst + c, v[u]);
+                }
+            }
+        }
+        return;
+    }
     const int total = nrows * nvec;
     for (int w0 = 0; w0 < total; w0 += CH_THREADS * CH_UNROLL) {
         V v[CH_UNROLL];
@@ -105,7 +171,130 @@ __device__ __forceinline__ void copy_rows(const V *__restrict__ in, V *__restric
     }
 }
 
-template <typename V>
+// The chunk metadata of sort+pad, in shared memory:
+//   s_start[c]  first input row of chunk c (exclusive scan of the sizes)
+//   s_chunk[p]  the chunk at output position p (-1 if out of range)
+//   s_cum[p]    rows before position p in output order; s_cum[C] = all
+//   s_grows[g]  unpadded rows of group g;  s_goff[g] its padded offset,
+//               s_goff[G] = the padded total
+// CTA 0 also writes group_off and the status bits.  Built by one warp (WARP,
+// few chunks: no CTA barrier inside) or by the whole CTA.
+struct SortPadMeta {
+    int64_t *s_start, *s_cum, *s_goff, *s_grows, *s_warp;
+    int32_t *s_chunk;
+};
+
+__device__ __forceinline__ int sort_pad_group_rows(const SortPadMeta &m, int g, int per_group,
+                                                   int align, const int32_t *padded_sizes)
+{
+    const int64_t rows = m.s_cum[(g + 1) * per_group] - m.s_cum[g * per_group];
+    m.s_grows[g] = rows;
+    int64_t padded = (rows + align - 1) / align * align;
+    int flags = 0;
+    if (padded_sizes != nullptr) {   // explicit padded sizes (loaded into s_goff first)
+        const int64_t ps = m.s_goff[g];
+        padded = ps < 0 ? 0 : ps;
+        if (padded < rows) flags = MP_STATUS_BAD_PADDED;
+    }
+    m.s_goff[g] = padded;
+    return flags;
+}
+
+__device__ void sort_pad_meta_warp(const SortPadMeta &m, const int32_t *split,
+                                   const int32_t *order, const int32_t *padded_sizes, int C,
+                                   int G, int align, int64_t N, int64_t out_rows,
+                                   int64_t *group_off, int32_t *status)
+{
+    const int lane = threadIdx.x & 31;
+    int flags = 0;
+    for (int c = lane; c < C; c += 32) {   // every metadata load issued together
+        int64_t v = split[c];
+        m.s_chunk[c] = order[c];
+        if (v < 0) { flags |= MP_STATUS_BAD_SPLIT; v = 0; }
+        m.s_start[c] = v;
+    }
+    if (padded_sizes != nullptr)
+        for (int g = lane; g < G; g += 32) m.s_goff[g] = padded_sizes[g];
+    __syncwarp();
+    const int64_t total_in = warp_exclusive_scan(m.s_start, C);
+    __syncwarp();
+    for (int p = lane; p < C; p += 32) {
+        const int32_t c = m.s_chunk[p];
+        const bool ok = c >= 0 && c < C;
+        if (!ok) flags |= MP_STATUS_BAD_ORDER;
+        m.s_chunk[p] = ok ? c : -1;
+        m.s_cum[p] = ok ? ((c + 1 < C ? m.s_start[c + 1] : total_in) - m.s_start[c]) : 0;
+    }
+    __syncwarp();
+    const int64_t total_ord = warp_exclusive_scan(m.s_cum, C);
+    if (lane == 0) m.s_cum[C] = total_ord;
+    __syncwarp();
+    const int per_group = C / G;
+    for (int g = lane; g < G; g += 32) flags |= sort_pad_group_rows(m, g, per_group, align, padded_sizes);
+    __syncwarp();
+    const int64_t total_pad = warp_exclusive_scan(m.s_goff, G);
+    if (lane == 0) m.s_goff[G] = total_pad;
+    flags = __reduce_or_sync(FULL_MASK, flags);
+    __syncwarp();
+    if (blockIdx.x == 0) {
+        for (int g = lane; g <= G; g += 32) group_off[g] = m.s_goff[g];
+        if (lane == 0) {
+            if (total_in > N) flags |= MP_STATUS_SPLIT_OVERFLOW;
+            if (total_pad > out_rows) flags |= MP_STATUS_ROWS_OVERFLOW;
+            or_status(status, flags);
+        }
+    }
+}
+
+__device__ void sort_pad_meta_cta(const SortPadMeta &m, const int32_t *split,
+                                  const int32_t *order, const int32_t *padded_sizes, int C,
+                                  int G, int align, int64_t N, int64_t out_rows,
+                                  int64_t *group_off, int32_t *status, int *s_flags)
+{
+    const int tid = threadIdx.x;
+    if (tid == 0) *s_flags = 0;
+    int flags = 0;
+    for (int c = tid; c < C; c += CH_THREADS) {   // every metadata load issued together
+        int64_t v = split[c];
+        m.s_chunk[c] = order[c];
+        if (v < 0) { flags |= MP_STATUS_BAD_SPLIT; v = 0; }
+        m.s_start[c] = v;
+    }
+    if (padded_sizes != nullptr)
+        for (int g = tid; g < G; g += CH_THREADS) m.s_goff[g] = padded_sizes[g];
+    __syncthreads();
+    const int64_t total_in = cta_exclusive_scan(m.s_start, C, m.s_warp);
+    for (int p = tid; p < C; p += CH_THREADS) {
+        const int32_t c = m.s_chunk[p];
+        const bool ok = c >= 0 && c < C;
+        if (!ok) flags |= MP_STATUS_BAD_ORDER;
+        m.s_chunk[p] = ok ? c : -1;
+        m.s_cum[p] = ok ? ((c + 1 < C ? m.s_start[c + 1] : total_in) - m.s_start[c]) : 0;
+    }
+    __syncthreads();
+    const int64_t total_ord = cta_exclusive_scan(m.s_cum, C, m.s_warp);
+    if (tid == 0) m.s_cum[C] = total_ord;
+    __syncthreads();
+    const int per_group = C / G;
+    for (int g = tid; g < G; g += CH_THREADS)
+        flags |= sort_pad_group_rows(m, g, per_group, align, padded_sizes);
+    if (flags) atomicOr(s_flags, flags);
+    __syncthreads();
+    const int64_t total_pad = cta_exclusive_scan(m.s_goff, G, m.s_warp);
+    if (tid == 0) m.s_goff[G] = total_pad;
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int g = tid; g <= G; g += CH_THREADS) group_off[g] = m.s_goff[g];
+        if (tid == 0) {
+            int bits = *s_flags;
+            if (total_in > N) bits |= MP_STATUS_SPLIT_OVERFLOW;
+            if (total_pad > out_rows) bits |= MP_STATUS_ROWS_OVERFLOW;
+            or_status(status, bits);
+        }
+    }
+}
+
+template <typename V, bool WARP_META>
 __global__ void __launch_bounds__(CH_THREADS)
     k_sort_pad(const V *__restrict__ x, const float *__restrict__ probs,
                const int32_t *__restrict__ split, const int32_t *__restrict__ order,
@@ -115,89 +304,53 @@ __global__ void __launch_bounds__(CH_THREADS)
                int64_t *__restrict__ group_off, int32_t *status)
 {
     extern __shared__ int64_t sm[];
-    int64_t *s_start = sm;               // [C]   first input row of chunk c
-    int64_t *s_cum = s_start + C;        // [C+1] rows before position p in output order
-    int64_t *s_goff = s_cum + C + 1;     // [G+1] padded group offsets
-    int64_t *s_grows = s_goff + G + 1;   // [G]   unpadded rows of group g
-    int64_t *s_warp = s_grows + G;       // [CH_WARPS]
-    int32_t *s_chunk = reinterpret_cast<int32_t *>(s_warp + CH_WARPS);  // [C]
-    int32_t *s_src = s_chunk + C;        // [CH_ROWS]
+    SortPadMeta m;
+    m.s_start = sm;                      // [C]
+    m.s_cum = m.s_start + C;             // [C+1]
+    m.s_goff = m.s_cum + C + 1;          // [G+1]
+    m.s_grows = m.s_goff + G + 1;        // [G]
+    m.s_warp = m.s_grows + G;            // [CH_WARPS]
+    m.s_chunk = reinterpret_cast<int32_t *>(m.s_warp + CH_WARPS);  // [C]
+    int32_t *s_src = m.s_chunk + C;      // [SP_ROWS]
     __shared__ int s_flags;
 
     const int tid = threadIdx.x;
-    if (tid == 0) s_flags = 0;
-    __syncthreads();
-    int flags = 0;
-    for (int c = tid; c < C; c += CH_THREADS) {
-        int64_t v = split[c];
-        if (v < 0) { flags |= MP_STATUS_BAD_SPLIT; v = 0; }
-        s_start[c] = v;
+    if (WARP_META) {
+        if (tid < 32)
+            sort_pad_meta_warp(m, split, order, padded_sizes, C, G, align, N, out_rows,
+                               group_off, status);
+        __syncthreads();
+    } else {
+        sort_pad_meta_cta(m, split, order, padded_sizes, C, G, align, N, out_rows, group_off,
+                          status, &s_flags);
     }
-    __syncthreads();
-    const int64_t total_in = cta_exclusive_scan(s_start, C, s_warp);
-
-    for (int p = tid; p < C; p += CH_THREADS) {
-        const int32_t c = order[p];
-        const bool ok = c >= 0 && c < C;
-        if (!ok) flags |= MP_STATUS_BAD_ORDER;
-        s_chunk[p] = ok ? c : -1;
-        s_cum[p] = ok ? ((c + 1 < C ? s_start[c + 1] : total_in) - s_start[c]) : 0;
-    }
-    if (flags) atomicOr(&s_flags, flags);
-    __syncthreads();
-    const int64_t total_ord = cta_exclusive_scan(s_cum, C, s_warp);
-    if (tid == 0) s_cum[C] = total_ord;
-    __syncthreads();
-
+    const int64_t total_pad = m.s_goff[G];
     const int per_group = C / G;
-    for (int g = tid; g < G; g += CH_THREADS) {
-        const int64_t rows = s_cum[(g + 1) * per_group] - s_cum[g * per_group];
-        s_grows[g] = rows;
-        int64_t padded = (rows + align - 1) / align * align;
-        if (padded_sizes != nullptr) {   // explicit padded sizes
-            const int32_t ps = padded_sizes[g];
-            padded = ps < 0 ? 0 : ps;
-            if (padded < rows) atomicOr(&s_flags, MP_STATUS_BAD_PADDED);
-        }
-        s_goff[g] = padded;
-    }
-    __syncthreads();
-    const int64_t total_pad = cta_exclusive_scan(s_goff, G, s_warp);
-    if (tid == 0) s_goff[G] = total_pad;
-    __syncthreads();
 
-    if (blockIdx.x == 0) {
-        for (int g = tid; g <= G; g += CH_THREADS) group_off[g] = s_goff[g];
-        if (tid == 0) {
-            int bits = s_flags;
-            if (total_in > N) bits |= MP_STATUS_SPLIT_OVERFLOW;
-            if (total_pad > out_rows) bits |= MP_STATUS_ROWS_OVERFLOW;
-            or_status(status, bits);
-        }
-    }
-
-    const int64_t row0 = (int64_t)blockIdx.x * CH_ROWS;
+    const int64_t row0 = (int64_t)blockIdx.x * SP_ROWS;
     const int64_t left = out_rows - row0;
-    const int nrows = left < CH_ROWS ? (int)left : CH_ROWS;
+    const int nrows = left < SP_ROWS ? (int)left : SP_ROWS;
+    float pv = 0.0f;   // this row's prob: loaded now, stored after the copy
     if (tid < nrows) {
         const int64_t d = row0 + tid;
         int32_t src = -1;
         if (d < total_pad) {
-            const int g = last_le(s_goff, 0, G, d);
-            const int64_t j = d - s_goff[g];
-            if (j < s_grows[g]) {
-                const int64_t target = s_cum[g * per_group] + j;
-                const int p = last_le(s_cum, g * per_group, (g + 1) * per_group, target);
-                const int64_t s = s_start[s_chunk[p]] + (target - s_cum[p]);
+            const int g = last_le(m.s_goff, 0, G, d);
+            const int64_t j = d - m.s_goff[g];
+            if (j < m.s_grows[g]) {
+                const int64_t target = m.s_cum[g * per_group] + j;
+                const int p = last_le(m.s_cum, g * per_group, (g + 1) * per_group, target);
+                const int64_t s = m.s_start[m.s_chunk[p]] + (target - m.s_cum[p]);
                 src = s < N ? (int32_t)s : -1;
             }
         }
         s_src[tid] = src;
         row_map[d] = src;
-        if (out_probs != nullptr) out_probs[d] = src >= 0 ? __ldg(probs + src) : 0.0f;
+        if (out_probs != nullptr && src >= 0) pv = __ldg(probs + src);
     }
     __syncthreads();
     if (nrows > 0) copy_rows<V, false>(x, out, s_src, row0, nrows, nvec);
+    if (out_probs != nullptr && tid < nrows) out_probs[row0 + tid] = pv;
 }
 
 template <typename V, bool SCATTER>
@@ -211,24 +364,30 @@ __global__ void __launch_bounds__(CH_THREADS)
     const int64_t row0 = (int64_t)blockIdx.x * CH_ROWS;
     const int64_t left = out_rows - row0;
     const int nrows = left < CH_ROWS ? (int)left : CH_ROWS;
+    // The row's prob is loaded before the copy and stored after it, so its
+    // latency does not hold the CTA at the barrier.
+    float pv = 0.0f;
+    int32_t m = -1;
     if (tid < nrows) {
         const int64_t d = row0 + tid;
-        int32_t m = __ldg(map + d);
+        if (SCATTER && in_probs != nullptr) pv = __ldg(in_probs + d);
+        m = __ldg(map + d);
         if (m < -1 || m >= N) {
             or_status(status, MP_STATUS_BAD_ROW);
             m = -1;
         }
         s_map[tid] = m;
-        if (in_probs != nullptr) {
-            if (SCATTER) {
-                if (m >= 0) out_probs[m] = __ldg(in_probs + d);
-            } else {
-                out_probs[d] = m >= 0 ? __ldg(in_probs + m) : 0.0f;
-            }
-        }
+        if (!SCATTER && in_probs != nullptr && m >= 0) pv = __ldg(in_probs + m);
     }
     __syncthreads();
     copy_rows<V, SCATTER>(in, out, s_map, row0, nrows, nvec);
+    if (in_probs != nullptr && tid < nrows) {
+        if (SCATTER) {
+            if (m >= 0) out_probs[m] = pv;
+        } else {
+            out_probs[row0 + tid] = pv;
+        }
+    }
 }
 
 inline bool chunk_vec_ok(int32_t H, std::initializer_list<const void *> ptrs)
@@ -242,7 +401,7 @@ inline bool chunk_vec_ok(int32_t H, std::initializer_list<const void *> ptrs)
 inline size_t sort_pad_smem(int C, int G)
 {
     return sizeof(int64_t) * (size_t)(C + (C + 1) + (G + 1) + G + CH_WARPS) +
-           sizeof(int32_t) * (size_t)(C + CH_ROWS);
+           sizeof(int32_t) * (size_t)(C + SP_ROWS);
 }
 
 // Rows are H 16-bit units wide.
@@ -306,17 +465,29 @@ mp_status_t sort_pad_impl(const void *x, const float *probs, const int32_t *spli
     if ((probs == nullptr) != (out_probs == nullptr)) return MP_ERR_INVALID_ARG;
     if (out_rows > 0 && (out == nullptr || row_map == nullptr)) return MP_ERR_INVALID_ARG;
     if (N > 0 && x == nullptr) return MP_ERR_INVALID_ARG;
-    const unsigned blocks = out_rows > 0 ? (unsigned)((out_rows + CH_ROWS - 1) / CH_ROWS) : 1u;
+    const unsigned blocks = out_rows > 0 ? (unsigned)((out_rows + SP_ROWS - 1) / SP_ROWS) : 1u;
     const size_t smem = sort_pad_smem(C, G);
     const int32_t w = (int32_t)W;
-    if (chunk_vec_ok(w, {x, out}))
-        k_sort_pad<uint4><<<blocks, CH_THREADS, smem, s>>>(
-            (const uint4 *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N,
-            out_rows, w / 8, (uint4 *)out, out_probs, row_map, group_off, dev_status);
-    else
-        k_sort_pad<uint16_t><<<blocks, CH_THREADS, smem, s>>>(
-            (const uint16_t *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N,
-            out_rows, w, (uint16_t *)out, out_probs, row_map, group_off, dev_status);
+    const bool warp_meta = C <= SP_WARP_META_MAX_C;
+    if (chunk_vec_ok(w, {x, out})) {
+        if (warp_meta)
+            k_sort_pad<uint4, true><<<blocks, CH_THREADS, smem, s>>>(
+                (const uint4 *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N,
+                out_rows, w / 8, (uint4 *)out, out_probs, row_map, group_off, dev_status);
+        else
+            k_sort_pad<uint4, false><<<blocks, CH_THREADS, smem, s>>>(
+                (const uint4 *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N,
+                out_rows, w / 8, (uint4 *)out, out_probs, row_map, group_off, dev_status);
+    } else {
+        if (warp_meta)
+            k_sort_pad<uint16_t, true><<<blocks, CH_THREADS, smem, s>>>(
+                (const uint16_t *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align,
+                N, out_rows, w, (uint16_t *)out, out_probs, row_map, group_off, dev_status);
+        else
+            k_sort_pad<uint16_t, false><<<blocks, CH_THREADS, smem, s>>>(
+                (const uint16_t *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align,
+                N, out_rows, w, (uint16_t *)out, out_probs, row_map, group_off, dev_status);
+    }
     return check_launch();
 }
 

@@ -7,10 +7,13 @@
 // large routed workload of the pages' configurations.
 //
 // k_topk_softmax: one warp per token; lane l holds logits l, l+32, ... (so
-// every load instruction reads 32 consecutive floats).  Group scores are warp
-// max-reductions; the K picks are K warp arg-max reductions on (logit desc,
-// expert asc), lane k keeping pick k.  The softmax runs in fp32: z_k = l_k -
-// l_0, expf (full accuracy), the sum in slot order, IEEE division.
+// every load instruction reads 32 consecutive floats).  Logits are compared
+// through an order-preserving 32-bit key (-0 folded into +0), so a warp's
+// arg-max on (logit desc, expert asc) is two single-instruction warp
+// reductions: the largest key, then the smallest expert holding it.  Group
+// scores are warp max-reductions of the same keys; the K picks are K such
+// arg-max rounds, lane k keeping pick k.  The softmax runs in fp32: z_k = l_k
+// - l_0, expf (full accuracy), the sum in slot order, IEEE division.
 // k_topk_softmax_bwd: one warp per token: zero the token's E gradients, then
 // p_k * (g_k - sum_j p_j g_j) at the picked experts.
 #include <cfloat>
@@ -24,25 +27,29 @@ namespace {
 constexpr int RT_THREADS = 256;
 constexpr int RT_WARPS = RT_THREADS / 32;
 
-// (value, index) arg-max across the warp: larger value, then smaller index.
-__device__ __forceinline__ void warp_argmax(float &v, int &i)
+// A 32-bit key with the order of the floats: key(a) < key(b) iff a < b (for
+// non-NaN values; -0 and +0 get the same key).  Every float's key is > 0, so 0
+// stands for "no candidate".
+__device__ __forceinline__ uint32_t order_key(float f)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(FULL_MASK, v, o);
-        const int oi = __shfl_xor_sync(FULL_MASK, i, o);
-        if (ov > v || (ov == v && oi < i)) {
-            v = ov;
-            i = oi;
-        }
-    }
+    uint32_t u = __float_as_uint(f);
+    if ((u << 1) == 0u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ float warp_max(float v)
+__device__ __forceinline__ float key_value(uint32_t k)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL_MASK, v, o));
-    return v;
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Arg-max across the warp on (key desc, index asc); every lane gets the
+// winning index (the key is returned through `key`).
+__device__ __forceinline__ uint32_t warp_argmax_key(uint32_t &key, uint32_t idx)
+{
+    const uint32_t m = __reduce_max_sync(FULL_MASK, key);
+    const uint32_t i = __reduce_min_sync(FULL_MASK, key == m ? idx : 0xffffffffu);
+    key = m;
+    return i;
 }
 
 template <int PER>
@@ -69,26 +76,21 @@ __global__ void __launch_bounds__(RT_THREADS)
     if (n_groups > 1) {
         const int per_group = E / n_groups;
         unsigned group_kept = 0;   // bit g: group g kept (same in every lane)
-        float score_g = -FLT_MAX;  // lane g holds group g's score
+        uint32_t score_g = 0;      // lane g holds group g's score key
         for (int g = 0; g < n_groups; ++g) {
-            float m = -FLT_MAX;
-            bool any = false;
+            uint32_t m = 0;
 #pragma unroll
             for (int j = 0; j < PER; ++j) {
                 const int e = lane + 32 * j;
-                if ((live >> j & 1u) && e / per_group == g) {
-                    m = any ? fmaxf(m, v[j]) : v[j];
-                    any = true;
-                }
+                if ((live >> j & 1u) && e / per_group == g) m = max(m, order_key(v[j]));
             }
-            m = warp_max(m);
+            m = __reduce_max_sync(FULL_MASK, m);
             if (lane == g) score_g = m;
         }
         for (int j = 0; j < topk_groups; ++j) {
-            float sv = (lane < n_groups && !(group_kept >> lane & 1u)) ? score_g : -FLT_MAX;
-            int si = (lane < n_groups && !(group_kept >> lane & 1u)) ? lane : INT_MAX;
-            warp_argmax(sv, si);
-            group_kept |= 1u << si;
+            uint32_t sk = (lane < n_groups && !(group_kept >> lane & 1u)) ? score_g : 0u;
+            const uint32_t gi = warp_argmax_key(sk, (uint32_t)lane);
+            group_kept |= 1u << gi;
         }
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
@@ -97,24 +99,24 @@ __global__ void __launch_bounds__(RT_THREADS)
         }
     }
 
+    uint32_t key[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) key[j] = order_key(v[j]);
     float my_v = 0.0f;
     int my_i = -1;
     for (int k = 0; k < K; ++k) {
-        float bv = -FLT_MAX;
-        int bi = INT_MAX;
+        uint32_t bk = 0u, bi = 0xffffffffu;   // this lane's best live expert
 #pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int e = lane + 32 * j;
-            if ((live >> j & 1u) && (bi == INT_MAX || v[j] > bv)) {
-                bv = v[j];
-                bi = e;
+        for (int j = 0; j < PER; ++j)
+            if ((live >> j & 1u) && key[j] > bk) {
+                bk = key[j];
+                bi = (uint32_t)(lane + 32 * j);
             }
-        }
-        warp_argmax(bv, bi);
-        if (bi != INT_MAX && (bi & 31) == lane) live &= ~(1u << (bi >> 5));
-        if (lane == (k & 31) && k < 32) {
-            my_v = bv;
-            my_i = bi;
+        const uint32_t pick = warp_argmax_key(bk, bi);
+        if ((int)(pick & 31u) == lane) live &= ~(1u << (pick >> 5));
+        if (lane == k) {
+            my_v = key_value(bk);
+            my_i = (int)pick;
         }
     }
     const float m = __shfl_sync(FULL_MASK, my_v, 0);
