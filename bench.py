@@ -571,6 +571,9 @@ def run_gpu(args):
         ep_bytes = nbytes["unpermute"] + 4 * T * K        # + the slot experts
         logits = dev_t(wl.router_logits(WORKLOAD, T=T, seed=base_seed))
         r_idx, r_probs = torch.empty_like(idx), torch.empty_like(probs)
+        g_rp = torch.ones_like(probs)
+        g_logits = torch.empty_like(logits)
+        quarter = torch.tensor([R * 3 // 4], dtype=torch.int32, device=dev)
         rim_c, s2f_c = torch.empty_like(rim), torch.empty_like(s2f)
         counts_c, offsets_c = torch.empty_like(counts), torch.empty_like(offsets)
         extra_ops = {
@@ -582,6 +585,13 @@ def run_gpu(args):
             "topk_softmax(router)": (
                 lambda: mp.mp_topk_softmax(logits, K, idx=r_idx, probs=r_probs),
                 4 * T * E + 8 * T * K),
+            "topk_softmax_bwd(router)": (
+                lambda: mp.mp_topk_softmax_bwd(g_rp, r_probs, r_idx, E, g_logits=g_logits),
+                12 * T * K + 4 * T * E),
+            "zero_rows_from(last quarter of the rows)": (
+                lambda: mp.mp_zero_rows_from(g_rows, quarter), (R - R * 3 // 4) * 2 * H),
+            "zero_rows_from(all rows routed: no store)": (
+                lambda: mp.mp_zero_rows_from(g_rows, offsets[-1:]), 0),
             f"unpermute_ep(ep={ep})": (
                 lambda: mp.mp_unpermute_ep(rows, rim, idx, E, ep, probs, out=y), ep_bytes),
             f"unpermute_ep(ep={ep},bf16_partials)": (
@@ -593,10 +603,13 @@ def run_gpu(args):
         }
         call("build_map")
         call("permute")
+        mp.mp_topk_softmax(logits, K, idx=r_idx, probs=r_probs)
         for name, (fn, b) in extra_ops.items():
             us = time_op(fn, flush, stream, max(30, min(args.steps, 100)))
             extras[name] = {"us": round(us, 2), "GB/s": round(b / (us * 1e-6) / 1e9, 1),
                             "frac_of_measured": round(b / (us * 1e-6) / 1e9 / peak, 4)}
+        call("build_map")
+        call("permute")
 
     out = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
