@@ -8,8 +8,9 @@
 // expert-major, tokens ascending, slots ascending.
 //
 // The routes are cut into tiles of 2048*f consecutive routes (f, a power of
-// two up to 8, keeps the tile count near 64).  Inside a tile, warp w owns the
-// contiguous range [w*256f, (w+1)*256f) and walks it in chunks of 32 routes:
+// two up to 8, keeps the tile count near 64).  Inside a tile (16 warps), warp
+// w owns the contiguous range [w*128f, (w+1)*128f) and walks it in chunks of
+// 32 routes (more warps with shorter walks: the map is latency-bound):
 // __match_any_sync groups the lanes that name one expert, and
 // popc(peers & lanemask_lt) is a lane's stable rank inside the chunk.
 //
@@ -44,10 +45,17 @@ void set_last_cuda_error(cudaError_t err) { g_last_cuda_error = static_cast<int3
 
 namespace {
 
-constexpr int MAP_THREADS = 256;
+#ifndef MP_MAP_THREADS
+#define MP_MAP_THREADS 512
+#endif
+#ifndef MP_MAP_CHUNKS
+#define MP_MAP_CHUNKS 4
+#endif
+
+constexpr int MAP_THREADS = MP_MAP_THREADS;
 constexpr int MAP_WARPS = MAP_THREADS / 32;
-constexpr int MAP_CHUNKS = 8;                          // 32-route chunks per warp group
-constexpr int MAP_GROUP = MAP_CHUNKS * 32;             // 256 routes per warp group
+constexpr int MAP_CHUNKS = MP_MAP_CHUNKS;              // 32-route chunks per warp group
+constexpr int MAP_GROUP = MAP_CHUNKS * 32;             // 128 routes per warp group
 constexpr int MAP_SUB = MAP_WARPS * MAP_GROUP;         // 2048 routes: a tile with f = 1
 constexpr int MAP_TARGET_TILES = 64;
 constexpr int MAP_MAX_F = 8;
@@ -461,10 +469,16 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *r
                                      counts, offsets);
         }
     } else {
-        k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)p.ntiles, cap, counts, offsets);
-        k_map_rank<false><<<grid, MAP_THREADS, smem, s>>>(idx, n, E, p.f, (int)p.ntiles, cap,
-                                                          tile_counts, row_id_map, sorted_to_flat,
-                                                          counts, offsets);
+        if (smem > 48 * 1024)
+            err = cudaFuncSetAttribute(k_map_rank<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err == cudaSuccess) {
+            k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)p.ntiles, cap, counts,
+                                                  offsets);
+            k_map_rank<false><<<grid, MAP_THREADS, smem, s>>>(idx, n, E, p.f, (int)p.ntiles, cap,
+                                                              tile_counts, row_id_map,
+                                                              sorted_to_flat, counts, offsets);
+        }
     }
     if (err != cudaSuccess) {
         cudaGetLastError();
