@@ -597,6 +597,9 @@ def run_gpu(args):
             f"unpermute_ep(ep={ep},bf16_partials)": (
                 lambda: mp.mp_unpermute_ep(rows, rim, idx, E, ep, probs, bf16_partials=True,
                                            out=y), ep_bytes),
+            f"unpermute_ep(ep={ep},fp64_cross_rank)": (
+                lambda: mp.mp_unpermute_ep(rows, rim, idx, E, ep, probs, fp64_cross_rank=True,
+                                           out=y), ep_bytes),
             f"unpermute_ep(ep={ep},bf16_partials,fp64_cross_rank)": (
                 lambda: mp.mp_unpermute_ep(rows, rim, idx, E, ep, probs, bf16_partials=True,
                                            fp64_cross_rank=True, out=y), ep_bytes),

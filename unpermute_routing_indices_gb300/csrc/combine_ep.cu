@@ -139,8 +139,14 @@ __device__ __forceinline__ void walk_ranks(const V (&r)[EP_KMAX], const float (&
     }
 }
 
+// CTAs per SM each variant is compiled for (registers are capped to fit).
+// Measured on the skewed T=16384, ep=8 combine: occupancy outweighs the
+// registers it spills (fp32 215 -> 187 us at 7 CTAs, bf16 partials 243 ->
+// 199 us, fp64 with bf16 / fp32 partials best at 6 / 5).
+constexpr int ep_min_blocks(bool fp64, bool bf16p) { return fp64 ? (bf16p ? 6 : 5) : 7; }
+
 template <typename V, bool PROBS, bool BF16P, bool FP64>
-__global__ void __launch_bounds__(EP_THREADS, FP64 ? 4 : 1)
+__global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
     k_unpermute_ep(const V *__restrict__ rows, const float *__restrict__ probs,
                    const int32_t *__restrict__ map, const int32_t *__restrict__ idx, int64_t T,
                    int K, int nvec, int tpt_log2, int per_rank, V *__restrict__ out)
