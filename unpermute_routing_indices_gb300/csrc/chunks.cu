@@ -29,6 +29,9 @@ namespace {
 #define MP_CH_UNROLL 8
 #endif
 
+#ifndef MP_CH_MIN_BLOCKS
+#define MP_CH_MIN_BLOCKS 1
+#endif
 #ifndef MP_SP_ROWS
 #define MP_SP_ROWS 32
 #endif
@@ -295,7 +298,7 @@ __device__ void sort_pad_meta_cta(const SortPadMeta &m, const int32_t *split,
 }
 
 template <typename V, bool WARP_META>
-__global__ void __launch_bounds__(CH_THREADS)
+__global__ void __launch_bounds__(CH_THREADS, MP_CH_MIN_BLOCKS)
     k_sort_pad(const V *__restrict__ x, const float *__restrict__ probs,
                const int32_t *__restrict__ split, const int32_t *__restrict__ order,
                const int32_t *__restrict__ padded_sizes, int C, int G,
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(CH_THREADS)
 }
 
 template <typename V, bool SCATTER>
-__global__ void __launch_bounds__(CH_THREADS)
+__global__ void __launch_bounds__(CH_THREADS, MP_CH_MIN_BLOCKS)
     k_rows_remap(const V *__restrict__ in, const float *__restrict__ in_probs,
                  const int32_t *__restrict__ map, int64_t out_rows, int64_t N, int nvec,
                  V *__restrict__ out, float *__restrict__ out_probs, int32_t *status)
