@@ -107,3 +107,40 @@ def test_chunk_ops_reject(lib):
     assert lib.mp_unpad_restore(FAKE, None, FAKE, 0, 10, 8, FAKE, None, None, None) == 0
     assert lib.mp_unpad_restore_bwd(FAKE, None, None, 10, 10, 8, FAKE, None, None, None) == -1
     assert lib.mp_sort_chunks_pad_bwd(FAKE, None, FAKE, -1, 10, 8, FAKE, None, None, None) == -1
+
+
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, -1, 64, 8, 1, 1, FAKE, FAKE, None), -1),      # T < 0
+    ((FAKE, 4, 64, 0, 1, 1, FAKE, FAKE, None), -1),       # K < 1
+    ((FAKE, 4, 64, 33, 1, 1, FAKE, FAKE, None), -3),      # K > 32
+    ((FAKE, 4, 2048, 8, 1, 1, FAKE, FAKE, None), -3),     # E > MP_MAX_EXPERTS
+    ((FAKE, 4, 64, 8, 64, 1, FAKE, FAKE, None), -3),      # n_groups > 32
+    ((FAKE, 4, 64, 8, 3, 1, FAKE, FAKE, None), -1),       # E % n_groups != 0
+    ((FAKE, 4, 64, 8, 8, 9, FAKE, FAKE, None), -1),       # topk_groups > n_groups
+    ((FAKE, 4, 64, 8, 16, 1, FAKE, FAKE, None), -1),      # kept experts < K
+    ((FAKE, 4, 4, 8, 1, 1, FAKE, FAKE, None), -1),        # K > E
+    ((FAKE, 0, 64, 8, 1, 1, None, None, None), 0),        # empty: no-op
+    ((None, 4, 64, 8, 1, 1, FAKE, FAKE, None), -1),       # logits NULL
+])
+def test_router_rejects(lib, args, code):
+    assert lib.mp_topk_softmax(*args) == code
+
+
+def test_router_bwd_rejects(lib):
+    assert lib.mp_topk_softmax_bwd(FAKE, FAKE, FAKE, 4, 64, 33, FAKE, None) == -3   # K > 32
+    assert lib.mp_topk_softmax_bwd(FAKE, FAKE, FAKE, 4, 2048, 8, FAKE, None) == -3  # E too big
+    assert lib.mp_topk_softmax_bwd(FAKE, FAKE, None, 4, 64, 8, FAKE, None) == -1    # idx NULL
+    assert lib.mp_topk_softmax_bwd(None, None, None, 0, 64, 8, None, None) == 0     # empty
+
+
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, None, FAKE, FAKE, 2**30, 4, 64, 64, 8, 0, FAKE, None), -1),   # T*K > int32
+    ((FAKE, None, FAKE, FAKE, 4, 2, 64, 64, 6, 0, FAKE, None), -1),       # E % ep_size != 0
+    ((FAKE, None, FAKE, FAKE, 4, 2, 64, 64, 0, 0, FAKE, None), -1),       # ep_size < 1
+    ((FAKE, None, FAKE, FAKE, 4, 2, 64, 64, 8, 4, FAKE, None), -1),       # unknown flag
+    ((FAKE, None, FAKE, FAKE, 4, 9, 64, 64, 8, 0, FAKE, None), -3),       # K > 8
+    ((FAKE, None, FAKE, None, 4, 2, 64, 64, 8, 0, FAKE, None), -1),       # idx NULL
+    ((None, None, None, None, 0, 2, 64, 64, 8, 3, None, None), 0),        # empty: no-op
+])
+def test_unpermute_ep_rejects(lib, args, code):
+    assert lib.mp_unpermute_ep(*args) == code

@@ -17,8 +17,12 @@
 namespace mp {
 namespace {
 
+#ifndef MP_FILL_MAX_BLOCKS
+#define MP_FILL_MAX_BLOCKS (152 * 8)
+#endif
+
 constexpr int FILL_THREADS = 256;
-constexpr int FILL_MAX_BLOCKS = 152 * 8;
+constexpr int FILL_MAX_BLOCKS = MP_FILL_MAX_BLOCKS;
 
 template <typename V>
 __global__ void __launch_bounds__(FILL_THREADS)
