@@ -514,7 +514,7 @@ def run_gpu(args):
         h_outs[0]["g_x"].copy_(g_x, non_blocking=True)
         h_outs[0]["g_probs"].copy_(g_probs, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 50))
+    e2e_steps = max(50, min(args.steps, 200))   # its own count: the pipeline fills and drains once
     for _ in range(max(args.warmup, 3)):
         e2e_step()
     torch.cuda.synchronize()
