@@ -319,6 +319,24 @@ def test_permute_bwd_is_adjoint_of_permute():
     assert np.all(g_p[rim < 0] == 0)
 
 
+def test_permute_bwd_of_permute_with_one_slot_is_identity():
+    """K = 1, no probs: each token has one row, and the backward's slot sum
+    of a single bf16 value (widened to fp32 and rounded back) is that value,
+    except -0, which comes back as +0 because the sum starts from +0."""
+    rng = np.random.default_rng(33)
+    T, E, H = 57, 5, 9
+    idx = rng.integers(0, E, size=(T, 1)).astype(np.int32)
+    rim, *_ = oracle.build_map(idx, E)
+    x = rng.integers(0, 1 << 16, size=(T, H)).astype(np.uint16)
+    x[(x & 0x7F80) == 0x7F80] = 0x3F80          # no inf / NaN patterns
+    x[::7, 2] = 0x8000                           # -0
+    x[::5, 3] = 0x0001                           # the smallest subnormal
+    out, _ = oracle.permute(x, None, rim)
+    g_x, _ = oracle.permute_bwd(out, None, rim, T, H)
+    want = np.where(x == 0x8000, np.uint16(0), x)
+    np.testing.assert_array_equal(g_x, want)
+
+
 def test_unpermute_bwd_is_adjoint_of_unpermute():
     T, K, E, H = 24, 4, 6, 10
     rng = np.random.default_rng(41)
