@@ -103,6 +103,22 @@ def test_sort_pad_edges(G, R, align, H, empty_group, extra):
     np.testing.assert_array_equal(h(out2), h(out))
 
 
+def test_sort_pad_many_chunks_large_output():
+    """512 chunks (metadata built by the whole CTA) and more than 16,384 output
+    rows (one row per warp in flight): the remaining kernel variant."""
+    G, R, align, H = 16, 32, 8, 512
+    sizes, order = _meta(512, G, R, max_size=120)
+    N = int(sizes.sum())
+    out_rows = N + G * (align - 1) + 11
+    assert out_rows > 16384 and G * R > 256
+    x = wl.random_rows(N, H, 4)
+    probs = np.random.default_rng(5).random(N).astype(np.float32)
+    out, out_p, row_map, _ = run_case(x, probs, sizes, order, G, align, out_rows)
+    y, y_p = mp.mp_unpad_restore(out, row_map, N, out_p)
+    np.testing.assert_array_equal(h(y), x)
+    np.testing.assert_array_equal(h(y_p), probs)
+
+
 def test_sort_pad_status_bits():
     x = wl.random_rows(64, 16, 5)
     p = np.arange(64, dtype=np.float32)

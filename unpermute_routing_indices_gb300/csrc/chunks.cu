@@ -32,6 +32,9 @@ namespace {
 #ifndef MP_CH_MIN_BLOCKS
 #define MP_CH_MIN_BLOCKS 1
 #endif
+#ifndef MP_SP_RP2_MAX_ROWS
+#define MP_SP_RP2_MAX_ROWS 16384
+#endif
 #ifndef MP_SP_ROWS
 #define MP_SP_ROWS 32
 #endif
@@ -117,30 +120,43 @@ __device__ __forceinline__ int last_le(const int64_t *a, int lo, int hi, int64_t
 // Rows of at least 32 vectors go one warp per row, the lanes across the row
 // (CH_UNROLL vectors in flight per lane, addresses by immediate offsets from
 // the row base); narrower rows are spread over the CTA as one flat range.
-template <typename V, bool SCATTER>
+template <typename V, bool SCATTER, int RP = 1>
 __device__ __forceinline__ void copy_rows(const V *__restrict__ in, V *__restrict__ out,
                                           const int32_t *s_map, int64_t row0, int nrows, int nvec)
 {
     if (nvec >= 32) {
+        // One warp per RP rows at a time: RP * CH_UNROLL vectors in flight per lane.
         const int lane = threadIdx.x & 31;
-        for (int r = threadIdx.x >> 5; r < nrows; r += CH_WARPS) {
-            const int32_t m = s_map[r];
-            if (SCATTER && m < 0) continue;
-            const bool zero = !SCATTER && m < 0;
-            const V *src = in + (SCATTER ? row0 + r : (int64_t)(zero ? 0 : m)) * nvec;
-            V *dst = out + (SCATTER ? (int64_t)m : row0 + r) * nvec;
+        for (int r0 = (threadIdx.x >> 5) * RP; r0 < nrows; r0 += CH_WARPS * RP) {
+            const V *src[RP];
+            V *dst[RP];
+            bool live[RP], zero[RP];
+#pragma unroll
+            for (int q = 0; q < RP; ++q) {
+                const int r = r0 + q;
+                const int32_t m = r < nrows ? s_map[r] : -1;
+                live[q] = r < nrows && (!SCATTER || m >= 0);
+                zero[q] = !SCATTER && m < 0;
+                src[q] = in + (SCATTER ? row0 + r : (int64_t)(m < 0 ? 0 : m)) * nvec;
+                dst[q] = out + (SCATTER ? (int64_t)(m < 0 ? 0 : m) : row0 + r) * nvec;
+            }
             for (int c0 = lane; c0 < nvec; c0 += 32 * CH_UNROLL) {
-                V v[CH_UNROLL];
+                V v[RP][CH_UNROLL];
 #pragma unroll
-                for (int u = 0; u < CH_UNROLL; ++u) {
-                    const int c = c0 + 32 * u;
-                    v[u] = (!zero && c < nvec) ? ld_stream(src + c) : zero_vec<V>();
-                }
+                for (int q = 0; q < RP; ++q)
 #pragma unroll
-                for (int u = 0; u < CH_UNROLL; ++u) {
-                    const int c = c0 + 32 * u;
-                    if (c < nvec) st_row(dst + c, v[u]);
-                }
+                    for (int u = 0; u < CH_UNROLL; ++u) {
+                        const int c = c0 + 32 * u;
+                        v[q][u] = (live[q] && !zero[q] && c < nvec) ? ld_stream(src[q] + c)
+                                                                     : zero_vec<V>();
+                    }
+#pragma unroll
+                for (int q = 0; q < RP; ++q)
+#pragma unroll
+                    for (int u = 0; u < CH_UNROLL; ++u) {
+                        const int c = c0 + 32 * u;
+                        if (live[q] && c < nvec) st_row(dst[q] + c, v[q][u]);
+                    }
             }
         }
         return;
@@ -297,7 +313,7 @@ __device__ void sort_pad_meta_cta(const SortPadMeta &m, const int32_t *split,
     }
 }
 
-template <typename V, bool WARP_META>
+template <typename V, bool WARP_META, int RP>
 __global__ void __launch_bounds__(CH_THREADS, MP_CH_MIN_BLOCKS)
     k_sort_pad(const V *__restrict__ x, const float *__restrict__ probs,
                const int32_t *__restrict__ split, const int32_t *__restrict__ order,
@@ -352,7 +368,7 @@ __global__ void __launch_bounds__(CH_THREADS, MP_CH_MIN_BLOCKS)
         if (out_probs != nullptr && src >= 0) pv = __ldg(probs + src);
     }
     __syncthreads();
-    if (nrows > 0) copy_rows<V, false>(x, out, s_src, row0, nrows, nvec);
+    if (nrows > 0) copy_rows<V, false, RP>(x, out, s_src, row0, nrows, nvec);
     if (out_probs != nullptr && tid < nrows) out_probs[row0 + tid] = pv;
 }
 
@@ -472,25 +488,23 @@ mp_status_t sort_pad_impl(const void *x, const float *probs, const int32_t *spli
     const size_t smem = sort_pad_smem(C, G);
     const int32_t w = (int32_t)W;
     const bool warp_meta = C <= SP_WARP_META_MAX_C;
+    // Small outputs (about one wave of CTAs) keep two rows per warp in
+    // flight; larger ones keep one, for more resident CTAs.
+    const bool two = out_rows <= MP_SP_RP2_MAX_ROWS;
+#define MP_SORT_PAD_LAUNCH(VT, WM, RPV, NV)                                                  \
+    k_sort_pad<VT, WM, RPV><<<blocks, CH_THREADS, smem, s>>>(                               \
+        (const VT *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N, out_rows, \
+        NV, (VT *)out, out_probs, row_map, group_off, dev_status)
     if (chunk_vec_ok(w, {x, out})) {
-        if (warp_meta)
-            k_sort_pad<uint4, true><<<blocks, CH_THREADS, smem, s>>>(
-                (const uint4 *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N,
-                out_rows, w / 8, (uint4 *)out, out_probs, row_map, group_off, dev_status);
-        else
-            k_sort_pad<uint4, false><<<blocks, CH_THREADS, smem, s>>>(
-                (const uint4 *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N,
-                out_rows, w / 8, (uint4 *)out, out_probs, row_map, group_off, dev_status);
+        if (warp_meta && two) MP_SORT_PAD_LAUNCH(uint4, true, 2, w / 8);
+        else if (warp_meta) MP_SORT_PAD_LAUNCH(uint4, true, 1, w / 8);
+        else if (two) MP_SORT_PAD_LAUNCH(uint4, false, 2, w / 8);
+        else MP_SORT_PAD_LAUNCH(uint4, false, 1, w / 8);
     } else {
-        if (warp_meta)
-            k_sort_pad<uint16_t, true><<<blocks, CH_THREADS, smem, s>>>(
-                (const uint16_t *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align,
-                N, out_rows, w, (uint16_t *)out, out_probs, row_map, group_off, dev_status);
-        else
-            k_sort_pad<uint16_t, false><<<blocks, CH_THREADS, smem, s>>>(
-                (const uint16_t *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align,
-                N, out_rows, w, (uint16_t *)out, out_probs, row_map, group_off, dev_status);
+        if (warp_meta) MP_SORT_PAD_LAUNCH(uint16_t, true, 1, w);
+        else MP_SORT_PAD_LAUNCH(uint16_t, false, 1, w);
     }
+#undef MP_SORT_PAD_LAUNCH
     return check_launch();
 }
 
