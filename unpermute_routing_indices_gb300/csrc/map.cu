@@ -57,7 +57,10 @@ constexpr int MAP_WARPS = MAP_THREADS / 32;
 constexpr int MAP_CHUNKS = MP_MAP_CHUNKS;              // 32-route chunks per warp group
 constexpr int MAP_GROUP = MAP_CHUNKS * 32;             // 128 routes per warp group
 constexpr int MAP_SUB = MAP_WARPS * MAP_GROUP;         // 2048 routes: a tile with f = 1
-constexpr int MAP_TARGET_TILES = 64;
+#ifndef MP_MAP_TARGET_TILES
+#define MP_MAP_TARGET_TILES 64
+#endif
+constexpr int MAP_TARGET_TILES = MP_MAP_TARGET_TILES;
 constexpr int MAP_MAX_F = 8;
 constexpr int64_t MAP_FUSED_MAX_COUNTS = 32768;        // count matrix each rank CTA reads
 constexpr int SCAN_THREADS = 1024;
