@@ -90,8 +90,9 @@ int32_t mp_last_cuda_error(void);
 /* Routing map  [d9d make_row_id_map; mops "Operators: permute"; xt]         */
 /* ------------------------------------------------------------------------ */
 
-/* Bytes of device workspace mp_build_map needs for these sizes (a multiple
- * of 256; 0 never).  Returns 0 for invalid sizes. */
+/* Bytes of device workspace mp_build_map (and mp_build_map_capacity) needs
+ * for these sizes: a multiple of 256, at least 256.  Returns 0 only for
+ * invalid sizes (those mp_build_map rejects). */
 size_t mp_build_map_workspace_size(int64_t T, int32_t K, int32_t E);
 
 /*
@@ -178,7 +179,9 @@ mp_status_t mp_build_map_noalloc(const int32_t *idx, int64_t T, int32_t K, int32
  * scores favour the lower group); then pick the K largest logits among the
  * kept experts (equal logits favour the lower expert), slot 0 the largest.
  * probs = fp32 softmax over the K picked logits: z_k = l_k - l_0, expf
- * (CUDA's full-accuracy expf), sum in slot order, IEEE division.
+ * (CUDA's full-accuracy expf), sum in slot order, IEEE division.  Logits
+ * compare as floats (+0 and -0 are equal); with a NaN logit the picks are
+ * unspecified.
  *   logits  device fp32 [T,E];  idx device int32 [T,K];  probs device fp32 [T,K]
  * Limits: E <= MP_MAX_EXPERTS, K <= 32, n_groups <= 32, E % n_groups == 0,
  * topk_groups * E / n_groups >= K.
@@ -207,11 +210,12 @@ mp_status_t mp_topk_softmax_bwd(const float *g_probs, const float *probs, const 
  * probs[t,k], for every non-empty slot.  The row is copied whatever its
  * probability.
  *   x          device bf16 [T,H]
- *   probs      device fp32 [T,K] or NULL (then out_probs is ignored)
+ *   probs      device fp32 [T,K] or NULL
  *   row_id_map device int32 [T,K] from mp_build_map
  *   out        device bf16 [R_out,H], R_out > every row id (T*K suffices);
  *              rows no slot maps to are not written.
- *   out_probs  device fp32 [R_out] or NULL
+ *   out_probs  device fp32 [R_out] or NULL; given exactly when probs is
+ *              (otherwise MP_ERR_INVALID_ARG)
  */
 mp_status_t mp_permute(const mp_bf16_t *x, const float *probs, const int32_t *row_id_map,
                        int64_t T, int32_t K, int32_t H, mp_bf16_t *out, float *out_probs,
@@ -313,7 +317,8 @@ mp_status_t mp_zero_rows_from(void *buf, int64_t rows, int64_t row_bytes,
  * chunk's rows consecutive and in input order, then zero rows up to a
  * multiple of `align`.  Output rows past the padded total, up to out_rows,
  * are zero too.
- *   x, probs            device bf16 [N,H], fp32 [N] or NULL
+ *   x, probs            device bf16 [N,H], fp32 [N] or NULL (probs and
+ *                       out_probs are both given or both NULL)
  *   split_sizes         device int32 [C]   (runtime data: a graph replays with
  *   chunk_order         device int32 [C]    new sizes in the same buffers)
  *   out, out_probs      device bf16 [out_rows,H], fp32 [out_rows] or NULL
