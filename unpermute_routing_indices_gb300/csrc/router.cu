@@ -11,8 +11,11 @@
 // through an order-preserving 32-bit key (-0 folded into +0), so a warp's
 // arg-max on (logit desc, expert asc) is two single-instruction warp
 // reductions: the largest key, then the smallest expert holding it.  Group
-// scores are warp max-reductions of the same keys; the K picks are K such
-// arg-max rounds, lane k keeping pick k.  The softmax runs in fp32: z_k = l_k
+// scores are warp max-reductions of the same keys.  For the K picks (up to
+// 256 experts) each lane first sorts its own experts with a fixed sorting
+// network, so a round is the two reductions on the lanes' heads and the
+// winner drops its head; wider rows rescan each lane's experts per round.
+// Lane k keeps pick k.  The softmax runs in fp32: z_k = l_k
 // - l_0, expf (full accuracy), the sum in slot order, IEEE division.
 // k_topk_softmax_bwd: one warp per token: zero the token's E gradients, then
 // p_k * (g_k - sum_j p_j g_j) at the picked experts.
@@ -50,6 +53,32 @@ __device__ __forceinline__ uint32_t warp_argmax_key(uint32_t &key, uint32_t idx)
     const uint32_t i = __reduce_min_sync(FULL_MASK, key == m ? idx : 0xffffffffu);
     key = m;
     return i;
+}
+
+// Compare-exchange for a descending order on (key desc, index asc).
+__device__ __forceinline__ void cx_desc(uint32_t &ka, uint32_t &ia, uint32_t &kb, uint32_t &ib)
+{
+    const bool keep = ka > kb || (ka == kb && ia < ib);
+    const uint32_t k0 = keep ? ka : kb, k1 = keep ? kb : ka;
+    const uint32_t i0 = keep ? ia : ib, i1 = keep ? ib : ia;
+    ka = k0; kb = k1; ia = i0; ib = i1;
+}
+
+// Batcher's odd-even merge sort of N (a power of two) (key, index) pairs,
+// descending; every index is a compile-time constant once unrolled.
+template <int N>
+__device__ __forceinline__ void sort_desc(uint32_t (&k)[N], uint32_t (&ix)[N])
+{
+#pragma unroll
+    for (int p = 1; p < N; p <<= 1)
+#pragma unroll
+        for (int q = p; q >= 1; q >>= 1)
+#pragma unroll
+            for (int j = q % p; j + q < N; j += 2 * q)
+#pragma unroll
+                for (int i = 0; i < q; ++i)
+                    if (i + j + q < N && (i + j) / (2 * p) == (i + j + q) / (2 * p))
+                        cx_desc(k[i + j], ix[i + j], k[i + j + q], ix[i + j + q]);
 }
 
 template <int PER>
@@ -99,24 +128,55 @@ __global__ void __launch_bounds__(RT_THREADS)
         }
     }
 
-    uint32_t key[PER];
-#pragma unroll
-    for (int j = 0; j < PER; ++j) key[j] = order_key(v[j]);
     float my_v = 0.0f;
     int my_i = -1;
-    for (int k = 0; k < K; ++k) {
-        uint32_t bk = 0u, bi = 0xffffffffu;   // this lane's best live expert
+    if constexpr (PER <= 8) {
+        // Each lane sorts its live experts once (dead ones get key 0, last);
+        // a round's winner then drops its head, so every lane's head stays
+        // its best remaining expert.
+        uint32_t key[PER], ex[PER];
 #pragma unroll
-        for (int j = 0; j < PER; ++j)
-            if ((live >> j & 1u) && key[j] > bk) {
-                bk = key[j];
-                bi = (uint32_t)(lane + 32 * j);
+        for (int j = 0; j < PER; ++j) {
+            key[j] = (live >> j & 1u) ? order_key(v[j]) : 0u;
+            ex[j] = (uint32_t)(lane + 32 * j);
+        }
+        sort_desc<PER>(key, ex);
+        for (int k = 0; k < K; ++k) {
+            uint32_t bk = key[0];
+            const uint32_t pick = warp_argmax_key(bk, ex[0]);
+            if ((int)(pick & 31u) == lane) {
+#pragma unroll
+                for (int j = 0; j + 1 < PER; ++j) {
+                    key[j] = key[j + 1];
+                    ex[j] = ex[j + 1];
+                }
+                key[PER - 1] = 0u;
             }
-        const uint32_t pick = warp_argmax_key(bk, bi);
-        if ((int)(pick & 31u) == lane) live &= ~(1u << (pick >> 5));
-        if (lane == k) {
-            my_v = key_value(bk);
-            my_i = (int)pick;
+            if (lane == k) {
+                my_v = key_value(bk);
+                my_i = (int)pick;
+            }
+        }
+    } else {
+        // Wide rows (more than 256 experts): each round rescans the lane's
+        // live experts (a sort network that large would not stay in registers).
+        uint32_t key[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) key[j] = order_key(v[j]);
+        for (int k = 0; k < K; ++k) {
+            uint32_t bk = 0u, bi = 0xffffffffu;   // this lane's best live expert
+#pragma unroll
+            for (int j = 0; j < PER; ++j)
+                if ((live >> j & 1u) && key[j] > bk) {
+                    bk = key[j];
+                    bi = (uint32_t)(lane + 32 * j);
+                }
+            const uint32_t pick = warp_argmax_key(bk, bi);
+            if ((int)(pick & 31u) == lane) live &= ~(1u << (pick >> 5));
+            if (lane == k) {
+                my_v = key_value(bk);
+                my_i = (int)pick;
+            }
         }
     }
     const float m = __shfl_sync(FULL_MASK, my_v, 0);
