@@ -294,7 +294,9 @@ __device__ int32_t cta_exclusive_scan(int32_t *a, int n, int32_t *s_warp)
 
 inline size_t rank_smem(int E) { return ((size_t)(MAP_WARPS + 2) * (E + 1) + MAP_WARPS) * sizeof(int32_t); }
 
-template <bool FUSED>
+constexpr int MAP_CACHE_F = 2;   // tiles of up to 2 warp groups keep their ranks in registers
+
+template <bool FUSED, bool CACHE>
 __global__ void __launch_bounds__(MAP_THREADS)
     k_map_rank(const int32_t *__restrict__ idx, int64_t n, int E, int f, int ntiles, int cap,
                const int32_t *__restrict__ tile_counts, int32_t *__restrict__ row_id_map,
@@ -313,17 +315,39 @@ __global__ void __launch_bounds__(MAP_THREADS)
     for (int b = tid; b < MAP_WARPS * stride; b += MAP_THREADS) s_cnt[b] = 0;
     __syncthreads();
 
-    // Per-warp histograms of this tile: reads idx only.
+    // Per-warp histograms of this tile: reads idx only.  With CACHE (f <=
+    // MAP_CACHE_F) each lane also keeps its routes' buckets and their ranks
+    // within the warp's range, so the final pass needs no second walk.
     const int64_t base = warp_base(tile, warp, f);
+    const unsigned lt = lanemask_lt();
     bool bad = false;
-    for (int g = 0; g < f; ++g) {
-        int bk[MAP_CHUNKS];
-        load_buckets(idx, n, E, base + g * MAP_GROUP, lane, bk, bad);
+    int cb[CACHE ? MAP_CACHE_F : 1][MAP_CHUNKS];   // bucket of each route (CACHE)
+    int cr[CACHE ? MAP_CACHE_F : 1][MAP_CHUNKS];   // its rank within the warp's range
+    if (CACHE) {
 #pragma unroll
-        for (int c = 0; c < MAP_CHUNKS; ++c) {
-            const unsigned peers = __match_any_sync(FULL_MASK, bk[c]);
-            if (bk[c] >= 0 && lane == __ffs(peers) - 1) mine[bk[c]] += __popc(peers);
-            __syncwarp();
+        for (int g = 0; g < MAP_CACHE_F; ++g) {
+            if (g >= f) break;
+            load_buckets(idx, n, E, base + g * MAP_GROUP, lane, cb[g], bad);
+#pragma unroll
+            for (int c = 0; c < MAP_CHUNKS; ++c) {
+                const int b = cb[g][c];
+                const unsigned peers = __match_any_sync(FULL_MASK, b);
+                cr[g][c] = (b >= 0) ? mine[b] + __popc(peers & lt) : 0;
+                __syncwarp();
+                if (b >= 0 && lane == __ffs(peers) - 1) mine[b] += __popc(peers);
+                __syncwarp();
+            }
+        }
+    } else {
+        for (int g = 0; g < f; ++g) {
+            int bk[MAP_CHUNKS];
+            load_buckets(idx, n, E, base + g * MAP_GROUP, lane, bk, bad);
+#pragma unroll
+            for (int c = 0; c < MAP_CHUNKS; ++c) {
+                const unsigned peers = __match_any_sync(FULL_MASK, bk[c]);
+                if (bk[c] >= 0 && lane == __ffs(peers) - 1) mine[bk[c]] += __popc(peers);
+                __syncwarp();
+            }
         }
     }
 
@@ -391,26 +415,46 @@ __global__ void __launch_bounds__(MAP_THREADS)
     }
     __syncthreads();
 
-    const unsigned lt = lanemask_lt();
-    for (int g = 0; g < f; ++g) {
-        int bk[MAP_CHUNKS];
-        const int64_t gbase = base + g * MAP_GROUP;
-        load_buckets(idx, n, E, gbase, lane, bk, bad);
+    if (CACHE) {
+        // mine[b] is now the warp's first rank in bucket b within the expert.
 #pragma unroll
-        for (int c = 0; c < MAP_CHUNKS; ++c) {
-            const int b = bk[c];
-            const unsigned peers = __match_any_sync(FULL_MASK, b);
-            int32_t rank = 0;
-            if (b >= 0) rank = mine[b] + __popc(peers & lt);
-            __syncwarp();
-            if (b >= 0 && lane == __ffs(peers) - 1) mine[b] += __popc(peers);
-            __syncwarp();
-            if (b >= 0) {
-                const int64_t i = gbase + c * 32 + lane;
-                const bool keep = b < E && rank < cap;
-                const int32_t row = keep ? s_off[b] + rank : -1;
-                row_id_map[i] = row;
-                if (keep && sorted_to_flat != nullptr) sorted_to_flat[row] = (int32_t)i;
+        for (int g = 0; g < MAP_CACHE_F; ++g) {
+            if (g >= f) break;
+            const int64_t gbase = base + g * MAP_GROUP;
+#pragma unroll
+            for (int c = 0; c < MAP_CHUNKS; ++c) {
+                const int b = cb[g][c];
+                if (b >= 0) {
+                    const int32_t rank = mine[b] + cr[g][c];
+                    const int64_t i = gbase + c * 32 + lane;
+                    const bool keep = b < E && rank < cap;
+                    const int32_t row = keep ? s_off[b] + rank : -1;
+                    row_id_map[i] = row;
+                    if (keep && sorted_to_flat != nullptr) sorted_to_flat[row] = (int32_t)i;
+                }
+            }
+        }
+    } else {
+        for (int g = 0; g < f; ++g) {
+            int bk[MAP_CHUNKS];
+            const int64_t gbase = base + g * MAP_GROUP;
+            load_buckets(idx, n, E, gbase, lane, bk, bad);
+#pragma unroll
+            for (int c = 0; c < MAP_CHUNKS; ++c) {
+                const int b = bk[c];
+                const unsigned peers = __match_any_sync(FULL_MASK, b);
+                int32_t rank = 0;
+                if (b >= 0) rank = mine[b] + __popc(peers & lt);
+                __syncwarp();
+                if (b >= 0 && lane == __ffs(peers) - 1) mine[b] += __popc(peers);
+                __syncwarp();
+                if (b >= 0) {
+                    const int64_t i = gbase + c * 32 + lane;
+                    const bool keep = b < E && rank < cap;
+                    const int32_t row = keep ? s_off[b] + rank : -1;
+                    row_id_map[i] = row;
+                    if (keep && sorted_to_flat != nullptr) sorted_to_flat[row] = (int32_t)i;
+                }
             }
         }
     }
@@ -451,11 +495,12 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *r
     k_map_count<<<grid, MAP_THREADS, (E + 1) * sizeof(int32_t), s>>>(idx, n, E, p.f, (int)p.ntiles,
                                                                      tile_counts, dev_status);
     const size_t smem = rank_smem(E);
+    const bool cache = p.f <= MAP_CACHE_F;
     cudaError_t err = cudaSuccess;
     if (p.fused) {
+        auto fn = cache ? k_map_rank<true, true> : k_map_rank<true, false>;
         if (smem > 48 * 1024)
-            err = cudaFuncSetAttribute(k_map_rank<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+            err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(grid);
@@ -467,20 +512,19 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *r
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            err = cudaLaunchKernelEx(&cfg, k_map_rank<true>, idx, n, E, p.f, (int)p.ntiles, cap,
+            err = cudaLaunchKernelEx(&cfg, fn, idx, n, E, p.f, (int)p.ntiles, cap,
                                      (const int32_t *)tile_counts, row_id_map, sorted_to_flat,
                                      counts, offsets);
         }
     } else {
+        auto fn = cache ? k_map_rank<false, true> : k_map_rank<false, false>;
         if (smem > 48 * 1024)
-            err = cudaFuncSetAttribute(k_map_rank<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err == cudaSuccess) {
             k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)p.ntiles, cap, counts,
                                                   offsets);
-            k_map_rank<false><<<grid, MAP_THREADS, smem, s>>>(idx, n, E, p.f, (int)p.ntiles, cap,
-                                                              tile_counts, row_id_map,
-                                                              sorted_to_flat, counts, offsets);
+            fn<<<grid, MAP_THREADS, smem, s>>>(idx, n, E, p.f, (int)p.ntiles, cap, tile_counts,
+                                               row_id_map, sorted_to_flat, counts, offsets);
         }
     }
     if (err != cudaSuccess) {
