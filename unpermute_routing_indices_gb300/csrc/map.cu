@@ -24,10 +24,13 @@
 //                for every bucket the routes in earlier tiles and the total
 //                (the exclusive scan, done redundantly by every CTA with warp
 //                reductions over the count matrix in L2), seeds per-warp
-//                counters with a scan across its warps, and walks its routes
-//                again: a route's rank within its expert, below the expert's
+//                counters with a scan across its warps, and ranks its routes:
+//                a route's rank within its expert, below the expert's
 //                capacity, gives row = offsets[e] + rank, else the route is
-//                dropped (-1).  CTA 0 writes counts and offsets.
+//                dropped (-1).  For tiles of up to two warp groups the first
+//                pass keeps each route's bucket and in-warp rank in
+//                registers; larger tiles walk their routes again.  CTA 0
+//                writes counts and offsets.
 // When the count matrix is large (every rank CTA would read too much), a single-CTA
 // k_map_scan turns it into bases first and k_map_rank reads them (3 launches).
 // No atomics whose order reaches the result: the map is deterministic.

@@ -15,8 +15,8 @@
 // 256 experts) each lane first sorts its own experts with a fixed sorting
 // network, so a round is the two reductions on the lanes' heads and the
 // winner drops its head; wider rows rescan each lane's experts per round.
-// Lane k keeps pick k.  The softmax runs in fp32: z_k = l_k
-// - l_0, expf (full accuracy), the sum in slot order, IEEE division.
+// Lane k keeps pick k.  The softmax runs in fp32: z_k = l_k - l_0, expf
+// (full accuracy), the sum in slot order, IEEE division.
 // k_topk_softmax_bwd: one warp per token: zero the token's E gradients, then
 // p_k * (g_k - sum_j p_j g_j) at the picked experts.
 #include <cfloat>
