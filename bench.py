@@ -571,6 +571,8 @@ def run_gpu(args):
         ep_bytes = nbytes["unpermute"] + 4 * T * K        # + the slot experts
         logits = dev_t(wl.router_logits(WORKLOAD, T=T, seed=base_seed))
         r_idx, r_probs = torch.empty_like(idx), torch.empty_like(probs)
+        n_groups = wl.ROUTED[WORKLOAD].get("n_groups", 1)
+        topk_groups = wl.ROUTED[WORKLOAD].get("topk_groups", 1)
         g_rp = torch.ones_like(probs)
         g_logits = torch.empty_like(logits)
         quarter = torch.tensor([R * 3 // 4], dtype=torch.int32, device=dev)
@@ -583,7 +585,8 @@ def run_gpu(args):
                                                  offsets=offsets_c, workspace=ws),
                 nbytes["build_map"]),
             "topk_softmax(router)": (
-                lambda: mp.mp_topk_softmax(logits, K, idx=r_idx, probs=r_probs),
+                lambda: mp.mp_topk_softmax(logits, K, n_groups=n_groups, topk_groups=topk_groups,
+                                           idx=r_idx, probs=r_probs),
                 4 * T * E + 8 * T * K),
             "topk_softmax_bwd(router)": (
                 lambda: mp.mp_topk_softmax_bwd(g_rp, r_probs, r_idx, E, g_logits=g_logits),
@@ -606,7 +609,8 @@ def run_gpu(args):
         }
         call("build_map")
         call("permute")
-        mp.mp_topk_softmax(logits, K, idx=r_idx, probs=r_probs)
+        mp.mp_topk_softmax(logits, K, n_groups=n_groups, topk_groups=topk_groups, idx=r_idx,
+                           probs=r_probs)
         for name, (fn, b) in extra_ops.items():
             us = time_op(fn, flush, stream, max(30, min(args.steps, 100)))
             extras[name] = {"us": round(us, 2), "GB/s": round(b / (us * 1e-6) / 1e9, 1),
@@ -844,7 +848,11 @@ def main():
                     help="skip the capacity-map and EP-combine timings")
     ap.add_argument("--tokens", type=int, default=None,
                     help="smaller T of the same workload (profiling captures only)")
+    ap.add_argument("--workload", choices=["skewed", "large", "mid"], default="skewed",
+                    help="routed workload of the step (the metric is quoted on 'skewed')")
     args = ap.parse_args()
+    global WORKLOAD
+    WORKLOAD = args.workload
     if args.warmup < 3:
         args.warmup = 3
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)

@@ -104,15 +104,20 @@ __global__ void __launch_bounds__(RT_THREADS)
 
     if (n_groups > 1) {
         const int per_group = E / n_groups;
+        int grp[PER];              // group of each of this lane's experts (one division each)
+        uint32_t kj[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            grp[j] = (lane + 32 * j) / per_group;
+            kj[j] = (live >> j & 1u) ? order_key(v[j]) : 0u;
+        }
         unsigned group_kept = 0;   // bit g: group g kept (same in every lane)
         uint32_t score_g = 0;      // lane g holds group g's score key
         for (int g = 0; g < n_groups; ++g) {
             uint32_t m = 0;
 #pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                const int e = lane + 32 * j;
-                if ((live >> j & 1u) && e / per_group == g) m = max(m, order_key(v[j]));
-            }
+            for (int j = 0; j < PER; ++j)
+                if (grp[j] == g) m = max(m, kj[j]);
             m = __reduce_max_sync(FULL_MASK, m);
             if (lane == g) score_g = m;
         }
@@ -122,10 +127,8 @@ __global__ void __launch_bounds__(RT_THREADS)
             group_kept |= 1u << gi;
         }
 #pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int e = lane + 32 * j;
-            if ((live >> j & 1u) && !(group_kept >> (e / per_group) & 1u)) live &= ~(1u << j);
-        }
+        for (int j = 0; j < PER; ++j)
+            if ((live >> j & 1u) && !(group_kept >> grp[j] & 1u)) live &= ~(1u << j);
     }
 
     float my_v = 0.0f;
