@@ -33,6 +33,8 @@
 //                writes counts and offsets.
 // When the count matrix is large (every rank CTA would read too much), a single-CTA
 // k_map_scan turns it into bases first and k_map_rank reads them (3 launches).
+// Maps of at most 4,096 routes take one launch: a single k_map_rank CTA whose
+// per-warp histograms are the whole count (no count kernel, no dependency).
 // No atomics whose order reaches the result: the map is deterministic.
 #include <mutex>
 
@@ -299,12 +301,29 @@ inline size_t rank_smem(int E) { return ((size_t)(MAP_WARPS + 2) * (E + 1) + MAP
 
 constexpr int MAP_CACHE_F = 2;   // tiles of up to 2 warp groups keep their ranks in registers
 
-template <bool FUSED, bool CACHE>
+// How k_map_rank gets each bucket's totals and earlier-tile counts:
+//   MAP_MODE_PDL     from the tile counts of k_map_count, reduced in every
+//                    CTA (a programmatic dependent launch of the count kernel);
+//   MAP_MODE_SCANNED from the bases k_map_scan computed;
+//   MAP_MODE_SINGLE  one CTA holds all routes (one tile): its own per-warp
+//                    histograms are the counts, and no other kernel runs.
+constexpr int MAP_MODE_PDL = 0, MAP_MODE_SCANNED = 1, MAP_MODE_SINGLE = 2;
+// Maps of up to this many routes are built by one CTA in one launch.  Measured
+// (build_map alone, event-timed after an L2 flush): one CTA 8.2 us up to 2,048
+// routes and 10.3 us at 4,096, against 10.2-12.3 us for the two kernels; from
+// 8,192 routes on the two kernels are as fast or faster (12.3 vs 12.8 / 18.5).
+#ifndef MP_MAP_SINGLE_MAX
+#define MP_MAP_SINGLE_MAX 4096
+#endif
+constexpr int64_t MAP_SINGLE_MAX = MP_MAP_SINGLE_MAX;
+static_assert(MAP_SINGLE_MAX <= (int64_t)MAP_SUB * MAP_MAX_F, "one tile must hold the routes");
+
+template <int MODE, bool CACHE>
 __global__ void __launch_bounds__(MAP_THREADS)
     k_map_rank(const int32_t *__restrict__ idx, int64_t n, int E, int f, int ntiles, int cap,
                const int32_t *__restrict__ tile_counts, int32_t *__restrict__ row_id_map,
                int32_t *__restrict__ sorted_to_flat, int32_t *__restrict__ counts,
-               int32_t *__restrict__ offsets)
+               int32_t *__restrict__ offsets, int32_t *status)
 {
     extern __shared__ int32_t sm[];
     const int stride = E + 1;
@@ -318,19 +337,34 @@ __global__ void __launch_bounds__(MAP_THREADS)
     for (int b = tid; b < MAP_WARPS * stride; b += MAP_THREADS) s_cnt[b] = 0;
     __syncthreads();
 
-    // Per-warp histograms of this tile: reads idx only.  With CACHE (f <=
-    // MAP_CACHE_F) each lane also keeps its routes' buckets and their ranks
-    // within the warp's range, so the final pass needs no second walk.
+    // Per-warp histograms of this tile: reads idx only.  With CACHE (f <= CF)
+    // each lane also keeps its routes' buckets and their ranks within the
+    // warp's range, so the final pass needs no second walk; all of a warp's
+    // loads are issued before the first is used.
     const int64_t base = warp_base(tile, warp, f);
     const unsigned lt = lanemask_lt();
     bool bad = false;
-    int cb[CACHE ? MAP_CACHE_F : 1][MAP_CHUNKS];   // bucket of each route (CACHE)
-    int cr[CACHE ? MAP_CACHE_F : 1][MAP_CHUNKS];   // its rank within the warp's range
+    constexpr int CF = MODE == MAP_MODE_SINGLE ? MAP_MAX_F : MAP_CACHE_F;
+    int cb[CACHE ? CF : 1][MAP_CHUNKS];   // bucket of each route (CACHE)
+    int cr[CACHE ? CF : 1][MAP_CHUNKS];   // its rank within the warp's range
     if (CACHE) {
 #pragma unroll
-        for (int g = 0; g < MAP_CACHE_F; ++g) {
+        for (int g = 0; g < CF; ++g)
+#pragma unroll
+            for (int c = 0; c < MAP_CHUNKS; ++c) {
+                const int64_t i = base + g * MAP_GROUP + c * 32 + lane;
+                cb[g][c] = (g < f && i < n) ? __ldg(idx + i) : -1;   // raw value first
+            }
+#pragma unroll
+        for (int g = 0; g < CF; ++g) {
             if (g >= f) break;
-            load_buckets(idx, n, E, base + g * MAP_GROUP, lane, cb[g], bad);
+#pragma unroll
+            for (int c = 0; c < MAP_CHUNKS; ++c) {
+                const int64_t i = base + g * MAP_GROUP + c * 32 + lane;
+                const int32_t v = cb[g][c];
+                cb[g][c] = (i < n) ? bucket_of(v, E) : -1;
+                bad |= (i < n) && v != -1 && cb[g][c] == E;
+            }
 #pragma unroll
             for (int c = 0; c < MAP_CHUNKS; ++c) {
                 const int b = cb[g][c];
@@ -354,10 +388,24 @@ __global__ void __launch_bounds__(MAP_THREADS)
         }
     }
 
-    griddep_wait();   // the tile counts of every tile are complete from here on
+    if (MODE != MAP_MODE_SINGLE)
+        griddep_wait();   // the tile counts of every tile are complete from here on
 
     int32_t kept;     // rows of the permuted tensor (routes kept), offsets[E]
-    if (FUSED) {
+    if constexpr (MODE == MAP_MODE_SINGLE) {
+        __syncthreads();   // every warp's histogram is complete
+        for (int b = tid; b <= E; b += MAP_THREADS) {
+            int32_t tot = 0;
+#pragma unroll
+            for (int w = 0; w < MAP_WARPS; ++w) tot += s_cnt[w * stride + b];
+            s_off[b] = (b < E) ? min(tot, cap) : 0;   // rows the expert keeps
+            s_base[b] = 0;
+            if (b < E) counts[b] = min(tot, cap);
+        }
+        if (__syncthreads_or(bad) && tid == 0) or_status(status, MP_STATUS_BAD_EXPERT);
+        kept = cta_exclusive_scan(s_off, stride, s_warp);  // s_off: first row of each expert
+        for (int b = tid; b <= E; b += MAP_THREADS) offsets[b] = s_off[b];
+    } else if constexpr (MODE == MAP_MODE_PDL) {
         // Warp w sums buckets w, w+8, ...: its lanes read the bucket's row of
         // the expert-major count matrix (consecutive tiles, coalesced) and
         // two warp reductions give the bucket's total and the routes of
@@ -421,7 +469,7 @@ __global__ void __launch_bounds__(MAP_THREADS)
     if (CACHE) {
         // mine[b] is now the warp's first rank in bucket b within the expert.
 #pragma unroll
-        for (int g = 0; g < MAP_CACHE_F; ++g) {
+        for (int g = 0; g < CF; ++g) {
             if (g >= f) break;
             const int64_t gbase = base + g * MAP_GROUP;
 #pragma unroll
@@ -494,14 +542,32 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *r
         k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, 0, cap, counts, offsets);
         return check_launch();
     }
+    const size_t smem = rank_smem(E);
+    cudaError_t err = cudaSuccess;
+    if (n <= MAP_SINGLE_MAX) {
+        // One CTA, one launch: for small maps the two-kernel form is all
+        // latency (launches, the dependency, L2 round trips).
+        int f = 1;
+        while ((int64_t)MAP_SUB * f < n) f *= 2;
+        auto fn = k_map_rank<MAP_MODE_SINGLE, true>;   // every group cached (f <= MAP_MAX_F)
+        if (smem > 48 * 1024)
+            err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err == cudaSuccess)
+            fn<<<1, MAP_THREADS, smem, s>>>(idx, n, E, f, 1, cap, nullptr, row_id_map,
+                                            sorted_to_flat, counts, offsets, dev_status);
+        if (err != cudaSuccess) {
+            cudaGetLastError();
+            set_last_cuda_error(err);
+            return MP_ERR_CUDA;
+        }
+        return check_launch();
+    }
     const unsigned grid = (unsigned)p.ntiles;
     k_map_count<<<grid, MAP_THREADS, (E + 1) * sizeof(int32_t), s>>>(idx, n, E, p.f, (int)p.ntiles,
                                                                      tile_counts, dev_status);
-    const size_t smem = rank_smem(E);
     const bool cache = p.f <= MAP_CACHE_F;
-    cudaError_t err = cudaSuccess;
     if (p.fused) {
-        auto fn = cache ? k_map_rank<true, true> : k_map_rank<true, false>;
+        auto fn = cache ? k_map_rank<MAP_MODE_PDL, true> : k_map_rank<MAP_MODE_PDL, false>;
         if (smem > 48 * 1024)
             err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err == cudaSuccess) {
@@ -517,17 +583,18 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *r
             cfg.numAttrs = 1;
             err = cudaLaunchKernelEx(&cfg, fn, idx, n, E, p.f, (int)p.ntiles, cap,
                                      (const int32_t *)tile_counts, row_id_map, sorted_to_flat,
-                                     counts, offsets);
+                                     counts, offsets, (int32_t *)nullptr);
         }
     } else {
-        auto fn = cache ? k_map_rank<false, true> : k_map_rank<false, false>;
+        auto fn = cache ? k_map_rank<MAP_MODE_SCANNED, true> : k_map_rank<MAP_MODE_SCANNED, false>;
         if (smem > 48 * 1024)
             err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err == cudaSuccess) {
             k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)p.ntiles, cap, counts,
                                                   offsets);
             fn<<<grid, MAP_THREADS, smem, s>>>(idx, n, E, p.f, (int)p.ntiles, cap, tile_counts,
-                                               row_id_map, sorted_to_flat, counts, offsets);
+                                               row_id_map, sorted_to_flat, counts, offsets,
+                                               nullptr);
         }
     }
     if (err != cudaSuccess) {
