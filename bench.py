@@ -50,9 +50,9 @@ FALLBACK_HBM_GBS = 6800.0
 # one ncu capture, keyed by op; valid only while the kernel source that was
 # profiled is unchanged (sha256 prefix of the .cu file).
 NCU_TRAFFIC = {
-    # one-pass capture of the full bench workload (dram__bytes_read.sum 1,209,081,600
-    # + dram__bytes_write.sum 1,014,064,896); profiles/traffic_skewed_T16384_row_kernels.md
-    "unpermute_bwd": {"bytes": 2223146496, "src": "61e7a019030b1a1a"},
+    # one-pass capture of the full bench workload (dram__bytes_read.sum 1,209,255,936
+    # + dram__bytes_write.sum 1,013,933,056); profiles/traffic_skewed_T16384_row_kernels.md
+    "unpermute_bwd": {"bytes": 2223188992, "src": "d6f2ac6e0b741e3f"},
 }
 
 
@@ -95,9 +95,12 @@ def measured_peaks():
 
 
 def src_hash(name):
-    path = os.path.join(ROOT, "unpermute_routing_indices_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel's source file and the device helpers it includes."""
+    h = hashlib.sha256()
+    for part in (name, "common.cuh"):
+        with open(os.path.join(ROOT, "unpermute_routing_indices_gb300", "csrc", part), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 class ClockSampler:
@@ -421,18 +424,28 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     nev = len(ops) + 1
 
-    def timed_steps(n, record):
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n)]
+    def timed_steps(n, per_op, flushed=True):
+        """n steps.  per_op=False: events at the ends of each step only, so each
+        kernel's launch overlaps the tail of the one before it (programmatic
+        dependent launch); per_op=True: an event after every op as well, which
+        serialises the ops and times each one alone."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev if per_op else 2)]
+               for _ in range(n)]
         for i in range(n):
-            flush(i)                                    # L2 flush between steps
+            if flushed:
+                flush(i)                                # L2 flush between steps
             evs[i][0].record(stream)
             for j, op in enumerate(ops):
                 call(op)
-                evs[i][j + 1].record(stream)
+                if per_op:
+                    evs[i][j + 1].record(stream)
+            if not per_op:
+                evs[i][1].record(stream)
         return evs
 
     for _ in range(args.warmup):
         timed_steps(1, False)
+        timed_steps(1, True)
     torch.cuda.synchronize()
     routed = int(offsets[-1].item())
     nbytes = routed_bytes(T, H, K, E, routed)
@@ -442,32 +455,32 @@ def run_gpu(args):
         torch.cuda.synchronize()
         barrier()
         t0 = time.time()
-        evs = timed_steps(args.steps, True)
+        evs = timed_steps(args.steps, False)
         torch.cuda.synchronize()
         t1 = time.time()
         barrier()
+        # the same steps again with an event after every op: per-kernel times
+        op_evs = timed_steps(args.steps, True)
+        torch.cuda.synchronize()
+        barrier()
     clocks = clk.summary(t0, t1)
 
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
     samples = {op: [] for op in ops}
-    step_ms = []
-    for e in evs:
-        step_ms.append(e[0].elapsed_time(e[-1]))
+    op_step_ms = []
+    for e in op_evs:
+        op_step_ms.append(e[0].elapsed_time(e[-1]))
         for j, op in enumerate(ops):
             samples[op].append(e[j].elapsed_time(e[j + 1]))
-    ms = sum(step_ms) / len(step_ms)
+    ms_serialised = sum(op_step_ms) / len(op_step_ms)
     per_op = {op: statistics.mean(v) for op, v in samples.items()}
     med_op = {op: statistics.median(v) for op, v in samples.items()}
-    ms = max_over_ranks(ms, world, dev)
 
     # warm numbers: the same steps back to back, no L2 flush in between
     warm_n = max(3, min(args.steps, 100))
     torch.cuda.synchronize()
-    wev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(warm_n)]
-    for i in range(warm_n):
-        wev[i][0].record(stream)
-        for j, op in enumerate(ops):
-            call(op)
-            wev[i][j + 1].record(stream)
+    wev = timed_steps(warm_n, True, flushed=False)
     torch.cuda.synchronize()
     warm_op = {op: statistics.median(wev[i][j].elapsed_time(wev[i][j + 1]) for i in range(warm_n))
                for j, op in enumerate(ops)}
@@ -632,6 +645,8 @@ def run_gpu(args):
         "pct_of_nominal_peak": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_peak": round(100 * gbs / world / peak, 2),
         "tokens_per_s": round(world * T / (ms * 1e-3), 1),
+        "ms_per_step_serialised": round(ms_serialised, 4),
+        "ops_timing": "each op alone: the same steps again with an event after every op",
         "ops": {op: {"us": round(per_op[op] * 1e3, 2), "us_median": round(med_op[op] * 1e3, 2),
                      "us_warm_median": round(warm_op[op] * 1e3, 2), "bytes": nbytes[op],
                      "GB/s": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9, 1),

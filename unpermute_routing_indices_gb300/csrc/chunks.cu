@@ -322,6 +322,8 @@ __global__ void __launch_bounds__(CH_THREADS, MP_CH_MIN_BLOCKS)
                float *__restrict__ out_probs, int32_t *__restrict__ row_map,
                int64_t *__restrict__ group_off, int32_t *status)
 {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ int64_t sm[];
     SortPadMeta m;
     m.s_start = sm;                      // [C]
@@ -378,6 +380,8 @@ __global__ void __launch_bounds__(CH_THREADS, MP_CH_MIN_BLOCKS)
                  const int32_t *__restrict__ map, int64_t out_rows, int64_t N, int nvec,
                  V *__restrict__ out, float *__restrict__ out_probs, int32_t *status)
 {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t s_map[CH_ROWS];
     const int tid = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.x * CH_ROWS;
@@ -440,20 +444,22 @@ mp_status_t remap(const void *in, const float *in_probs, const int32_t *map, int
     const unsigned blocks = (unsigned)((out_rows + CH_ROWS - 1) / CH_ROWS);
     if (chunk_vec_ok(H, {in, out})) {
         if (scatter)
-            k_rows_remap<uint4, true><<<blocks, CH_THREADS, 0, s>>>(
-                (const uint4 *)in, in_probs, map, out_rows, N, H / 8, (uint4 *)out, out_probs, status);
+            (void)launch_pdl(k_rows_remap<uint4, true>, blocks, CH_THREADS, 0, s,
+                             (const uint4 *)in, in_probs, map, out_rows, N, H / 8, (uint4 *)out,
+                             out_probs, status);
         else
-            k_rows_remap<uint4, false><<<blocks, CH_THREADS, 0, s>>>(
-                (const uint4 *)in, in_probs, map, out_rows, N, H / 8, (uint4 *)out, out_probs, status);
+            (void)launch_pdl(k_rows_remap<uint4, false>, blocks, CH_THREADS, 0, s,
+                             (const uint4 *)in, in_probs, map, out_rows, N, H / 8, (uint4 *)out,
+                             out_probs, status);
     } else {
         if (scatter)
-            k_rows_remap<uint16_t, true><<<blocks, CH_THREADS, 0, s>>>(
-                (const uint16_t *)in, in_probs, map, out_rows, N, H, (uint16_t *)out, out_probs,
-                status);
+            (void)launch_pdl(k_rows_remap<uint16_t, true>, blocks, CH_THREADS, 0, s,
+                             (const uint16_t *)in, in_probs, map, out_rows, N, H, (uint16_t *)out,
+                             out_probs, status);
         else
-            k_rows_remap<uint16_t, false><<<blocks, CH_THREADS, 0, s>>>(
-                (const uint16_t *)in, in_probs, map, out_rows, N, H, (uint16_t *)out, out_probs,
-                status);
+            (void)launch_pdl(k_rows_remap<uint16_t, false>, blocks, CH_THREADS, 0, s,
+                             (const uint16_t *)in, in_probs, map, out_rows, N, H, (uint16_t *)out,
+                             out_probs, status);
     }
     return check_launch();
 }
@@ -492,9 +498,9 @@ mp_status_t sort_pad_impl(const void *x, const float *probs, const int32_t *spli
     // flight; larger ones keep one, for more resident CTAs.
     const bool two = out_rows <= MP_SP_RP2_MAX_ROWS;
 #define MP_SORT_PAD_LAUNCH(VT, WM, RPV, NV)                                                  \
-    k_sort_pad<VT, WM, RPV><<<blocks, CH_THREADS, smem, s>>>(                               \
-        (const VT *)x, probs, split_sizes, chunk_order, padded_sizes, C, G, align, N, out_rows, \
-        NV, (VT *)out, out_probs, row_map, group_off, dev_status)
+    (void)launch_pdl(k_sort_pad<VT, WM, RPV>, blocks, CH_THREADS, smem, s, (const VT *)x,   \
+                     probs, split_sizes, chunk_order, padded_sizes, C, G, align, N, out_rows,  \
+                     NV, (VT *)out, out_probs, row_map, group_off, dev_status)
     if (chunk_vec_ok(w, {x, out})) {
         if (warp_meta && two) MP_SORT_PAD_LAUNCH(uint4, true, 2, w / 8);
         else if (warp_meta) MP_SORT_PAD_LAUNCH(uint4, true, 1, w / 8);

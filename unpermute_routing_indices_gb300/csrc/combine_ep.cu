@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                    const int32_t *__restrict__ map, const int32_t *__restrict__ idx, int64_t T,
                    int K, int nvec, int tpt_log2, int per_rank, V *__restrict__ out)
 {
+    pdl_trigger();
+    pdl_wait();
     constexpr int L = Lanes<V>::N;
     const int tpt = 1 << tpt_log2;
     const int lane = threadIdx.x & (tpt - 1);
@@ -296,7 +298,7 @@ void launch_ep(const void *rows, const float *probs, const int32_t *map, const i
     if (l > lmax) l = lmax;
     const int64_t per_block = EP_THREADS >> l;
     const unsigned blocks = (unsigned)((T + per_block - 1) / per_block);
-    k_unpermute_ep<V, PROBS, BF16P, FP64><<<blocks, EP_THREADS, 0, s>>>(
+    (void)launch_pdl(k_unpermute_ep<V, PROBS, BF16P, FP64>, blocks, EP_THREADS, 0, s,
         (const V *)rows, probs, map, idx, T, K, nvec, l, per_rank, (V *)out);
 }
 

@@ -29,6 +29,39 @@ inline mp_status_t check_launch()
 
 inline cudaStream_t as_stream(mp_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel is launched with programmatic
+// stream serialisation and starts with pdl_trigger() then pdl_wait(): its
+// launch and CTA scheduling overlap the tail of the kernel before it in the
+// stream, while pdl_wait() holds every thread until that kernel has finished
+// and its memory is visible, before anything is read.  After a copy, a
+// memset or a kernel launched the usual way the attribute has no effect.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline int ceil_log2(int v)

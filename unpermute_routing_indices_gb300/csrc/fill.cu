@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(FILL_THREADS)
     k_zero_rows_from(V *__restrict__ buf, int64_t rows, int64_t units_per_row,
                      const int32_t *__restrict__ first_row)
 {
+    pdl_trigger();
+    pdl_wait();
     int64_t s = __ldg(first_row);
     s = s < 0 ? 0 : (s > rows ? rows : s);
     const int64_t end = rows * units_per_row;
@@ -50,8 +52,8 @@ void launch_fill(void *buf, int64_t rows, int64_t units_per_row, const int32_t *
     const int64_t total = rows * units_per_row;
     int64_t blocks = (total + FILL_THREADS - 1) / FILL_THREADS;
     blocks = blocks < 1 ? 1 : (blocks > FILL_MAX_BLOCKS ? FILL_MAX_BLOCKS : blocks);
-    k_zero_rows_from<V><<<(unsigned)blocks, FILL_THREADS, 0, s>>>(static_cast<V *>(buf), rows,
-                                                                  units_per_row, first_row);
+    (void)launch_pdl(k_zero_rows_from<V>, (unsigned)blocks, FILL_THREADS, 0, s,
+                     static_cast<V *>(buf), rows, units_per_row, first_row);
 }
 
 }  // namespace

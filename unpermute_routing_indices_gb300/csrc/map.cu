@@ -87,12 +87,6 @@ inline MapPlan map_plan(int64_t n, int E)
     return MapPlan{f, ntiles, (int64_t)(E + 1) * ntiles <= MAP_FUSED_MAX_COUNTS};
 }
 
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 __device__ __forceinline__ int bucket_of(int32_t v, int E) { return (v >= 0 && v < E) ? v : E; }
 
 __device__ __forceinline__ unsigned lanemask_lt()
@@ -131,7 +125,10 @@ __global__ void __launch_bounds__(MAP_THREADS)
     k_map_count(const int32_t *__restrict__ idx, int64_t n, int E, int f, int ntiles,
                 int32_t *__restrict__ tile_counts, int32_t *status)
 {
-    griddep_launch_dependents();   // the rank kernel's idx-only pass may start now
+    // Wait before the trigger: the rank kernel reads idx before its own wait,
+    // so it may start only once whatever wrote idx has finished.
+    pdl_wait();
+    pdl_trigger();   // the rank kernel's idx-only pass may start now
     extern __shared__ int32_t s_hist[];  // [E+1]
     for (int b = threadIdx.x; b <= E; b += MAP_THREADS) s_hist[b] = 0;
     __syncthreads();
@@ -173,6 +170,8 @@ __global__ void __launch_bounds__(SCAN_THREADS)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t M = (int64_t)(E + 1) * ntiles;
     int32_t carry = 0;
+    pdl_wait();      // the count kernel has finished, and so has idx's writer
+    pdl_trigger();   // the rank kernel reads idx before its wait: only after this one's
 
     for (int64_t base = 0; base < M; base += SCAN_PASS) {
 #pragma unroll
@@ -325,6 +324,11 @@ __global__ void __launch_bounds__(MAP_THREADS)
                int32_t *__restrict__ sorted_to_flat, int32_t *__restrict__ counts,
                int32_t *__restrict__ offsets, int32_t *status)
 {
+    pdl_trigger();
+    // A single launch reads nothing from another map kernel: it waits here.
+    // The two-kernel forms read idx first and wait below for the counts; the
+    // kernel before them waited for idx's writer before it let them start.
+    if (MODE == MAP_MODE_SINGLE) pdl_wait();
     extern __shared__ int32_t sm[];
     const int stride = E + 1;
     int32_t *s_cnt = sm;                              // [MAP_WARPS][E+1] per-warp counters
@@ -389,7 +393,7 @@ __global__ void __launch_bounds__(MAP_THREADS)
     }
 
     if (MODE != MAP_MODE_SINGLE)
-        griddep_wait();   // the tile counts of every tile are complete from here on
+        pdl_wait();   // the tile counts of every tile are complete from here on
 
     int32_t kept;     // rows of the permuted tensor (routes kept), offsets[E]
     if constexpr (MODE == MAP_MODE_SINGLE) {
@@ -539,7 +543,8 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *r
 {
     const MapPlan p = map_plan(n, E);
     if (p.ntiles == 0) {
-        k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, 0, cap, counts, offsets);
+        (void)launch_pdl(k_map_scan, 1, SCAN_THREADS, 0, s, tile_counts, E, 0, cap, counts,
+                         offsets);
         return check_launch();
     }
     const size_t smem = rank_smem(E);
@@ -553,8 +558,8 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *r
         if (smem > 48 * 1024)
             err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err == cudaSuccess)
-            fn<<<1, MAP_THREADS, smem, s>>>(idx, n, E, f, 1, cap, nullptr, row_id_map,
-                                            sorted_to_flat, counts, offsets, dev_status);
+            (void)launch_pdl(fn, 1, MAP_THREADS, smem, s, idx, n, E, f, 1, cap, nullptr,
+                             row_id_map, sorted_to_flat, counts, offsets, dev_status);
         if (err != cudaSuccess) {
             cudaGetLastError();
             set_last_cuda_error(err);
@@ -563,38 +568,27 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *r
         return check_launch();
     }
     const unsigned grid = (unsigned)p.ntiles;
-    k_map_count<<<grid, MAP_THREADS, (E + 1) * sizeof(int32_t), s>>>(idx, n, E, p.f, (int)p.ntiles,
-                                                                     tile_counts, dev_status);
+    (void)launch_pdl(k_map_count, grid, MAP_THREADS, (E + 1) * sizeof(int32_t), s, idx, n, E,
+                     p.f, (int)p.ntiles, tile_counts, dev_status);
     const bool cache = p.f <= MAP_CACHE_F;
     if (p.fused) {
         auto fn = cache ? k_map_rank<MAP_MODE_PDL, true> : k_map_rank<MAP_MODE_PDL, false>;
         if (smem > 48 * 1024)
             err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err == cudaSuccess) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(grid);
-            cfg.blockDim = dim3(MAP_THREADS);
-            cfg.dynamicSmemBytes = smem;
-            cfg.stream = s;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            err = cudaLaunchKernelEx(&cfg, fn, idx, n, E, p.f, (int)p.ntiles, cap,
-                                     (const int32_t *)tile_counts, row_id_map, sorted_to_flat,
-                                     counts, offsets, (int32_t *)nullptr);
-        }
+        if (err == cudaSuccess)
+            err = launch_pdl(fn, grid, MAP_THREADS, smem, s, idx, n, E, p.f, (int)p.ntiles, cap,
+                             (const int32_t *)tile_counts, row_id_map, sorted_to_flat, counts,
+                             offsets, (int32_t *)nullptr);
     } else {
         auto fn = cache ? k_map_rank<MAP_MODE_SCANNED, true> : k_map_rank<MAP_MODE_SCANNED, false>;
         if (smem > 48 * 1024)
             err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err == cudaSuccess) {
-            k_map_scan<<<1, SCAN_THREADS, 0, s>>>(tile_counts, E, (int)p.ntiles, cap, counts,
-                                                  offsets);
-            fn<<<grid, MAP_THREADS, smem, s>>>(idx, n, E, p.f, (int)p.ntiles, cap, tile_counts,
-                                               row_id_map, sorted_to_flat, counts, offsets,
-                                               nullptr);
+            (void)launch_pdl(k_map_scan, 1, SCAN_THREADS, 0, s, tile_counts, E, (int)p.ntiles,
+                             cap, counts, offsets);
+            (void)launch_pdl(fn, grid, MAP_THREADS, smem, s, idx, n, E, p.f, (int)p.ntiles, cap,
+                             (const int32_t *)tile_counts, row_id_map, sorted_to_flat, counts,
+                             offsets, (int32_t *)nullptr);
         }
     }
     if (err != cudaSuccess) {

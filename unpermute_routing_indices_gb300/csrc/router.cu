@@ -86,6 +86,8 @@ __global__ void __launch_bounds__(RT_THREADS)
     k_topk_softmax(const float *__restrict__ logits, int64_t T, int E, int K, int n_groups,
                    int topk_groups, int32_t *__restrict__ idx, float *__restrict__ probs)
 {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * RT_WARPS + (threadIdx.x >> 5);
     if (t >= T) return;  // whole warps exit together
@@ -197,6 +199,8 @@ __global__ void __launch_bounds__(RT_THREADS)
                        const int32_t *__restrict__ idx, int64_t T, int E, int K,
                        float *__restrict__ g_logits)
 {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * RT_WARPS + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -232,17 +236,17 @@ extern "C" mp_status_t mp_topk_softmax(const float *logits, int64_t T, int32_t E
     cudaStream_t s = as_stream(stream);
     const int per = (E + 31) / 32;   // logits per lane
     if (per <= 4)
-        k_topk_softmax<4><<<blocks, RT_THREADS, 0, s>>>(logits, T, E, K, n_groups, topk_groups,
-                                                        idx, probs);
+        (void)launch_pdl(k_topk_softmax<4>, blocks, RT_THREADS, 0, s, logits, T, E, K,
+                         n_groups, topk_groups, idx, probs);
     else if (per <= 8)
-        k_topk_softmax<8><<<blocks, RT_THREADS, 0, s>>>(logits, T, E, K, n_groups, topk_groups,
-                                                        idx, probs);
+        (void)launch_pdl(k_topk_softmax<8>, blocks, RT_THREADS, 0, s, logits, T, E, K,
+                         n_groups, topk_groups, idx, probs);
     else if (per <= 16)
-        k_topk_softmax<16><<<blocks, RT_THREADS, 0, s>>>(logits, T, E, K, n_groups, topk_groups,
-                                                         idx, probs);
+        (void)launch_pdl(k_topk_softmax<16>, blocks, RT_THREADS, 0, s, logits, T, E, K,
+                         n_groups, topk_groups, idx, probs);
     else
-        k_topk_softmax<32><<<blocks, RT_THREADS, 0, s>>>(logits, T, E, K, n_groups, topk_groups,
-                                                         idx, probs);
+        (void)launch_pdl(k_topk_softmax<32>, blocks, RT_THREADS, 0, s, logits, T, E, K,
+                         n_groups, topk_groups, idx, probs);
     return check_launch();
 }
 
@@ -256,7 +260,7 @@ extern "C" mp_status_t mp_topk_softmax_bwd(const float *g_probs, const float *pr
     if (g_probs == nullptr || probs == nullptr || idx == nullptr || g_logits == nullptr)
         return MP_ERR_INVALID_ARG;
     const unsigned blocks = (unsigned)((T + RT_WARPS - 1) / RT_WARPS);
-    k_topk_softmax_bwd<<<blocks, RT_THREADS, 0, as_stream(stream)>>>(g_probs, probs, idx, T, E, K,
-                                                                     g_logits);
+    (void)launch_pdl(k_topk_softmax_bwd, blocks, RT_THREADS, 0, as_stream(stream), g_probs, probs,
+                     idx, T, E, K, g_logits);
     return check_launch();
 }

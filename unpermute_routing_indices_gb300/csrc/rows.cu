@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(ROW_THREADS)
               const int32_t *__restrict__ map, int64_t T, int K, int nvec, int tpt_log2,
               V *__restrict__ out, float *__restrict__ out_probs)
 {
+    pdl_trigger();
+    pdl_wait();
     const int tpt = 1 << tpt_log2;
     const int lane = threadIdx.x & (tpt - 1);
     const int64_t t = (int64_t)blockIdx.x * (ROW_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
@@ -101,6 +103,8 @@ __global__ void __launch_bounds__(ROW_THREADS)
                 V *__restrict__ out, const float *__restrict__ g_out_probs,
                 float *__restrict__ g_probs)
 {
+    pdl_trigger();
+    pdl_wait();
     constexpr int L = Lanes<V>::N;
     const int tpt = 1 << tpt_log2;
     const int lane = threadIdx.x & (tpt - 1);
@@ -167,6 +171,8 @@ __global__ void __launch_bounds__(ROW_THREADS)
                     int K, int nvec, int tpt_log2, V *__restrict__ g_rows,
                     float *__restrict__ g_probs)
 {
+    pdl_trigger();
+    pdl_wait();
     constexpr int L = Lanes<V>::N;
     __shared__ float s_red[ROW_THREADS / 32][KB];
     const int tpt = 1 << tpt_log2;
@@ -272,10 +278,10 @@ void launch_permute(const void *x, const float *probs, const int32_t *map, int64
 {
     const RowGrid g = row_grid(T, nvec, VPT);
     if (probs != nullptr && out_probs != nullptr)
-        k_permute<V, VPT, true><<<g.blocks, ROW_THREADS, 0, s>>>(
+        (void)launch_pdl(k_permute<V, VPT, true>, g.blocks, ROW_THREADS, 0, s,
             (const V *)x, probs, map, T, K, nvec, g.tpt_log2, (V *)out, out_probs);
     else
-        k_permute<V, VPT, false><<<g.blocks, ROW_THREADS, 0, s>>>(
+        (void)launch_pdl(k_permute<V, VPT, false>, g.blocks, ROW_THREADS, 0, s,
             (const V *)x, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr);
 }
 
@@ -286,14 +292,14 @@ void launch_unpermute(const void *rows, const float *probs, const int32_t *map, 
 {
     const RowGrid g = row_grid(T, nvec, VPT);
     if (probs != nullptr)
-        k_unpermute<V, VPT, true, false><<<g.blocks, ROW_THREADS, 0, s>>>(
+        (void)launch_pdl(k_unpermute<V, VPT, true, false>, g.blocks, ROW_THREADS, 0, s,
             (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr, nullptr);
     else if (g_probs != nullptr)
-        k_unpermute<V, VPT, false, true><<<g.blocks, ROW_THREADS, 0, s>>>(
+        (void)launch_pdl(k_unpermute<V, VPT, false, true>, g.blocks, ROW_THREADS, 0, s,
             (const V *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, g_out_probs,
             g_probs);
     else
-        k_unpermute<V, VPT, false, false><<<g.blocks, ROW_THREADS, 0, s>>>(
+        (void)launch_pdl(k_unpermute<V, VPT, false, false>, g.blocks, ROW_THREADS, 0, s,
             (const V *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr, nullptr);
 }
 
@@ -303,7 +309,7 @@ void launch_unpermute_bwd(const void *gy, const void *rows, const float *probs,
                           float *g_probs, cudaStream_t s)
 {
     const RowGrid g = row_grid(T, nvec, VPT);
-    k_unpermute_bwd<V, VPT><<<g.blocks, ROW_THREADS, 0, s>>>(
+    (void)launch_pdl(k_unpermute_bwd<V, VPT>, g.blocks, ROW_THREADS, 0, s,
         (const V *)gy, (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)g_rows, g_probs);
 }
 
