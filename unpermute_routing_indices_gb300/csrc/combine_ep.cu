@@ -19,7 +19,9 @@
 // changes no bit.  GB300 runs FP64 at a small fraction of its FP32 rate, so
 // where the fp64 sum of the partials is provably exact (their magnitudes span
 // few enough binades) the same exact sum is formed in fp32 -- by plain adds,
-// or as a TwoSum pair -- and only wider spans take the fp64 additions.
+// or as a TwoSum pair -- and only wider spans take the fp64 additions.  Those
+// forms run the FMA chains and sums on packed fp32 pairs (f32x2: two
+// elements per instruction, each rounded as the scalar operation would be).
 #include <climits>
 
 #include "common.cuh"
@@ -85,6 +87,51 @@ __device__ __forceinline__ uint4 pack_bits(const uint16_t (&b)[8])
 
 __device__ __forceinline__ uint16_t pack_bits(const uint16_t (&b)[1]) { return b[0]; }
 
+// Packed pairs of fp32 (the f32x2 arithmetic of sm_100 and later): one
+// instruction rounds each half exactly as the scalar operation would.
+__device__ __forceinline__ uint64_t f2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t r, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// The two bf16 of a 32-bit word as a pair of fp32 (exact).
+__device__ __forceinline__ uint64_t bf16x2_wide(uint32_t w) { return f2(bf16_lo(w), bf16_hi(w)); }
+
 // Compare-exchange on (key, row, prob) triples, smaller key first.
 __device__ __forceinline__ void cx(int32_t &ka, int32_t &ra, float &pa, int32_t &kb, int32_t &rb,
                                    float &pb)
@@ -139,11 +186,39 @@ __device__ __forceinline__ void walk_ranks(const V (&r)[EP_KMAX], const float (&
     }
 }
 
+// walk_ranks on packed pairs: the four element pairs of a 16-byte vector.
+template <bool PROBS, typename Add>
+__device__ __forceinline__ void walk_ranks2(const uint4 (&r)[EP_KMAX], const float (&p)[EP_KMAX],
+                                            unsigned valid, unsigned last, Add add)
+{
+    uint64_t part[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) part[i] = 0;
+#pragma unroll
+    for (int j = 0; j < EP_KMAX; ++j) {
+        if (!(valid >> j & 1u)) continue;
+        const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+        const uint64_t pp = f2(p[j], p[j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            part[i] = PROBS ? fma2(pp, bf16x2_wide(w[i]), part[i])
+                            : add2(part[i], bf16x2_wide(w[i]));
+        if (last >> j & 1u) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                add(i, part[i]);
+                part[i] = 0;
+            }
+        }
+    }
+}
+
 // CTAs per SM each variant is compiled for (registers are capped to fit).
 // Measured on the skewed T=16384, ep=8 combine: occupancy outweighs the
 // registers it spills (fp32 215 -> 187 us at 7 CTAs, bf16 partials 243 ->
-// 199 us, fp64 with bf16 / fp32 partials best at 6 / 5).
-constexpr int ep_min_blocks(bool fp64, bool bf16p) { return fp64 ? (bf16p ? 6 : 5) : 7; }
+// 199 us); the fp64 forms, which also prefetch their next pass into L2, are
+// best at 5 (bf16 partials, 242 us) and 4 (fp32 partials, 300 us).
+constexpr int ep_min_blocks(bool fp64, bool bf16p) { return fp64 ? (bf16p ? 5 : 4) : 7; }
 
 template <typename V, bool PROBS, bool BF16P, bool FP64>
 __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
@@ -191,6 +266,16 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
             r[i] = ((valid >> i & 1u) && c < nvec) ? ld_stream(rows + (int64_t)rk[i] * nvec + c)
                                                    : zero_vec<V>();
         if constexpr (FP64) {
+            // the fp64 forms compute long enough per pass to hide an L2 fill
+            // of the next pass's rows behind it
+            const int cn = c + tpt;
+#pragma unroll
+            for (int i = 0; i < EP_KMAX; ++i)
+                if ((valid >> i & 1u) && cn < nvec)
+                    asm volatile("prefetch.global.L2 [%0];"
+                                 ::"l"(rows + (int64_t)rk[i] * nvec + cn));
+        }
+        if constexpr (FP64) {
             // Exact cross-rank sum, then one rounding to bf16.  The partials
             // are bf16 (BF16P) or fp32 values, each a multiple of its own
             // quantum, and the smallest nonzero magnitude m has the smallest
@@ -205,7 +290,10 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
             //    order, the definition itself.
             // In the first two cases every running sum has at most 45
             // significant bits, so the fp64 additions are exact as well and
-            // all three give the same bits.
+            // all three give the same bits.  On 16-byte vectors the partials
+            // are formed and added as packed fp32 pairs; with bf16 partials
+            // the bound uses 8 * the largest |partial| (at most 8 ranks) in
+            // place of a, from integer max / min of the bf16 magnitudes.
             constexpr float TIER2 = BF16P ? 0x1p36f : 0x1p20f;
             uint16_t bits[L];
             unsigned pair = 0, dbl = 0;   // elements that take the pair / fp64 sum
@@ -216,7 +304,64 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                 sb[e] = 0.0f;
                 sm[e] = __int_as_float(0x7f800000);
             }
-            if (BF16P) {
+            if constexpr (BF16P && L == 8) {
+                // Largest and smallest |partial| of each element as bf16 bit
+                // patterns (ordered like magnitudes; +inf bits start the
+                // minimum, NaN patterns exceed every finite one).  With at most
+                // 8 partials, sum |p| <= 8 max, so max <= 2^12 min implies the
+                // plain-add bound and max <= 2^33 min the pair bound.
+                uint64_t sa2[4];
+                uint32_t mx[4], mn[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    sa2[i] = 0;
+                    mx[i] = 0;
+                    mn[i] = 0x7f807f80u;
+                }
+                walk_ranks2<PROBS>(r, pk, valid, last, [&](int i, uint64_t p) {
+                    float lo, hi;
+                    f2_split(p, lo, hi);
+                    const uint32_t w = pack_bf16x2(lo, hi);
+                    sa2[i] = add2(sa2[i], bf16x2_wide(w));
+                    const uint32_t a = w & 0x7fff7fffu;
+                    mx[i] = max_u16x2(mx[i], a);
+                    mn[i] = min_u16x2(mn[i], a);
+                });
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float a0, a1;
+                    f2_split(sa2[i], a0, a1);
+                    const uint32_t wb = pack_bf16x2(a0, a1);
+                    bits[2 * i] = static_cast<uint16_t>(wb & 0xffffu);
+                    bits[2 * i + 1] = static_cast<uint16_t>(wb >> 16);
+                    const float hx[2] = {bf16_lo(mx[i]), bf16_hi(mx[i])};
+                    const float hn[2] = {bf16_lo(mn[i]), bf16_hi(mn[i])};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const bool fin = hx[h] <= 0x1p120f;
+                        if (!(fin && hx[h] <= __fmul_rn(hn[h], 0x1p12f)))
+                            (fin && hx[h] <= __fmul_rn(hn[h], 0x1p33f) ? pair : dbl) |=
+                                1u << (2 * i + h);
+                    }
+                }
+                if (pair) {
+#pragma unroll
+                    for (int e = 0; e < L; ++e) {
+                        sa[e] = 0.0f;
+                        sb[e] = 0.0f;
+                    }
+                    walk_ranks<PROBS, true, L>(r, pk, valid, last, [&](int e, float p) {
+                        const float s = __fadd_rn(sa[e], p);
+                        const float bb = __fsub_rn(s, sa[e]);
+                        sb[e] = __fadd_rn(sb[e], __fadd_rn(__fsub_rn(sa[e], __fsub_rn(s, bb)),
+                                                           __fsub_rn(p, bb)));
+                        sa[e] = s;
+                    });
+#pragma unroll
+                    for (int e = 0; e < L; ++e)
+                        if (pair >> e & 1u) bits[e] = bf16_from_pair(sa[e], sb[e]);
+                }
+            } else if (BF16P) {
                 walk_ranks<PROBS, true, L>(r, pk, valid, last, [&](int e, float p) {
                     sa[e] = __fadd_rn(sa[e], p);
                     sb[e] = __fadd_rn(sb[e], fabsf(p));
@@ -247,6 +392,50 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                     for (int e = 0; e < L; ++e)
                         if (pair >> e & 1u) bits[e] = bf16_from_pair(sa[e], sb[e]);
                 }
+            } else if constexpr (L == 8) {
+                uint64_t sa2[4], sl2[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sa2[i] = sl2[i] = 0;
+                walk_ranks2<PROBS>(r, pk, valid, last, [&](int i, uint64_t p) {
+                    const uint64_t s2 = add2(sa2[i], p);
+                    const uint64_t bb = sub2(s2, sa2[i]);
+                    sl2[i] = add2(sl2[i], add2(sub2(sa2[i], sub2(s2, bb)), sub2(p, bb)));
+                    sa2[i] = s2;
+                    float lo, hi;
+                    f2_split(p, lo, hi);
+                    sb[2 * i] = __fadd_rn(sb[2 * i], fabsf(lo));
+                    sb[2 * i + 1] = __fadd_rn(sb[2 * i + 1], fabsf(hi));
+                    sm[2 * i] = fminf(sm[2 * i], fabsf(lo));
+                    sm[2 * i + 1] = fminf(sm[2 * i + 1], fabsf(hi));
+                });
+                // hi = fl(sa + sl) rounds to the same bf16 as the exact sum
+                // unless it lies exactly halfway between two bf16 values (the
+                // midpoints are fp32 values, so a first rounding cannot cross
+                // one); only then is the pair's error needed.
+                unsigned tie = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float h0, h1;
+                    f2_split(add2(sa2[i], sl2[i]), h0, h1);
+                    const uint32_t wb = pack_bf16x2(h0, h1);
+                    bits[2 * i] = static_cast<uint16_t>(wb & 0xffffu);
+                    bits[2 * i + 1] = static_cast<uint16_t>(wb >> 16);
+                    tie |= ((__float_as_uint(h0) & 0xffffu) == 0x8000u ? 1u : 0u) << (2 * i);
+                    tie |= ((__float_as_uint(h1) & 0xffffu) == 0x8000u ? 1u : 0u) << (2 * i + 1);
+                }
+                if (tie) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float a0, a1, l0, l1;
+                        f2_split(sa2[i], a0, a1);
+                        f2_split(sl2[i], l0, l1);
+                        if (tie >> (2 * i) & 1u) bits[2 * i] = bf16_from_pair(a0, l0);
+                        if (tie >> (2 * i + 1) & 1u) bits[2 * i + 1] = bf16_from_pair(a1, l1);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < L; ++e)
+                    if (!(sb[e] <= 0x1p120f && sb[e] <= __fmul_rn(sm[e], TIER2))) dbl |= 1u << e;
             } else {
                 float sl[L];
 #pragma unroll

@@ -31,11 +31,13 @@ inline cudaStream_t as_stream(mp_stream_t s) { return reinterpret_cast<cudaStrea
 
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel is launched with programmatic
-// stream serialisation and starts with pdl_trigger() then pdl_wait(): its
-// launch and CTA scheduling overlap the tail of the kernel before it in the
-// stream, while pdl_wait() holds every thread until that kernel has finished
-// and its memory is visible, before anything is read.  After a copy, a
-// memset or a kernel launched the usual way the attribute has no effect.
+// stream serialisation and calls pdl_trigger() and pdl_wait() before it
+// touches global memory: its launch and CTA scheduling overlap the tail of
+// the kernel before it in the stream, while pdl_wait() holds every thread
+// until that kernel has finished and its memory is visible.  (The map's count
+// and scan kernels wait before they trigger; the map's rank kernel reads idx
+// before its wait.)  After a copy, a memset or a kernel launched the usual way
+// the attribute has no effect.
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
