@@ -231,3 +231,38 @@ def test_sort_pad_explicit_padded_sizes(slack):
     np.testing.assert_array_equal(h(goff), o_goff)
     assert mp.status_bits(int(h(st)[0])) == {k for k, v in fl.items() if v}
     assert (slack == "smaller") == bool(fl["bad_padded"])
+
+
+def test_sort_pad_past_int32_element_offsets():
+    """540,000 rows of H = 4,096 (2.2e9 elements, past 2^31) through sort+pad
+    and unpad+restore: row offsets must be formed in 64 bits.  The rows are
+    counter-based, so any row can be rebuilt on the host; the layout (row_map,
+    group_off) is checked in full against the oracle, whose layout does not
+    depend on H, and the copied rows on a sample that includes the last ones."""
+    N, H = 540000, 4096
+    sizes, order = wl.chunk_layout(N)
+    G, align = wl.CHUNKS["experts"], wl.CHUNKS["align"]
+    out_rows = wl.padded_rows_bound(N, G, align)
+    assert out_rows * H > 2**31
+    x = wl.hashed_rows_torch(N, H, 41, DEV)
+    out, _, row_map, goff = mp.mp_sort_chunks_pad(x, d(sizes), d(order), G, align, out_rows)
+    _, _, o_map, o_goff, _ = oracle.sort_chunks_pad(np.zeros((N, 8), np.uint16), None, sizes,
+                                                    order, G, align, out_rows)
+    np.testing.assert_array_equal(h(row_map), o_map)
+    np.testing.assert_array_equal(h(goff), o_goff)
+    rng = np.random.default_rng(8)
+    dsample = np.unique(np.concatenate([rng.choice(out_rows, 96, replace=False),
+                                        np.arange(out_rows - 32, out_rows),
+                                        np.nonzero(o_map >= N - 16)[0]]))
+    got = h(out.index_select(0, torch.from_numpy(dsample.astype(np.int64)).to(DEV)))
+    src = o_map[dsample]
+    want = np.zeros((dsample.size, H), np.uint16)
+    want[src >= 0] = wl.hashed_rows(src[src >= 0], H, 41)
+    np.testing.assert_array_equal(got, want)
+    del x
+    y, _ = mp.mp_unpad_restore(out, row_map, N)
+    ysample = np.unique(np.concatenate([rng.choice(N, 96, replace=False),
+                                        np.arange(N - 32, N)]))
+    np.testing.assert_array_equal(
+        h(y.index_select(0, torch.from_numpy(ysample.astype(np.int64)).to(DEV))),
+        wl.hashed_rows(ysample, H, 41))

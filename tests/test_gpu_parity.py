@@ -303,6 +303,59 @@ def test_full_size_sampled(name):
     np.testing.assert_array_equal(h(g_x)[sample], o_gx)
 
 
+def test_rows_past_int32_element_offsets():
+    """T = 66,000 tokens, K = 8, H = 4,096: the permuted tensors hold 2.16e9
+    elements, past 2^31, so row offsets must be formed in 64 bits.  All the
+    row tensors are counter-based (rebuilt on the host for any row); sampled
+    tokens include those holding the last rows of the permuted tensor."""
+    T, H, K = 66000, 4096, 8
+    idx_h, probs_h, E = wl.routing("skewed", T=T, seed=5)
+    R = T * K
+    assert R * H > 2**31
+    rim = mp.mp_build_map(d(idx_h), E)[0]
+    o_rim, *_ = oracle.build_map(idx_h, E)
+    np.testing.assert_array_equal(h(rim), o_rim)
+    rng = np.random.default_rng(12)
+    high = np.unique(np.nonzero(o_rim >= (2**31) // H)[0])           # rows past 2^31 elements
+    sample = np.unique(np.concatenate([rng.choice(T, 64, replace=False),
+                                       rng.choice(high, 64, replace=False), [0, T - 1]]))
+    assert (o_rim[sample] >= (2**31) // H).any()
+    rs = torch.from_numpy(o_rim[sample].ravel().astype(np.int64)).to(DEV)
+    ts = torch.from_numpy(sample.astype(np.int64)).to(DEV)
+    probs = d(probs_h)
+
+    x = wl.hashed_rows_torch(T, H, 31, DEV)
+    out, _ = mp.mp_permute(x, rim)
+    got = h(out.index_select(0, rs)).reshape(len(sample), K, H)
+    np.testing.assert_array_equal(got, np.repeat(wl.hashed_rows(sample, H, 31)[:, None, :], K,
+                                                 axis=1))
+    del out, x
+
+    rows = wl.hashed_rows_torch(R, H, 32, DEV)
+    rim_s = o_rim[sample]
+    rows_s = wl.hashed_rows(rim_s.ravel(), H, 32)
+    local = np.arange(rim_s.size, dtype=np.int32).reshape(rim_s.shape)
+    y = h(mp.mp_unpermute(rows, rim, probs).index_select(0, ts))
+    np.testing.assert_array_equal(y, oracle.unpermute(rows_s, probs_h[sample], local,
+                                                      len(sample), H))
+    y_ep = h(mp.mp_unpermute_ep(rows, rim, d(idx_h), E, 8, probs).index_select(0, ts))
+    np.testing.assert_array_equal(y_ep, oracle.unpermute_ep(rows_s, probs_h[sample], local,
+                                                            idx_h[sample], len(sample), H, E, 8))
+    g_x, _ = mp.mp_permute_bwd(rows, rim)
+    o_gx, _ = oracle.permute_bwd(rows_s, None, local, len(sample), H)
+    np.testing.assert_array_equal(h(g_x.index_select(0, ts)), o_gx)
+    del g_x
+
+    gy = wl.hashed_rows_torch(T, H, 33, DEV)
+    gy_s = wl.hashed_rows(sample, H, 33)
+    g_rows, g_probs = mp.mp_unpermute_bwd(gy, rim, rows, probs)
+    o_grows, o_gp = oracle.unpermute_bwd(gy_s, rows_s, probs_h[sample], local)
+    np.testing.assert_array_equal(h(g_rows.index_select(0, rs)), o_grows)
+    gp = h(g_probs)[sample].astype(np.float64)
+    bound = gprobs_bound(f32(rows_s).reshape(len(sample), K, H), f32(gy_s)[:, None, :], o_gp)
+    assert np.all(np.abs(gp - o_gp) <= bound)
+
+
 # --------------------------------------------------------------------------
 # expert capacity (token dropping)
 # --------------------------------------------------------------------------
