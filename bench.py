@@ -10,7 +10,10 @@ with the identity as the expert in between (the unpermute reads the permuted
 rows; the permute backward reads the unpermute backward's row gradients).
 
 `value` is algorithmic bytes per step / device time per step, in GB/s
-(1 GB = 1e9 B), inputs resident in HBM, L2 flushed between steps.  Byte
+(1 GB = 1e9 B), inputs resident in HBM, L2 flushed between steps.  Each step
+is timed with events at its two ends only, so consecutive kernels overlap as
+programmatic dependent launches; the per-op times come from the same steps
+run again with an event after every op.  Byte
 accounting: every input row read once, every output row written once, maps
 and probabilities once.  `e2e` is the same metric through the same calls with
 the inputs copied from pinned host memory and the results copied back inside
@@ -48,7 +51,7 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture, keyed by op; valid only while the kernel source that was
-# profiled is unchanged (sha256 prefix of the .cu file).
+# profiled is unchanged (sha256 prefix of the .cu file and common.cuh).
 NCU_TRAFFIC = {
     # one-pass capture of the full bench workload (dram__bytes_read.sum 1,209,255,936
     # + dram__bytes_write.sum 1,013,933,056); profiles/traffic_skewed_T16384_row_kernels.md
