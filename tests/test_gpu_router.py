@@ -40,6 +40,12 @@ def _check_probs(got, want):
     (3001, 40, 5, 1, 1, "ties"),        # integer logits: many ties, odd sizes
     (2000, 96, 3, 6, 2, "ties"),
     (777, 1024, 32, 32, 8, "normal"),   # limits
+    # groups of whole 32-expert columns, s columns each
+    (3000, 256, 8, 4, 2, "normal"),     # s = 2
+    (2500, 192, 6, 2, 1, "ties"),       # s = 3, 6 of 8 slots per lane in use
+    (1200, 512, 8, 4, 3, "normal"),     # s = 4, 16 slots per lane
+    (900, 128, 4, 2, 1, "ties"),        # s = 2, 4 slots per lane
+    (700, 1024, 16, 4, 3, "skew"),      # s = 8, 32 slots per lane (the rescan path)
     (500, 8, 8, 1, 1, "normal"),        # K = E
 ])
 def test_topk_softmax_parity(T, E, K, G, TG, kind):

@@ -11,7 +11,10 @@
 // through an order-preserving 32-bit key (-0 folded into +0), so a warp's
 // arg-max on (logit desc, expert asc) is two single-instruction warp
 // reductions: the largest key, then the smallest expert holding it.  Group
-// scores are warp max-reductions of the same keys.  For the K picks (up to
+// scores are warp max-reductions of the same keys; when every group is a
+// whole number of 32-expert columns (each lane's slot j then lies in group
+// j / s for every lane), a group's score is one reduction of the column
+// maxima, and no lane computes a group index.  For the K picks (up to
 // 256 experts) each lane first sorts its own experts with a fixed sorting
 // network, so a round is the two reductions on the lanes' heads and the
 // winner drops its head; wider rows rescan each lane's experts per round.
@@ -104,7 +107,45 @@ __global__ void __launch_bounds__(RT_THREADS)
     for (int j = 0; j < PER; ++j)
         if (lane + 32 * j < E) live |= 1u << j;
 
-    if (n_groups > 1) {
+    if (n_groups > 1 && (E / n_groups) % 32 == 0) {
+        // Groups of whole 32-expert columns: slot j of every lane is in group
+        // j / s (s = columns per group), so a group's score is a warp max
+        // over its s slots; slots are walked with a counter, not a division.
+        const int s = (E / n_groups) / 32;
+        const int ncols = E / 32;
+        unsigned group_kept = 0;
+        uint32_t score_g = 0;      // lane g holds group g's score key
+        uint32_t colmax = 0;
+        int cnt = 0, gcur = 0;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            if (j < ncols) {
+                colmax = max(colmax, (live >> j & 1u) ? order_key(v[j]) : 0u);
+                if (++cnt == s) {
+                    const uint32_t m = __reduce_max_sync(FULL_MASK, colmax);
+                    if (lane == gcur) score_g = m;
+                    colmax = 0;
+                    cnt = 0;
+                    ++gcur;
+                }
+            }
+        }
+        for (int j = 0; j < topk_groups; ++j) {
+            uint32_t sk = (lane < n_groups && !(group_kept >> lane & 1u)) ? score_g : 0u;
+            const uint32_t gi = warp_argmax_key(sk, (uint32_t)lane);
+            group_kept |= 1u << gi;
+        }
+        cnt = 0;
+        gcur = 0;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            if (j < ncols && !(group_kept >> gcur & 1u)) live &= ~(1u << j);
+            if (++cnt == s) {
+                cnt = 0;
+                ++gcur;
+            }
+        }
+    } else if (n_groups > 1) {
         const int per_group = E / n_groups;
         int grp[PER];              // group of each of this lane's experts (one division each)
         uint32_t kj[PER];
@@ -146,10 +187,11 @@ __global__ void __launch_bounds__(RT_THREADS)
             ex[j] = (uint32_t)(lane + 32 * j);
         }
         sort_desc<PER>(key, ex);
+        uint32_t my_key = 0u;
         for (int k = 0; k < K; ++k) {
             uint32_t bk = key[0];
             const uint32_t pick = warp_argmax_key(bk, ex[0]);
-            if ((int)(pick & 31u) == lane) {
+            if (ex[0] == pick) {   // the winning lane (a live head's expert is unique)
 #pragma unroll
                 for (int j = 0; j + 1 < PER; ++j) {
                     key[j] = key[j + 1];
@@ -158,10 +200,11 @@ __global__ void __launch_bounds__(RT_THREADS)
                 key[PER - 1] = 0u;
             }
             if (lane == k) {
-                my_v = key_value(bk);
+                my_key = bk;
                 my_i = (int)pick;
             }
         }
+        my_v = key_value(my_key);
     } else {
         // Wide rows (more than 256 experts): each round rescans the lane's
         // live experts (a sort network that large would not stay in registers).
