@@ -17,7 +17,9 @@
 // maxima, and no lane computes a group index.  For the K picks (up to
 // 256 experts) each lane first sorts its own experts with a fixed sorting
 // network, so a round is the two reductions on the lanes' heads and the
-// winner drops its head; wider rows rescan each lane's experts per round.
+// winner drops its head; when at most half of the columns hold a live expert
+// (groups not kept, or few experts), the live ones are gathered and only
+// they are sorted.  Wider rows rescan each lane's experts per round.
 // Lane k keeps pick k.  The softmax runs in fp32: z_k = l_k - l_0, expf
 // (full accuracy), the sum in slot order, IEEE division.
 // k_topk_softmax_bwd: one warp per token: zero the token's E gradients, then
@@ -82,6 +84,33 @@ __device__ __forceinline__ void sort_desc(uint32_t (&k)[N], uint32_t (&ix)[N])
                 for (int i = 0; i < q; ++i)
                     if (i + j + q < N && (i + j) / (2 * p) == (i + j + q) / (2 * p))
                         cx_desc(k[i + j], ix[i + j], k[i + j + q], ix[i + j + q]);
+}
+
+// Sorts a lane's N (key, expert) slots, then runs the K pick rounds: each
+// round is two warp reductions on the lanes' heads, and the lane whose head
+// is the picked expert (a live head's expert is unique) drops it.  Lane k
+// keeps pick k.
+template <int N>
+__device__ __forceinline__ void pick_rounds(uint32_t (&key)[N], uint32_t (&ex)[N], int K,
+                                            int lane, uint32_t &my_key, int &my_i)
+{
+    sort_desc<N>(key, ex);
+    for (int k = 0; k < K; ++k) {
+        uint32_t bk = key[0];
+        const uint32_t pick = warp_argmax_key(bk, ex[0]);
+        if (ex[0] == pick) {
+#pragma unroll
+            for (int j = 0; j + 1 < N; ++j) {
+                key[j] = key[j + 1];
+                ex[j] = ex[j + 1];
+            }
+            key[N - 1] = 0u;
+        }
+        if (lane == k) {
+            my_key = bk;
+            my_i = (int)pick;
+        }
+    }
 }
 
 template <int PER>
@@ -179,30 +208,42 @@ __global__ void __launch_bounds__(RT_THREADS)
     if constexpr (PER <= 8) {
         // Each lane sorts its live experts once (dead ones get key 0, last);
         // a round's winner then drops its head, so every lane's head stays
-        // its best remaining expert.
+        // its best remaining expert (pick_rounds).
         uint32_t key[PER], ex[PER];
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             key[j] = (live >> j & 1u) ? order_key(v[j]) : 0u;
             ex[j] = (uint32_t)(lane + 32 * j);
         }
-        sort_desc<PER>(key, ex);
         uint32_t my_key = 0u;
-        for (int k = 0; k < K; ++k) {
-            uint32_t bk = key[0];
-            const uint32_t pick = warp_argmax_key(bk, ex[0]);
-            if (ex[0] == pick) {   // the winning lane (a live head's expert is unique)
+        // Columns with a live expert in any lane (the same in every lane).
+        const unsigned cols = __reduce_or_sync(FULL_MASK, live);
+        if (PER >= 4 && __popc(cols) <= PER / 2) {
+            // At most half the columns live (unkept groups, or E <= 16*PER):
+            // gather them into half as many slots, in any order, and sort
+            // those.
+            constexpr int HALF = PER >= 4 ? PER / 2 : 1;
+            uint32_t kc[HALF], xc[HALF];
 #pragma unroll
-                for (int j = 0; j + 1 < PER; ++j) {
-                    key[j] = key[j + 1];
-                    ex[j] = ex[j + 1];
+            for (int i = 0; i < HALF; ++i) {
+                kc[i] = 0u;
+                xc[i] = 0xffffffffu;
+            }
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                if (cols >> j & 1u) {
+#pragma unroll
+                    for (int i = HALF - 1; i > 0; --i) {
+                        kc[i] = kc[i - 1];
+                        xc[i] = xc[i - 1];
+                    }
+                    kc[0] = key[j];
+                    xc[0] = ex[j];
                 }
-                key[PER - 1] = 0u;
             }
-            if (lane == k) {
-                my_key = bk;
-                my_i = (int)pick;
-            }
+            pick_rounds<HALF>(kc, xc, K, lane, my_key, my_i);
+        } else {
+            pick_rounds<PER>(key, ex, K, lane, my_key, my_i);
         }
         my_v = key_value(my_key);
     } else {
