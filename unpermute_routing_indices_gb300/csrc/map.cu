@@ -35,6 +35,9 @@
 // k_map_scan turns it into bases first and k_map_rank reads them (3 launches).
 // Maps of at most 4,096 routes take one launch: a single k_map_rank CTA whose
 // per-warp histograms are the whole count (no count kernel, no dependency).
+// Maps of up to 32,768 routes take one launch of one thread-block cluster of
+// k_map_rank CTAs (a 2,048-route tile each) that exchange their tile
+// histograms through distributed shared memory.
 // No atomics whose order reaches the result: the map is deterministic.
 #include <mutex>
 
@@ -94,6 +97,26 @@ __device__ __forceinline__ unsigned lanemask_lt()
     unsigned m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
+}
+
+// Thread-block cluster helpers (one cluster holds every CTA of a map).
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// The int32 at `p` in the shared memory of the cluster's CTA `rank`.
+__device__ __forceinline__ int32_t ld_cluster(const int32_t *p, unsigned rank)
+{
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    unsigned ra;
+    int32_t v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+    return v;
 }
 
 // Buckets of this lane's 8 routes of one warp group; -1 past the end.
@@ -296,7 +319,7 @@ __device__ int32_t cta_exclusive_scan(int32_t *a, int n, int32_t *s_warp)
     return total;
 }
 
-inline size_t rank_smem(int E) { return ((size_t)(MAP_WARPS + 2) * (E + 1) + MAP_WARPS) * sizeof(int32_t); }
+inline size_t rank_smem(int E) { return ((size_t)(MAP_WARPS + 3) * (E + 1) + MAP_WARPS) * sizeof(int32_t); }
 
 constexpr int MAP_CACHE_F = 2;   // tiles of up to 2 warp groups keep their ranks in registers
 
@@ -305,8 +328,14 @@ constexpr int MAP_CACHE_F = 2;   // tiles of up to 2 warp groups keep their rank
 //                    CTA (a programmatic dependent launch of the count kernel);
 //   MAP_MODE_SCANNED from the bases k_map_scan computed;
 //   MAP_MODE_SINGLE  one CTA holds all routes (one tile): its own per-warp
-//                    histograms are the counts, and no other kernel runs.
-constexpr int MAP_MODE_PDL = 0, MAP_MODE_SCANNED = 1, MAP_MODE_SINGLE = 2;
+//                    histograms are the counts, and no other kernel runs;
+//   MAP_MODE_CLUSTER one thread-block cluster holds all routes, a tile per
+//                    CTA: each CTA publishes its tile's histogram in shared
+//                    memory, and every CTA reads all of them across the
+//                    cluster (distributed shared memory) after a cluster
+//                    barrier.  One launch, no count kernel, no global round
+//                    trip.
+constexpr int MAP_MODE_PDL = 0, MAP_MODE_SCANNED = 1, MAP_MODE_SINGLE = 2, MAP_MODE_CLUSTER = 3;
 // Maps of up to this many routes are built by one CTA in one launch.  Measured
 // (build_map alone, event-timed after an L2 flush): one CTA 8.2 us up to 2,048
 // routes and 10.3 us at 4,096, against 10.2-12.3 us for the two kernels; from
@@ -328,13 +357,15 @@ __global__ void __launch_bounds__(MAP_THREADS)
     // A single launch reads nothing from another map kernel: it waits here.
     // The two-kernel forms read idx first and wait below for the counts; the
     // kernel before them waited for idx's writer before it let them start.
-    if (MODE == MAP_MODE_SINGLE) pdl_wait();
+    constexpr bool ONE_LAUNCH = MODE == MAP_MODE_SINGLE || MODE == MAP_MODE_CLUSTER;
+    if (ONE_LAUNCH) pdl_wait();
     extern __shared__ int32_t sm[];
     const int stride = E + 1;
     int32_t *s_cnt = sm;                              // [MAP_WARPS][E+1] per-warp counters
     int32_t *s_base = s_cnt + MAP_WARPS * stride;     // [E+1] bucket routes in earlier tiles
     int32_t *s_warp = s_base + stride;                // [MAP_WARPS]
     int32_t *s_off = s_warp + MAP_WARPS;              // [E+1] first row of each expert
+    int32_t *s_tot = s_off + stride;                  // [E+1] this tile's histogram (cluster)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tile = blockIdx.x;
     int32_t *mine = s_cnt + warp * stride;
@@ -348,7 +379,7 @@ __global__ void __launch_bounds__(MAP_THREADS)
     const int64_t base = warp_base(tile, warp, f);
     const unsigned lt = lanemask_lt();
     bool bad = false;
-    constexpr int CF = MODE == MAP_MODE_SINGLE ? MAP_MAX_F : MAP_CACHE_F;
+    constexpr int CF = ONE_LAUNCH ? MAP_MAX_F : MAP_CACHE_F;
     int cb[CACHE ? CF : 1][MAP_CHUNKS];   // bucket of each route (CACHE)
     int cr[CACHE ? CF : 1][MAP_CHUNKS];   // its rank within the warp's range
     if (CACHE) {
@@ -392,7 +423,7 @@ __global__ void __launch_bounds__(MAP_THREADS)
         }
     }
 
-    if (MODE != MAP_MODE_SINGLE)
+    if (!ONE_LAUNCH)
         pdl_wait();   // the tile counts of every tile are complete from here on
 
     int32_t kept;     // rows of the permuted tensor (routes kept), offsets[E]
@@ -409,6 +440,34 @@ __global__ void __launch_bounds__(MAP_THREADS)
         if (__syncthreads_or(bad) && tid == 0) or_status(status, MP_STATUS_BAD_EXPERT);
         kept = cta_exclusive_scan(s_off, stride, s_warp);  // s_off: first row of each expert
         for (int b = tid; b <= E; b += MAP_THREADS) offsets[b] = s_off[b];
+    } else if constexpr (MODE == MAP_MODE_CLUSTER) {
+        // The CTA's cluster rank is its tile (the grid is one cluster).
+        __syncthreads();   // every warp's histogram is complete
+        for (int b = tid; b <= E; b += MAP_THREADS) {
+            int32_t tot = 0;
+#pragma unroll
+            for (int w = 0; w < MAP_WARPS; ++w) tot += s_cnt[w * stride + b];
+            s_tot[b] = tot;
+        }
+        if (__syncthreads_or(bad) && tid == 0) or_status(status, MP_STATUS_BAD_EXPERT);
+        cluster_arrive();
+        cluster_wait();    // every tile's histogram is visible across the cluster
+        for (int b = tid; b <= E; b += MAP_THREADS) {
+            int32_t tot = 0, pre = 0;
+            for (int c = 0; c < ntiles; ++c) {
+                const int32_t v = ld_cluster(s_tot + b, (unsigned)c);
+                tot += v;
+                pre += (c < tile) ? v : 0;
+            }
+            s_off[b] = (b < E) ? min(tot, cap) : 0;   // rows the expert keeps
+            s_base[b] = pre;
+            if (tile == 0 && b < E) counts[b] = min(tot, cap);
+        }
+        cluster_arrive();  // done reading the others' shared memory (waited on at exit)
+        __syncthreads();
+        kept = cta_exclusive_scan(s_off, stride, s_warp);  // s_off: first row of each expert
+        if (tile == 0)
+            for (int b = tid; b <= E; b += MAP_THREADS) offsets[b] = s_off[b];
     } else if constexpr (MODE == MAP_MODE_PDL) {
         // Warp w sums buckets w, w+8, ...: its lanes read the bucket's row of
         // the expert-major count matrix (consecutive tiles, coalesced) and
@@ -522,6 +581,8 @@ __global__ void __launch_bounds__(MAP_THREADS)
         const int64_t hi = min(n, lo + per);
         for (int64_t i = lo + tid; i < hi; i += MAP_THREADS) sorted_to_flat[i] = -1;
     }
+    // A CTA's shared memory must outlive every other CTA's reads of it.
+    if constexpr (MODE == MAP_MODE_CLUSTER) cluster_wait();
 }
 
 inline bool map_sizes_ok(int64_t T, int32_t K, int32_t E)
@@ -534,6 +595,85 @@ inline size_t map_workspace_bytes(int64_t n, int E)
     const MapPlan p = map_plan(n, E);
     const size_t bytes = (size_t)(E + 1) * (size_t)p.ntiles * sizeof(int32_t);
     return bytes == 0 ? 256 : (bytes + 255) / 256 * 256;
+}
+
+// The cluster form: tiles of 2048 * f routes, f from MP_MAP_CLUSTER_F0 up to
+// MAP_MAX_F, one CTA each, at most MP_MAP_CLUSTER_MAX CTAs in the cluster.
+#ifndef MP_MAP_CLUSTER_MAX
+#define MP_MAP_CLUSTER_MAX 16
+#endif
+#ifndef MP_MAP_CLUSTER_F0
+#define MP_MAP_CLUSTER_F0 1
+#endif
+#ifndef MP_MAP_CLUSTER_ROUTES
+#define MP_MAP_CLUSTER_ROUTES (MP_MAP_CLUSTER_MAX * 2048)
+#endif
+constexpr int MAP_CLUSTER_MAX = MP_MAP_CLUSTER_MAX;
+constexpr int64_t MAP_CLUSTER_ROUTES = MP_MAP_CLUSTER_ROUTES;
+static_assert(MAP_CLUSTER_ROUTES <= (int64_t)MAP_CLUSTER_MAX * MAP_SUB * MAP_MAX_F,
+              "the cluster must hold the routes");
+
+// Launches the cluster form when the GPU can hold such a cluster; returns
+// false (nothing launched) otherwise.  Whether it fits is asked once per
+// (cluster size, shared memory) and remembered.
+bool launch_map_cluster(const int32_t *idx, int64_t n, int E, int cap, int32_t *row_id_map,
+                        int32_t *sorted_to_flat, int32_t *counts, int32_t *offsets,
+                        int32_t *dev_status, cudaStream_t s, size_t smem, cudaError_t &err)
+{
+    int f = MP_MAP_CLUSTER_F0;
+    int64_t nc = (n + (int64_t)MAP_SUB * f - 1) / ((int64_t)MAP_SUB * f);
+    while (nc > MAP_CLUSTER_MAX && f < MAP_MAX_F) {
+        f *= 2;
+        nc = (n + (int64_t)MAP_SUB * f - 1) / ((int64_t)MAP_SUB * f);
+    }
+    if (nc > MAP_CLUSTER_MAX) return false;
+    auto fn = k_map_rank<MAP_MODE_CLUSTER, true>;
+    static std::mutex mu;
+    static bool attrs_set = false;
+    static int fits[MAP_CLUSTER_MAX + 1][2] = {};   // per size: smem tried, 1 + (fits ? 1 : 0)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nc);
+    cfg.blockDim = dim3(MAP_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nc;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attrs_set) {
+            err = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (err == cudaSuccess)
+                err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)rank_smem(MP_MAX_EXPERTS));
+            if (err != cudaSuccess) {
+                cudaGetLastError();
+                err = cudaSuccess;
+                return false;
+            }
+            attrs_set = true;
+        }
+        int *slot = fits[nc];
+        if (slot[0] != (int)smem || slot[1] == 0) {
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                clusters = 0;
+            }
+            slot[0] = (int)smem;
+            slot[1] = 1 + (clusters >= 1 ? 1 : 0);
+        }
+        if (slot[1] != 2) return false;
+    }
+    err = cudaLaunchKernelEx(&cfg, fn, idx, n, E, f, (int)nc, cap, (const int32_t *)nullptr,
+                             row_id_map, sorted_to_flat, counts, offsets, dev_status);
+    return true;
 }
 
 // Enqueues the map kernels; tile_counts holds (E+1) * plan.ntiles words.
@@ -560,6 +700,16 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *r
         if (err == cudaSuccess)
             (void)launch_pdl(fn, 1, MAP_THREADS, smem, s, idx, n, E, f, 1, cap, nullptr,
                              row_id_map, sorted_to_flat, counts, offsets, dev_status);
+        if (err != cudaSuccess) {
+            cudaGetLastError();
+            set_last_cuda_error(err);
+            return MP_ERR_CUDA;
+        }
+        return check_launch();
+    }
+    if (n <= MAP_CLUSTER_ROUTES &&
+        launch_map_cluster(idx, n, E, cap, row_id_map, sorted_to_flat, counts, offsets,
+                           dev_status, s, smem, err)) {
         if (err != cudaSuccess) {
             cudaGetLastError();
             set_last_cuda_error(err);
