@@ -97,6 +97,21 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def map_launches(routes: int, E: int) -> int:
+    """Kernels mp_build_map launches for this many routes: one CTA (up to
+    4,096 routes) or one thread-block cluster (up to 32,768) in one launch;
+    beyond, the count and rank kernels, with a scan kernel in between when
+    the count matrix ((E+1) x tiles of 2048*f routes, f doubling up to 8 until
+    there are at most 64 tiles) exceeds 32,768 entries."""
+    if routes <= 32768:
+        return 1
+    f = 1
+    while f < 8 and -(-routes // (2048 * f)) > 64:
+        f *= 2
+    tiles = -(-routes // (2048 * f))
+    return 2 if (E + 1) * tiles <= 32768 else 3
+
+
 def src_hash(name):
     """Hash of a kernel's source file and the device helpers it includes."""
     h = hashlib.sha256()
@@ -406,10 +421,9 @@ def run_gpu(args):
     flush = L2Flush(dev)
 
     ops = ["build_map", "permute", "unpermute", "unpermute_bwd", "permute_bwd"]
-    # kernels each op launches (the map: count + rank; a third, the single-CTA
-    # scan, only when the count matrix exceeds what the rank CTAs read)
-    launches = {"build_map": 2, "permute": 1, "unpermute": 1, "unpermute_bwd": 1,
-                "permute_bwd": 1}
+    # kernels each op launches
+    launches = {"build_map": map_launches(R, E), "permute": 1, "unpermute": 1,
+                "unpermute_bwd": 1, "permute_bwd": 1}
 
     def call(op):
         if op == "build_map":

@@ -52,3 +52,15 @@ def test_two_ranks_share_the_slowest_time_and_sum_their_bytes():
 def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks(4.5, 1) == 4.5
     assert bench.rank_seed(1003, 0) == 1003
+
+
+def test_map_launch_count():
+    """The kernels mp_build_map launches, as the bench counts them: one CTA or
+    one cluster up to 32,768 routes; count + rank beyond; + scan when the
+    count matrix passes 32,768 entries."""
+    assert bench.map_launches(512, 128) == 1
+    assert bench.map_launches(32768, 128) == 1
+    assert bench.map_launches(32769, 128) == 2
+    assert bench.map_launches(131072, 128) == 2       # the skewed step: 64 tiles
+    assert bench.map_launches(262144, 256) == 2       # large: 64 tiles of 4,096
+    assert bench.map_launches(131072, 1024) == 3      # 1,025 x 64 counts
