@@ -614,8 +614,8 @@ static_assert(MAP_CLUSTER_ROUTES <= (int64_t)MAP_CLUSTER_MAX * MAP_SUB * MAP_MAX
               "the cluster must hold the routes");
 
 // Launches the cluster form when the GPU can hold such a cluster; returns
-// false (nothing launched) otherwise.  Whether it fits is asked once per
-// (cluster size, shared memory) and remembered.
+// false (nothing launched) otherwise, or when the launch is refused.  Whether
+// it fits is asked once per (cluster size, shared memory) and remembered.
 bool launch_map_cluster(const int32_t *idx, int64_t n, int E, int cap, int32_t *row_id_map,
                         int32_t *sorted_to_flat, int32_t *counts, int32_t *offsets,
                         int32_t *dev_status, cudaStream_t s, size_t smem, cudaError_t &err)
@@ -673,6 +673,14 @@ bool launch_map_cluster(const int32_t *idx, int64_t n, int E, int cap, int32_t *
     }
     err = cudaLaunchKernelEx(&cfg, fn, idx, n, E, f, (int)nc, cap, (const int32_t *)nullptr,
                              row_id_map, sorted_to_flat, counts, offsets, dev_status);
+    if (err != cudaSuccess) {
+        // The launch was refused (nothing ran): remember, and take the two kernels.
+        cudaGetLastError();
+        err = cudaSuccess;
+        std::lock_guard<std::mutex> lock(mu);
+        fits[nc][1] = 1;
+        return false;
+    }
     return true;
 }
 
@@ -709,14 +717,8 @@ mp_status_t launch_map(const int32_t *idx, int64_t n, int E, int cap, int32_t *r
     }
     if (n <= MAP_CLUSTER_ROUTES &&
         launch_map_cluster(idx, n, E, cap, row_id_map, sorted_to_flat, counts, offsets,
-                           dev_status, s, smem, err)) {
-        if (err != cudaSuccess) {
-            cudaGetLastError();
-            set_last_cuda_error(err);
-            return MP_ERR_CUDA;
-        }
+                           dev_status, s, smem, err))
         return check_launch();
-    }
     const unsigned grid = (unsigned)p.ntiles;
     (void)launch_pdl(k_map_count, grid, MAP_THREADS, (E + 1) * sizeof(int32_t), s, idx, n, E,
                      p.f, (int)p.ntiles, tile_counts, dev_status);
