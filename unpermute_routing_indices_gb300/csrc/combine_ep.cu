@@ -22,6 +22,9 @@
 // or as a TwoSum pair -- and only wider spans take the fp64 additions.  Those
 // forms run the FMA chains and sums on packed fp32 pairs (f32x2: two
 // elements per instruction, each rounded as the scalar operation would be).
+// With bf16 partials, each rounded partial is added to its fp32 sum by a
+// mixed-precision add (add.rn.f32.bf16: the bf16 operand widened exactly,
+// one fp32 rounding), with no separate widening step.
 #include <climits>
 
 #include "common.cuh"
@@ -128,6 +131,14 @@ __device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b)
     uint32_t r;
     asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
+}
+// a0 += bf16 lo half of w, a1 += bf16 hi half (each one fp32 rounding, the
+// bf16 operand widened exactly, as in a plain fp32 add of the widened value).
+__device__ __forceinline__ void add_bf16x2(uint32_t w, float &a0, float &a1)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(a0), "+f"(a1) : "r"(w));
 }
 // The two bf16 of a 32-bit word as a pair of fp32 (exact).
 __device__ __forceinline__ uint64_t bf16x2_wide(uint32_t w) { return f2(bf16_lo(w), bf16_hi(w)); }
@@ -310,11 +321,9 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                 // minimum, NaN patterns exceed every finite one).  With at most
                 // 8 partials, sum |p| <= 8 max, so max <= 2^12 min implies the
                 // plain-add bound and max <= 2^33 min the pair bound.
-                uint64_t sa2[4];
                 uint32_t mx[4], mn[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    sa2[i] = 0;
                     mx[i] = 0;
                     mn[i] = 0x7f807f80u;
                 }
@@ -322,15 +331,14 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                     float lo, hi;
                     f2_split(p, lo, hi);
                     const uint32_t w = pack_bf16x2(lo, hi);
-                    sa2[i] = add2(sa2[i], bf16x2_wide(w));
+                    add_bf16x2(w, sa[2 * i], sa[2 * i + 1]);
                     const uint32_t a = w & 0x7fff7fffu;
                     mx[i] = max_u16x2(mx[i], a);
                     mn[i] = min_u16x2(mn[i], a);
                 });
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    float a0, a1;
-                    f2_split(sa2[i], a0, a1);
+                    const float a0 = sa[2 * i], a1 = sa[2 * i + 1];
                     const uint32_t wb = pack_bf16x2(a0, a1);
                     bits[2 * i] = static_cast<uint16_t>(wb & 0xffffu);
                     bits[2 * i + 1] = static_cast<uint16_t>(wb >> 16);
@@ -471,8 +479,16 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
             float acc[L];
 #pragma unroll
             for (int e = 0; e < L; ++e) acc[e] = 0.0f;
-            walk_ranks<PROBS, BF16P, L>(r, pk, valid, last,
-                                        [&](int e, float p) { acc[e] = __fadd_rn(acc[e], p); });
+            if constexpr (BF16P && L == 8) {
+                walk_ranks2<PROBS>(r, pk, valid, last, [&](int i, uint64_t p) {
+                    float lo, hi;
+                    f2_split(p, lo, hi);
+                    add_bf16x2(pack_bf16x2(lo, hi), acc[2 * i], acc[2 * i + 1]);
+                });
+            } else {
+                walk_ranks<PROBS, BF16P, L>(r, pk, valid, last,
+                                            [&](int e, float p) { acc[e] = __fadd_rn(acc[e], p); });
+            }
             if (c < nvec) st_row(out + t * nvec + c, pack(acc));
         }
     }
