@@ -366,6 +366,8 @@ def test_rows_past_int32_element_offsets():
     ("mid", None, 300),
     ("large", None, 700),         # 2 sub-tiles per tile
     ("mid", 2000, -1),            # no limit: the plain map
+    ("skewed", 300, 10),          # one CTA (2,400 routes)
+    ("skewed", 4000, 150),        # one thread-block cluster (32,000 routes)
 ])
 def test_build_map_capacity(name, T, cap):
     idx, probs, E = wl.routing(name, T=T)
