@@ -35,6 +35,8 @@ def f32(bits):
     ((301, 3), torch.bfloat16, 0),      # 6-byte rows: byte stores
     ((777,), torch.float32, 0),         # probs: 4-byte rows
     ((129, 64), torch.bfloat16, 1),     # 2-byte offset: not 16-byte aligned
+    ((5003, 24), torch.bfloat16, 0),    # 3 vectors a row: a ragged last chunk
+    ((20000, 1024), torch.bfloat16, 0), # more units than one pass of the grid
 ])
 @pytest.mark.parametrize("start", [-5, 0, 7, "last", "rows", "past"])
 def test_zero_rows_from(shape, dtype, offset, start):

@@ -10,7 +10,8 @@
 // round trip, and a CUDA graph replays it with new routing.
 //
 // k_zero_rows_from: a grid-stride store loop over [first_row * row, rows * row)
-// in units of V (16, 4 or 1 bytes, the widest the pointer and row size allow).
+// in units of V (16, 4 or 1 bytes, the widest the pointer and row size allow),
+// four stores per thread per step (a CTA owns 4 * 256 consecutive units).
 // Every CTA reads the start once; with everything routed no store is issued.
 #include "common.cuh"
 
@@ -22,6 +23,7 @@ namespace {
 #endif
 
 constexpr int FILL_THREADS = 256;
+constexpr int FILL_UNROLL = 4;   // stores in flight per thread per step
 constexpr int FILL_MAX_BLOCKS = MP_FILL_MAX_BLOCKS;
 
 template <typename V>
@@ -40,9 +42,13 @@ __global__ void __launch_bounds__(FILL_THREADS)
         z = make_uint4(0, 0, 0, 0);
     else
         z = 0;
-    for (int64_t i = s * units_per_row + (int64_t)blockIdx.x * FILL_THREADS + threadIdx.x;
-         i < end; i += step)
-        buf[i] = z;
+    constexpr int U = FILL_UNROLL;
+    int64_t i = s * units_per_row + (int64_t)blockIdx.x * FILL_THREADS * U + threadIdx.x;
+    for (; i + (U - 1) * FILL_THREADS < end; i += step * U) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) buf[i + u * FILL_THREADS] = z;
+    }
+    for (; i < end; i += FILL_THREADS) buf[i] = z;
 }
 
 template <typename V>
@@ -50,7 +56,7 @@ void launch_fill(void *buf, int64_t rows, int64_t units_per_row, const int32_t *
                  cudaStream_t s)
 {
     const int64_t total = rows * units_per_row;
-    int64_t blocks = (total + FILL_THREADS - 1) / FILL_THREADS;
+    int64_t blocks = (total + FILL_THREADS * FILL_UNROLL - 1) / (FILL_THREADS * FILL_UNROLL);
     blocks = blocks < 1 ? 1 : (blocks > FILL_MAX_BLOCKS ? FILL_MAX_BLOCKS : blocks);
     (void)launch_pdl(k_zero_rows_from<V>, (unsigned)blocks, FILL_THREADS, 0, s,
                      static_cast<V *>(buf), rows, units_per_row, first_row);
