@@ -615,7 +615,8 @@ static_assert(MAP_CLUSTER_ROUTES <= (int64_t)MAP_CLUSTER_MAX * MAP_SUB * MAP_MAX
 
 // Launches the cluster form when the GPU can hold such a cluster; returns
 // false (nothing launched) otherwise, or when the launch is refused.  Whether
-// it fits is asked once per (cluster size, shared memory) and remembered.
+// it fits is asked once per (cluster size, shared memory) and remembered for
+// the process (which drives one GPU).
 bool launch_map_cluster(const int32_t *idx, int64_t n, int E, int cap, int32_t *row_id_map,
                         int32_t *sorted_to_flat, int32_t *counts, int32_t *offsets,
                         int32_t *dev_status, cudaStream_t s, size_t smem, cudaError_t &err)
