@@ -82,11 +82,12 @@ def test_build_map_edges(case):
     check_map(idx, E)
 
 
-def test_build_map_bad_index_sets_status():
+@pytest.mark.parametrize("T", [500, 2500, 12000])   # one CTA, one cluster, two kernels
+def test_build_map_bad_index_sets_status(T):
     rng = np.random.default_rng(5)
-    idx = rng.integers(0, 20, size=(2500, 4)).astype(np.int32)
+    idx = rng.integers(0, 20, size=(T, 4)).astype(np.int32)
     idx[7, 1] = 20
-    idx[1999, 3] = -7
+    idx[T - 3, 3] = -7
     check_map(idx, 20, expect_status=mp.STATUS_BITS["bad_expert"])
 
 
