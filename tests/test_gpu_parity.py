@@ -82,6 +82,27 @@ def test_build_map_edges(case):
     check_map(idx, E)
 
 
+@pytest.mark.parametrize("T,K,E,empty", [
+    (4097, 1, 7, 0.0),        # one route past the one-CTA form: a cluster of 3
+    (513, 8, 64, 0.1),        # 4,104 routes
+    (2048, 16, 1024, 0.0),    # 32,768 routes: 16 CTAs, the largest cluster, E at its limit
+    (2047, 16, 1, 0.3),       # one expert, many empty slots
+    (4000, 8, 257, 0.05),     # 32,000 routes, ragged last tile
+    (1500, 6, 1024, 0.5),     # half the slots empty
+])
+def test_build_map_cluster_sizes(T, K, E, empty):
+    """The map built by one thread-block cluster (4,097 to 32,768 routes)."""
+    rng = np.random.default_rng(T * K + E)
+    idx = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    idx[rng.random((T, K)) < empty] = -1
+    check_map(idx, E)
+    cap = max(1, T * K // (2 * E))
+    got = mp.mp_build_map_capacity(d(idx), E, cap)
+    want = oracle.build_map_capacity(idx, E, cap)
+    for a, b in zip(got, want[:4]):
+        np.testing.assert_array_equal(h(a), b)
+
+
 @pytest.mark.parametrize("T", [500, 2500, 12000])   # one CTA, one cluster, two kernels
 def test_build_map_bad_index_sets_status(T):
     rng = np.random.default_rng(5)
