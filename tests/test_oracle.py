@@ -608,6 +608,29 @@ def test_unpermute_ep_exact_tree(ep, bf16p, fp64):
         np.testing.assert_array_equal(got, _ep_exact(rows, p, rim, idx, T, H, E, ep, bf16p, fp64))
 
 
+def test_unpermute_ep_fp64_sum_decides_a_bf16_tie():
+    """Three ranks with partials 1, 2^-8 and +-2^-30 (one slot each, no probs):
+    1 + 2^-8 lies exactly halfway between the bf16 values 1 and 1 + 2^-7.  The
+    binary64 sum keeps the 2^-30 and rounds away from the tie; an fp32 sum
+    drops it (half an fp32 ulp of 1 is 2^-24) and ties to even, giving 1."""
+    bits = {1.0: 0x3F80, 2.0**-8: 0x3B80, 2.0**-30: 0x3080, -(2.0**-30): 0xB080,
+            -1.0: 0xBF80, -(2.0**-8): 0xBB80}
+    cases = [((1.0, 2.0**-8, 2.0**-30), 0x3F81, 0x3F80),
+             ((1.0, 2.0**-8, -(2.0**-30)), 0x3F80, 0x3F80),
+             ((-1.0, -(2.0**-8), -(2.0**-30)), 0xBF81, 0xBF80)]
+    T, K, E, H = len(cases), 3, 3, 1
+    idx = np.tile(np.arange(3, dtype=np.int32), (T, 1))          # slot k on rank k
+    rim, *_ = oracle.build_map(idx, E)
+    rows = np.zeros((T * K, H), np.uint16)
+    for t, (vals, _, _) in enumerate(cases):
+        for k in range(K):
+            rows[rim[t, k], 0] = bits[vals[k]]
+    y64 = oracle.unpermute_ep(rows, None, rim, idx, T, H, E, 3, False, True)
+    y32 = oracle.unpermute_ep(rows, None, rim, idx, T, H, E, 3, False, False)
+    assert [int(v) for v in y64[:, 0]] == [c[1] for c in cases]
+    assert [int(v) for v in y32[:, 0]] == [c[2] for c in cases]
+
+
 def test_unpermute_ep_with_one_rank_is_unpermute():
     T, K, E, H = 30, 4, 8, 16
     idx, probs, _ = _case(77, T, K, E, H, empty=True)

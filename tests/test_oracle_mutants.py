@@ -134,6 +134,20 @@ MUTANTS = {
                         if (l[e] > score)
                             score = l[e];""",
         [pins.test_topk_softmax_group_limited_brute_force]),
+    "map: rows past the routed ones marked 0 in sorted_to_flat": (
+        "            sorted_to_flat[i] = -1;", "            sorted_to_flat[i] = 0;",
+        [pins.test_worked_example_from_page, _brute_map, pins.test_build_map_invariants]),
+    "sort+pad: padding rows get probability one": (
+        "            out_probs[d] = 0.0f;", "            out_probs[d] = 1.0f;",
+        [_sort_pad_brute]),
+    "unpad+restore backward: padding rows get a gradient": (
+        "g_padded[d * H + h] = ok ? g_y[(int64_t)s * H + h] : (uint16_t)0;",
+        "g_padded[d * H + h] = ok ? g_y[(int64_t)s * H + h] : (uint16_t)0x3f80;",
+        [pins.test_sort_pad_backwards_are_adjoints]),
+    "EP combine: fp64 cross-rank sum rounded to fp32 at each rank": (
+        "                    acc64 = acc64 + (double)partial;",
+        "                    acc64 = (double)(float)(acc64 + (double)partial);",
+        [_ep_exact, pins.test_unpermute_ep_fp64_sum_decides_a_bf16_tie]),
     "router backward: sign flipped": (
         "probs[t * K + k] * (g_probs[t * K + k] - d)", "probs[t * K + k] * (d - g_probs[t * K + k])",
         [pins.test_topk_softmax_bwd_is_the_softmax_jacobian]),
