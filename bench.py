@@ -795,6 +795,17 @@ def bench_chunks(mp, wl, dev, flush, args):
         sp = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
         ur = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
         rt = statistics.median(e[0].elapsed_time(e[2]) for e in evs)
+        # the same roundtrip with events at its ends only: the restore's launch
+        # then overlaps the tail of sort+pad (programmatic dependent launch)
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, z in cev:
+            flush(1)
+            a.record(stream)
+            roundtrip()
+            z.record(stream)
+        torch.cuda.synchronize()
+        rt_chained = statistics.median(a.elapsed_time(z) for a, z in cev)
         padded = int(goff[-1].item())
         b = chunk_bytes(N, H * esize // 2, padded, out_rows)
         key = str(N) if tdt == torch.bfloat16 else f"{N} fp32"
@@ -822,6 +833,7 @@ def bench_chunks(mp, wl, dev, flush, args):
                     "unpad_restore_us": round(ur * 1e3, 2),
                     "roundtrip_GB/s": round((b["sort_chunks_pad"] + b["unpad_restore"])
                                             / (rt * 1e-3) / 1e9, 1),
+                    "roundtrip_chained_ms": round(rt_chained, 4),
                     "sort_pad_alone_us": round(sp_alone, 2),
                     "unpad_restore_alone_us": round(ur_alone, 2),
                     "sort_pad_alone_GB/s": round(b["sort_chunks_pad"] / sp_alone / 1e3, 1),
