@@ -11,6 +11,7 @@ Tensors: bf16 hidden rows, fp32 probabilities, int32 indices and maps.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 
 import torch
@@ -63,8 +64,21 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(device):
+    """The current CUDA stream of `device` as a raw handle."""
+    if _raw_stream is not None and device.index is not None:
+        return ctypes.c_void_p(_raw_stream(device.index))
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _on(device):
+    """Context that makes `device` current for the call (free when it is)."""
+    if device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 def _need(t, name, dtype, ndim=None, device=None):
@@ -150,7 +164,7 @@ def _build_map(fn, idx, num_experts, capacity, with_sorted_to_flat, row_id_map, 
     else:
         _need(workspace, "workspace", torch.uint8, 1, dev)
     _opt(status, "status", torch.int32, 1, dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         if capacity is None:
             code = lib.mp_build_map(
                 _ptr(idx), T, K, E, _ptr(row_id_map), _ptr(sorted_to_flat), _ptr(counts),
@@ -184,7 +198,7 @@ def mp_topk_softmax(logits, topk: int, *, n_groups: int = 1, topk_groups: int = 
         else _need(probs, "probs", torch.float32, 2, dev)
     _shape(idx, "idx", (T, K))
     _shape(probs, "probs", (T, K))
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("mp_topk_softmax", lib.mp_topk_softmax(
             _ptr(logits), T, E, K, int(n_groups), int(topk_groups), _ptr(idx), _ptr(probs),
             _stream(dev)))
@@ -205,7 +219,7 @@ def mp_topk_softmax_bwd(g_probs, probs, idx, num_experts: int, *, g_logits=None)
     g_logits = torch.empty((T, E), dtype=torch.float32, device=dev) if g_logits is None \
         else _need(g_logits, "g_logits", torch.float32, 2, dev)
     _shape(g_logits, "g_logits", (T, E))
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("mp_topk_softmax_bwd", lib.mp_topk_softmax_bwd(
             _ptr(g_probs), _ptr(probs), _ptr(idx), T, E, K, _ptr(g_logits), _stream(dev)))
     return g_logits
@@ -234,7 +248,7 @@ def mp_permute(x, row_id_map, probs=None, *, num_out_rows: int | None = None, ou
     if probs is not None and out_probs is None:
         out_probs = torch.empty(out.shape[0], dtype=torch.float32, device=dev)
     _opt(out_probs, "out_probs", torch.float32, 1, dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("mp_permute", lib.mp_permute(
             _ptr(x), _ptr(probs), _ptr(row_id_map), T, K, H, _ptr(out),
             _ptr(out_probs if probs is not None else None), _stream(dev)))
@@ -255,7 +269,7 @@ def mp_unpermute(rows, row_id_map, probs=None, *, out=None):
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if out is None \
         else _need(out, "out", torch.bfloat16, 2, dev)
     _shape(out, "out", (T, H))
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("mp_unpermute", lib.mp_unpermute(
             _ptr(rows), _ptr(probs), _ptr(row_id_map), T, K, H, _ptr(out), _stream(dev)))
     return out
@@ -282,7 +296,7 @@ def mp_unpermute_ep(rows, row_id_map, idx, num_experts: int, ep_size: int, probs
     _shape(out, "out", (T, H))
     flags = (EP_BF16_PARTIALS if bf16_partials else 0) | \
         (EP_FP64_CROSS_RANK if fp64_cross_rank else 0)
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("mp_unpermute_ep", lib.mp_unpermute_ep(
             _ptr(rows), _ptr(probs), _ptr(row_id_map), _ptr(idx), T, K, H, int(num_experts),
             int(ep_size), flags, _ptr(out), _stream(dev)))
@@ -306,7 +320,7 @@ def mp_permute_bwd(g_out, row_id_map, g_out_probs=None, *, g_x=None, g_probs=Non
     if g_out_probs is None:
         g_probs = None
     _opt(g_probs, "g_probs", torch.float32, 2, dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("mp_permute_bwd", lib.mp_permute_bwd(
             _ptr(g_out), _ptr(g_out_probs), _ptr(row_id_map), T, K, H, _ptr(g_x),
             _ptr(g_probs), _stream(dev)))
@@ -339,7 +353,7 @@ def mp_unpermute_bwd(g_y, row_id_map, rows=None, probs=None, *, num_out_rows=Non
     if probs is None:
         g_probs = None
     _opt(g_probs, "g_probs", torch.float32, 2, dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("mp_unpermute_bwd", lib.mp_unpermute_bwd(
             _ptr(g_y), _ptr(rows), _ptr(probs), _ptr(row_id_map), T, K, H, _ptr(g_rows),
             _ptr(g_probs), _stream(dev)))
@@ -359,7 +373,7 @@ def mp_zero_rows_from(buf, first_row):
         raise ValueError("first_row must hold at least one element")
     rows = buf.shape[0] if buf.dim() > 0 else 1
     row_bytes = (buf.numel() // rows if rows else 0) * buf.element_size()
-    with torch.cuda.device(dev):
+    with _on(dev):
         _check("mp_zero_rows_from", lib.mp_zero_rows_from(
             _ptr(buf), rows, row_bytes, _ptr(first_row), _stream(dev)))
     return buf
@@ -405,7 +419,7 @@ def mp_sort_chunks_pad(x, split_sizes, chunk_order, num_groups: int, align: int,
     group_off = torch.empty(G + 1, dtype=torch.int64, device=dev) if group_off is None \
         else _need(group_off, "group_off", torch.int64, 1, dev)
     _opt(status, "status", torch.int32, 1, dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         if dt == 0 and padded_sizes is None:
             code = lib.mp_sort_chunks_pad(
                 _ptr(x), _ptr(probs), _ptr(split_sizes), _ptr(chunk_order), C, G, int(align), N,
@@ -436,7 +450,7 @@ def _remap(name, src, row_map, n_rows, src_probs, out, out_probs, status, gather
     if src_probs is None:
         out_probs = None
     _opt(status, "status", torch.int32, 1, dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         if dt == 0:
             code = getattr(lib, name)(
                 _ptr(src), _ptr(src_probs), _ptr(row_map), row_map.shape[0], int(n_rows), H,
