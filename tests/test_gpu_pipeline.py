@@ -40,8 +40,9 @@ def _step_fn(E, T, K, H):
     return step
 
 
-@pytest.mark.parametrize("n_steps", [1, 2, 7])
-def test_pipeline_matches_serial_steps(n_steps):
+@pytest.mark.parametrize("n_steps,graph", [(1, False), (2, False), (7, False), (1, True),
+                                           (7, True)])
+def test_pipeline_matches_serial_steps(n_steps, graph):
     T, H = 2048, 1024
     sets = []
     for s in range(3):
@@ -53,7 +54,7 @@ def test_pipeline_matches_serial_steps(n_steps):
     out_spec = {"y": ((T, H), torch.bfloat16), "g_x": ((T, H), torch.bfloat16),
                 "g_probs": ((T, K), torch.float32)}
     step = _step_fn(E, T, K, H)
-    pipe = HostPipeline(DEV, in_spec, out_spec, step)
+    pipe = HostPipeline(DEV, in_spec, out_spec, step, graph=graph)
     host_in = [sets[i % 3] for i in range(n_steps)]
     host_out = [{k: torch.empty(s, dtype=t).pin_memory() for k, (s, t) in out_spec.items()}
                 for _ in range(n_steps)]

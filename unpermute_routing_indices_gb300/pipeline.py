@@ -14,6 +14,12 @@ compute of step i-2 has finished reading that input set, and its compute
 waits until the copy-out of step i-2 has finished reading that output set.
 The step function launches library calls on the current stream; it must not
 allocate buffers that outlive the call on another stream.
+
+With graph=True the step is captured once per buffer set, as a CUDA graph on
+the compute stream, the first time that set is used; later steps replay the
+graph, so issuing a step costs one replay instead of one Python call per
+kernel.  The step must then be capturable: no host synchronisation and no
+data-dependent host logic.  Every library call is.
 """
 from __future__ import annotations
 
@@ -32,8 +38,11 @@ class HostPipeline:
     specs; device buffers (two sets each) are allocated here."""
 
     def __init__(self, device, in_spec: Spec, out_spec: Spec,
-                 step: Callable[[Dict[str, torch.Tensor], Dict[str, torch.Tensor]], None]):
+                 step: Callable[[Dict[str, torch.Tensor], Dict[str, torch.Tensor]], None],
+                 graph: bool = False):
         self.device = torch.device(device)
+        self.graph = graph
+        self._graphs = [None, None]     # the captured step of each buffer set
         self.in_spec, self.out_spec, self.step = in_spec, out_spec, step
         self.dev_in = [{k: torch.empty(s, dtype=t, device=self.device)
                         for k, (s, t) in in_spec.items()} for _ in range(2)]
@@ -71,6 +80,11 @@ class HostPipeline:
         self._check_host(host_out, self.out_spec, "output")
         b = i % 2
         din, dout = self.dev_in[b], self.dev_out[b]
+        if self.graph and self._graphs[b] is None:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.s_comp):
+                self.step(din, dout)
+            self._graphs[b] = g
         with torch.cuda.stream(self.s_in):
             if self._in_free[b] is not None:
                 self.s_in.wait_event(self._in_free[b])
@@ -82,7 +96,10 @@ class HostPipeline:
             self.s_comp.wait_event(ready)
             if self._out_free[b] is not None:
                 self.s_comp.wait_event(self._out_free[b])
-            self.step(din, dout)
+            if self.graph:
+                self._graphs[b].replay()
+            else:
+                self.step(din, dout)
             done = torch.cuda.Event()
             done.record(self.s_comp)
         self._in_free[b] = done
