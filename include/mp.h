@@ -26,6 +26,11 @@
  *    returns.  Grids depend on the shape arguments only, so a call can be
  *    captured in a CUDA graph and replayed with new routing in the same
  *    buffers.
+ *  - Kernels are launched as programmatic dependents of the work before them
+ *    in the stream: a kernel may be scheduled while the previous kernel
+ *    drains, but it waits for that kernel to finish before it touches
+ *    memory.  Stream order holds as for ordinary launches, and a caller needs
+ *    no extra synchronisation.
  *  - Tensors are dense and row-major.  bf16 tensors are passed as their
  *    16-bit patterns (mp_bf16_t).  A row of H bf16 values is 2*H bytes.
  *    Rows move as 16-byte vectors when H % 8 == 0 and every row pointer is
