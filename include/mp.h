@@ -258,7 +258,7 @@ mp_status_t mp_unpermute(const mp_bf16_t *rows, const float *probs,
  * flags gives exactly mp_unpermute.
  *   idx        device int32 [T,K]: the expert of each slot (the routing input
  *              of mp_build_map); other arguments as mp_unpermute.
- * Limits: K <= 8, E % ep_size == 0.
+ * Limits: K <= 16, E % ep_size == 0.
  */
 mp_status_t mp_unpermute_ep(const mp_bf16_t *rows, const float *probs,
                             const int32_t *row_id_map, const int32_t *idx, int64_t T, int32_t K,

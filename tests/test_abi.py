@@ -138,7 +138,7 @@ def test_router_bwd_rejects(lib):
     ((FAKE, None, FAKE, FAKE, 4, 2, 64, 64, 6, 0, FAKE, None), -1),       # E % ep_size != 0
     ((FAKE, None, FAKE, FAKE, 4, 2, 64, 64, 0, 0, FAKE, None), -1),       # ep_size < 1
     ((FAKE, None, FAKE, FAKE, 4, 2, 64, 64, 8, 4, FAKE, None), -1),       # unknown flag
-    ((FAKE, None, FAKE, FAKE, 4, 9, 64, 64, 8, 0, FAKE, None), -3),       # K > 8
+    ((FAKE, None, FAKE, FAKE, 4, 17, 64, 64, 8, 0, FAKE, None), -3),      # K > 16
     ((FAKE, None, FAKE, None, 4, 2, 64, 64, 8, 0, FAKE, None), -1),       # idx NULL
     ((None, None, None, None, 0, 2, 64, 64, 8, 3, None, None), 0),        # empty: no-op
 ])

@@ -3,7 +3,7 @@
 Each case draws T, K, E, H, the fraction of empty slots, duplicate experts
 per token and a pointer offset (so both the 16-byte vector path and the
 element path run), then checks the map, permute, unpermute (with and
-without probs), both backwards, the EP combine (every mode, K <= 8), the
+without probs), both backwards, the EP combine (every mode, K <= 16), the
 router and the chunk sort+pad roundtrip: bit-exact, except the probability
 gradient (fp32 summation bound against the oracle's fp64 sum) and the router
 probabilities (a few ulps: two expf implementations)."""
@@ -85,7 +85,7 @@ def test_routed_ops_fuzz(seed):
     bound = gprobs_bound(_f32(rows)[np.maximum(o_rim, 0)], _f32(gy)[:, None, :], o_gprobs)
     assert np.all(np.abs(gp - o_gprobs) <= bound)
 
-    if K <= 8:
+    if K <= 16:
         ep = int(rng.choice([r for r in (1, 2, 4, 8) if E % r == 0]))
         for bf16p, fp64 in ((False, False), (True, False), (False, True), (True, True)):
             got = mp.mp_unpermute_ep(drows, rim, d(idx), E, ep, dp, bf16_partials=bf16p,

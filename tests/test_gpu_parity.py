@@ -445,6 +445,27 @@ def test_unpermute_ep(name, T, H, ep, bf16p, fp64):
         np.testing.assert_array_equal(h(got), want)
 
 
+@pytest.mark.parametrize("K,H,ep", [(12, 136, 8), (16, 64, 4), (9, 37, 16), (16, 40, 64)])
+@pytest.mark.parametrize("bf16p,fp64", [(False, False), (True, False), (False, True),
+                                         (True, True)])
+def test_unpermute_ep_more_than_eight_slots(K, H, ep, bf16p, fp64):
+    """9 to 16 slots per token (the second kernel form), with empty slots and
+    repeated experts, on the vector and element paths."""
+    rng = np.random.default_rng(K * H + ep)
+    T, E = 777, 64
+    idx = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    idx[rng.random((T, K)) < 0.15] = -1
+    probs = rng.random((T, K)).astype(np.float32)
+    rows = wl.random_rows(T * K, H, K + H)
+    rim, *_ = mp.mp_build_map(d(idx), E)
+    o_rim, *_ = oracle.build_map(idx, E)
+    for p in (probs, None):
+        got = mp.mp_unpermute_ep(d(rows), rim, d(idx), E, ep, None if p is None else d(p),
+                                 bf16_partials=bf16p, fp64_cross_rank=fp64)
+        want = oracle.unpermute_ep(rows, p, o_rim, idx, T, H, E, ep, bf16p, fp64)
+        np.testing.assert_array_equal(h(got), want)
+
+
 def test_unpermute_ep_one_rank_is_unpermute():
     w = _full_case("mid", T=1000)
     rim, *_ = mp.mp_build_map(d(w["idx"]), w["E"])

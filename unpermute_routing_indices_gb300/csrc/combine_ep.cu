@@ -33,7 +33,7 @@ namespace mp {
 namespace {
 
 constexpr int EP_THREADS = 128;
-constexpr int EP_KMAX = 8;
+constexpr int EP_KMAX = 16;   // slots per token: kernels for K <= 8 and for K <= 16
 
 // fp64 -> bf16, round to nearest even, in a single rounding, from the binary64
 // fields: keep the top 8 significant bits (1 + 7) for normal bf16 results, or
@@ -155,8 +155,7 @@ __device__ __forceinline__ void cx(int32_t &ka, int32_t &ra, float &pa, int32_t 
 }
 
 // Batcher's odd-even merge sort of 8 keys (19 comparators, fixed indices).
-__device__ __forceinline__ void sort8(int32_t (&k)[EP_KMAX], int32_t (&r)[EP_KMAX],
-                                      float (&p)[EP_KMAX])
+__device__ __forceinline__ void sort8(int32_t (&k)[8], int32_t (&r)[8], float (&p)[8])
 {
 #define MP_CX(a, b) cx(k[a], r[a], p[a], k[b], r[b], p[b])
     MP_CX(0, 1); MP_CX(2, 3); MP_CX(4, 5); MP_CX(6, 7);
@@ -168,19 +167,42 @@ __device__ __forceinline__ void sort8(int32_t (&k)[EP_KMAX], int32_t (&r)[EP_KMA
 #undef MP_CX
 }
 
+// The same merge sort for any power-of-two N (63 comparators for 16; every
+// index a compile-time constant once unrolled).  N = 8 uses the hand-ordered
+// network above, which the compiler schedules into fewer registers.
+template <int N>
+__device__ __forceinline__ void sort_slots(int32_t (&k)[N], int32_t (&r)[N], float (&p)[N])
+{
+    if constexpr (N == 8) {
+        sort8(k, r, p);
+    } else {
+#pragma unroll
+        for (int w = 1; w < N; w <<= 1)
+#pragma unroll
+            for (int q = w; q >= 1; q >>= 1)
+#pragma unroll
+                for (int j = q % w; j + q < N; j += 2 * q)
+#pragma unroll
+                    for (int i = 0; i < q; ++i)
+                        if (i + j + q < N && (i + j) / (2 * w) == (i + j + q) / (2 * w))
+                            cx(k[i + j], r[i + j], p[i + j], k[i + j + q], r[i + j + q],
+                               p[i + j + q]);
+    }
+}
+
 // Walks the token's slots sorted by (rank, slot): a slot-order chain of fused
 // multiply-adds (plain adds without probs) from +0 per rank, and add(e, p) at
 // each rank's last slot with the rank's partial p for element e (rounded to
 // bf16 if BF16P).  `valid` / `last` are bit masks over the sorted positions.
-template <bool PROBS, bool BF16P, int L, typename V, typename Add>
-__device__ __forceinline__ void walk_ranks(const V (&r)[EP_KMAX], const float (&p)[EP_KMAX],
+template <bool PROBS, bool BF16P, int L, int KM, typename V, typename Add>
+__device__ __forceinline__ void walk_ranks(const V (&r)[KM], const float (&p)[KM],
                                            unsigned valid, unsigned last, Add add)
 {
     float part[L];
 #pragma unroll
     for (int e = 0; e < L; ++e) part[e] = 0.0f;
 #pragma unroll
-    for (int j = 0; j < EP_KMAX; ++j) {
+    for (int j = 0; j < KM; ++j) {
         if (!(valid >> j & 1u)) continue;
         float f[L];
         unpack(r[j], f);
@@ -198,15 +220,15 @@ __device__ __forceinline__ void walk_ranks(const V (&r)[EP_KMAX], const float (&
 }
 
 // walk_ranks on packed pairs: the four element pairs of a 16-byte vector.
-template <bool PROBS, typename Add>
-__device__ __forceinline__ void walk_ranks2(const uint4 (&r)[EP_KMAX], const float (&p)[EP_KMAX],
+template <bool PROBS, int KM, typename Add>
+__device__ __forceinline__ void walk_ranks2(const uint4 (&r)[KM], const float (&p)[KM],
                                             unsigned valid, unsigned last, Add add)
 {
     uint64_t part[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) part[i] = 0;
 #pragma unroll
-    for (int j = 0; j < EP_KMAX; ++j) {
+    for (int j = 0; j < KM; ++j) {
         if (!(valid >> j & 1u)) continue;
         const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
         const uint64_t pp = f2(p[j], p[j]);
@@ -229,10 +251,15 @@ __device__ __forceinline__ void walk_ranks2(const uint4 (&r)[EP_KMAX], const flo
 // registers it spills (fp32 215 -> 187 us at 7 CTAs, bf16 partials 243 ->
 // 199 us); the fp64 forms, which also prefetch their next pass into L2, are
 // best at 5 (bf16 partials, 242 us) and 4 (fp32 partials, 300 us).
-constexpr int ep_min_blocks(bool fp64, bool bf16p) { return fp64 ? (bf16p ? 5 : 4) : 7; }
+// With up to 16 slots a thread holds twice the rows: 2 CTAs per SM (rare
+// shapes; correctness first).
+constexpr int ep_min_blocks(bool fp64, bool bf16p, int km)
+{
+    return km > 8 ? 2 : (fp64 ? (bf16p ? 5 : 4) : 7);
+}
 
-template <typename V, bool PROBS, bool BF16P, bool FP64>
-__global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
+template <typename V, bool PROBS, bool BF16P, bool FP64, int KM>
+__global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P, KM))
     k_unpermute_ep(const V *__restrict__ rows, const float *__restrict__ probs,
                    const int32_t *__restrict__ map, const int32_t *__restrict__ idx, int64_t T,
                    int K, int nvec, int tpt_log2, int per_rank, V *__restrict__ out)
@@ -246,34 +273,34 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
     if (t >= T) return;
 
     // The token's routed slots sorted by (rank, slot); unrouted slots last.
-    int32_t key[EP_KMAX], rk[EP_KMAX];
-    float pk[EP_KMAX];
+    int32_t key[KM], rk[KM];
+    float pk[KM];
 #pragma unroll
-    for (int i = 0; i < EP_KMAX; ++i) {
+    for (int i = 0; i < KM; ++i) {
         const bool in = i < K;
         const int32_t row = in ? __ldg(map + t * K + i) : -1;
         int32_t rank = in ? __ldg(idx + t * K + i) / per_rank : 0;
         rank = rank < -(1 << 20) ? -(1 << 20) : (rank > (1 << 20) ? (1 << 20) : rank);
-        key[i] = row >= 0 ? rank * EP_KMAX + i : INT_MAX;
+        key[i] = row >= 0 ? rank * KM + i : INT_MAX;
         rk[i] = row;
         pk[i] = (PROBS && in) ? __ldg(probs + t * K + i) : 1.0f;
     }
-    sort8(key, rk, pk);
+    sort_slots<KM>(key, rk, pk);
     unsigned valid = 0, last = 0;
 #pragma unroll
-    for (int j = 0; j < EP_KMAX; ++j) {
+    for (int j = 0; j < KM; ++j) {
         if (key[j] == INT_MAX) continue;
         valid |= 1u << j;
-        const bool next_same = j + 1 < EP_KMAX && key[j + 1] != INT_MAX &&
-                               (key[j + 1] - (key[j + 1] & (EP_KMAX - 1))) ==
-                                   (key[j] - (key[j] & (EP_KMAX - 1)));
+        const bool next_same = j + 1 < KM && key[j + 1] != INT_MAX &&
+                               (key[j + 1] - (key[j + 1] & (KM - 1))) ==
+                                   (key[j] - (key[j] & (KM - 1)));
         if (!next_same) last |= 1u << j;
     }
     for (int c0 = 0; c0 < nvec; c0 += tpt) {
         const int c = c0 + lane;
-        V r[EP_KMAX];
+        V r[KM];
 #pragma unroll
-        for (int i = 0; i < EP_KMAX; ++i)
+        for (int i = 0; i < KM; ++i)
             r[i] = ((valid >> i & 1u) && c < nvec) ? ld_stream(rows + (int64_t)rk[i] * nvec + c)
                                                    : zero_vec<V>();
         if constexpr (FP64) {
@@ -281,7 +308,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
             // of the next pass's rows behind it
             const int cn = c + tpt;
 #pragma unroll
-            for (int i = 0; i < EP_KMAX; ++i)
+            for (int i = 0; i < KM; ++i)
                 if ((valid >> i & 1u) && cn < nvec)
                     asm volatile("prefetch.global.L2 [%0];"
                                  ::"l"(rows + (int64_t)rk[i] * nvec + cn));
@@ -327,7 +354,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                     mx[i] = 0;
                     mn[i] = 0x7f807f80u;
                 }
-                walk_ranks2<PROBS>(r, pk, valid, last, [&](int i, uint64_t p) {
+                walk_ranks2<PROBS, KM>(r, pk, valid, last, [&](int i, uint64_t p) {
                     float lo, hi;
                     f2_split(p, lo, hi);
                     const uint32_t w = pack_bf16x2(lo, hi);
@@ -358,7 +385,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                         sa[e] = 0.0f;
                         sb[e] = 0.0f;
                     }
-                    walk_ranks<PROBS, true, L>(r, pk, valid, last, [&](int e, float p) {
+                    walk_ranks<PROBS, true, L, KM>(r, pk, valid, last, [&](int e, float p) {
                         const float s = __fadd_rn(sa[e], p);
                         const float bb = __fsub_rn(s, sa[e]);
                         sb[e] = __fadd_rn(sb[e], __fadd_rn(__fsub_rn(sa[e], __fsub_rn(s, bb)),
@@ -370,7 +397,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                         if (pair >> e & 1u) bits[e] = bf16_from_pair(sa[e], sb[e]);
                 }
             } else if (BF16P) {
-                walk_ranks<PROBS, true, L>(r, pk, valid, last, [&](int e, float p) {
+                walk_ranks<PROBS, true, L, KM>(r, pk, valid, last, [&](int e, float p) {
                     sa[e] = __fadd_rn(sa[e], p);
                     sb[e] = __fadd_rn(sb[e], fabsf(p));
                     sm[e] = fminf(sm[e], fabsf(p));
@@ -389,7 +416,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                         sa[e] = 0.0f;
                         sb[e] = 0.0f;
                     }
-                    walk_ranks<PROBS, true, L>(r, pk, valid, last, [&](int e, float p) {
+                    walk_ranks<PROBS, true, L, KM>(r, pk, valid, last, [&](int e, float p) {
                         const float s = __fadd_rn(sa[e], p);
                         const float bb = __fsub_rn(s, sa[e]);
                         sb[e] = __fadd_rn(sb[e], __fadd_rn(__fsub_rn(sa[e], __fsub_rn(s, bb)),
@@ -404,7 +431,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                 uint64_t sa2[4], sl2[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) sa2[i] = sl2[i] = 0;
-                walk_ranks2<PROBS>(r, pk, valid, last, [&](int i, uint64_t p) {
+                walk_ranks2<PROBS, KM>(r, pk, valid, last, [&](int i, uint64_t p) {
                     const uint64_t s2 = add2(sa2[i], p);
                     const uint64_t bb = sub2(s2, sa2[i]);
                     sl2[i] = add2(sl2[i], add2(sub2(sa2[i], sub2(s2, bb)), sub2(p, bb)));
@@ -448,7 +475,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                 float sl[L];
 #pragma unroll
                 for (int e = 0; e < L; ++e) sl[e] = 0.0f;
-                walk_ranks<PROBS, false, L>(r, pk, valid, last, [&](int e, float p) {
+                walk_ranks<PROBS, false, L, KM>(r, pk, valid, last, [&](int e, float p) {
                     const float s = __fadd_rn(sa[e], p);
                     const float bb = __fsub_rn(s, sa[e]);
                     sl[e] = __fadd_rn(sl[e], __fadd_rn(__fsub_rn(sa[e], __fsub_rn(s, bb)),
@@ -467,7 +494,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
                 double acc[L];
 #pragma unroll
                 for (int e = 0; e < L; ++e) acc[e] = 0.0;
-                walk_ranks<PROBS, BF16P, L>(r, pk, valid, last, [&](int e, float p) {
+                walk_ranks<PROBS, BF16P, L, KM>(r, pk, valid, last, [&](int e, float p) {
                     acc[e] = __dadd_rn(acc[e], (double)p);
                 });
 #pragma unroll
@@ -480,13 +507,13 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
 #pragma unroll
             for (int e = 0; e < L; ++e) acc[e] = 0.0f;
             if constexpr (BF16P && L == 8) {
-                walk_ranks2<PROBS>(r, pk, valid, last, [&](int i, uint64_t p) {
+                walk_ranks2<PROBS, KM>(r, pk, valid, last, [&](int i, uint64_t p) {
                     float lo, hi;
                     f2_split(p, lo, hi);
                     add_bf16x2(pack_bf16x2(lo, hi), acc[2 * i], acc[2 * i + 1]);
                 });
             } else {
-                walk_ranks<PROBS, BF16P, L>(r, pk, valid, last,
+                walk_ranks<PROBS, BF16P, L, KM>(r, pk, valid, last,
                                             [&](int e, float p) { acc[e] = __fadd_rn(acc[e], p); });
             }
             if (c < nvec) st_row(out + t * nvec + c, pack(acc));
@@ -494,7 +521,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P))
     }
 }
 
-template <typename V, bool PROBS, bool BF16P, bool FP64>
+template <typename V, bool PROBS, bool BF16P, bool FP64, int KM>
 void launch_ep(const void *rows, const float *probs, const int32_t *map, const int32_t *idx,
                int64_t T, int K, int nvec, int per_rank, void *out, cudaStream_t s)
 {
@@ -503,8 +530,25 @@ void launch_ep(const void *rows, const float *probs, const int32_t *map, const i
     if (l > lmax) l = lmax;
     const int64_t per_block = EP_THREADS >> l;
     const unsigned blocks = (unsigned)((T + per_block - 1) / per_block);
-    (void)launch_pdl(k_unpermute_ep<V, PROBS, BF16P, FP64>, blocks, EP_THREADS, 0, s,
+    (void)launch_pdl(k_unpermute_ep<V, PROBS, BF16P, FP64, KM>, blocks, EP_THREADS, 0, s,
         (const V *)rows, probs, map, idx, T, K, nvec, l, per_rank, (V *)out);
+}
+
+template <typename V, bool PROBS, int KM>
+void launch_ep_km(int flags, const void *rows, const float *probs, const int32_t *map,
+                  const int32_t *idx, int64_t T, int K, int nvec, int per_rank, void *out,
+                  cudaStream_t s)
+{
+    const bool b = flags & MP_EP_BF16_PARTIALS, d = flags & MP_EP_FP64_CROSS_RANK;
+    if (b && d)
+        launch_ep<V, PROBS, true, true, KM>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
+    else if (b)
+        launch_ep<V, PROBS, true, false, KM>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
+    else if (d)
+        launch_ep<V, PROBS, false, true, KM>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
+    else
+        launch_ep<V, PROBS, false, false, KM>(rows, probs, map, idx, T, K, nvec, per_rank, out,
+                                              s);
 }
 
 template <typename V, bool PROBS>
@@ -512,15 +556,10 @@ void launch_ep_flags(int flags, const void *rows, const float *probs, const int3
                      const int32_t *idx, int64_t T, int K, int nvec, int per_rank, void *out,
                      cudaStream_t s)
 {
-    const bool b = flags & MP_EP_BF16_PARTIALS, d = flags & MP_EP_FP64_CROSS_RANK;
-    if (b && d)
-        launch_ep<V, PROBS, true, true>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
-    else if (b)
-        launch_ep<V, PROBS, true, false>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
-    else if (d)
-        launch_ep<V, PROBS, false, true>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
+    if (K <= 8)
+        launch_ep_km<V, PROBS, 8>(flags, rows, probs, map, idx, T, K, nvec, per_rank, out, s);
     else
-        launch_ep<V, PROBS, false, false>(rows, probs, map, idx, T, K, nvec, per_rank, out, s);
+        launch_ep_km<V, PROBS, 16>(flags, rows, probs, map, idx, T, K, nvec, per_rank, out, s);
 }
 
 }  // namespace
