@@ -10,8 +10,9 @@
 // EP ranks are simulated: rank r owns experts [r*E/ep, (r+1)*E/ep).
 //
 // k_unpermute_ep: one group of tpt threads per token, one 16-byte vector (8
-// elements) per thread per pass.  Each thread sorts the token's K (<= 8)
-// slots by (rank, slot) once, with a fixed sorting network on registers, then
+// elements) per thread per pass.  Each thread sorts the token's K (<= 8, or
+// <= 16 in a second form) slots by (rank, slot) once, with a fixed sorting
+// network on registers, then
 // per pass loads the rows in that order and runs one fused multiply-add chain
 // that hands the rank's partial to the cross-rank sum at each rank's last
 // slot: K FMAs per element whatever the number of ranks.  A rank with no
