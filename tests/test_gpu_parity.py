@@ -445,14 +445,16 @@ def test_unpermute_ep(name, T, H, ep, bf16p, fp64):
         np.testing.assert_array_equal(h(got), want)
 
 
-@pytest.mark.parametrize("K,H,ep", [(12, 136, 8), (16, 64, 4), (9, 37, 16), (16, 40, 64)])
+@pytest.mark.parametrize("K,H,ep", [(12, 136, 8), (16, 64, 4), (9, 37, 16), (16, 40, 64),
+                                    (8, 72, 3), (6, 48, 6)])    # ranks not a power of two
 @pytest.mark.parametrize("bf16p,fp64", [(False, False), (True, False), (False, True),
                                          (True, True)])
-def test_unpermute_ep_more_than_eight_slots(K, H, ep, bf16p, fp64):
-    """9 to 16 slots per token (the second kernel form), with empty slots and
-    repeated experts, on the vector and element paths."""
+def test_unpermute_ep_wide_slots_and_odd_ranks(K, H, ep, bf16p, fp64):
+    """9 to 16 slots per token (the second kernel form), and rank counts that
+    are not powers of two, with empty slots and repeated experts, on the
+    vector and element paths."""
     rng = np.random.default_rng(K * H + ep)
-    T, E = 777, 64
+    T, E = 777, (64 if 64 % ep == 0 else 96)
     idx = rng.integers(0, E, size=(T, K)).astype(np.int32)
     idx[rng.random((T, K)) < 0.15] = -1
     probs = rng.random((T, K)).astype(np.float32)
