@@ -3,6 +3,7 @@ thread pool gives the single-thread oracle's bits, and the oracle wrappers'
 caller-owned outputs take only the rows the map names."""
 from __future__ import annotations
 
+import os
 from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
@@ -85,3 +86,24 @@ def test_sharded_oracle_reports_its_sample():
         assert "2 threads" in d and "bit-identical" in d
     finally:
         so.close()
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line with the keys the driver reads, on the GPU arm's metric."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "1"], capture_output=True, text=True,
+                         timeout=600, check=True).stdout
+    line = json.loads(out.strip().splitlines()[-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
