@@ -518,14 +518,14 @@ def test_unpermute_ep_wide_ranging_partials():
 @pytest.mark.parametrize("bf16p", [True, False])
 def test_unpermute_ep_fp64_sum_on_bf16_ties(bf16p):
     """Rank partials 1, 2^-8 (together exactly halfway between two bf16 values)
-    and a small third partial on a third rank that decides the rounding.  The
-    spans reach each way the kernel forms the exact sum, on both sides of
-    each bound: with bf16 partials, plain fp32 adds while the largest
-    magnitude is at most 2^12 times the smallest and an fp32 TwoSum pair up to
-    2^33; with fp32 partials, the pair while the sum of magnitudes is at most
-    2^20 times the smallest; fp64 adds beyond; and a zero partial.  With fp32
-    partials the pair's rounded sum is a bf16 midpoint in most rows, so the
-    pair's error decides."""
+    and a small third partial on a third rank that decides the rounding, from
+    2^-12 to 2^-40 of the first, either sign, or zero.  A third partial
+    below an fp32 ulp of the sum puts the midpoint at one end of the kernel's
+    directed-rounding bracket: where the other end rounds the other way, the
+    kernel takes its fp64 path for that element; elsewhere the bracket
+    decides alone.  The oracle's rounding of some rows is pinned below.  The last
+    rows cancel exactly: a sum rounded toward -inf gives -0 there, where the
+    fp64 sum is +0."""
     E, ep, K, H = 8, 4, 3, 8
     vals = [(1.0, 2.0**-8, 2.0**-30), (1.0, 2.0**-8, -2.0**-30), (1.0, 2.0**-8, 2.0**-40),
             (1.0, 2.0**-8, -2.0**-40), (1.0, 2.0**-8, 0.0), (-1.0, -(2.0**-8), -(2.0**-30)),
@@ -533,7 +533,8 @@ def test_unpermute_ep_fp64_sum_on_bf16_ties(bf16p):
             (1.0, 2.0**-8, 2.0**-12), (1.0, 2.0**-8, -2.0**-12), (1.0, 2.0**-8, 2.0**-14),
             (1.0, 2.0**-8, -2.0**-15), (1.0, 2.0**-8, 2.0**-15), (1.0, 2.0**-8, 2.0**-19),
             (1.0, 2.0**-8, -2.0**-21), (-(2.0**-14), -1.0, -(2.0**-8)),
-            (1.0, 2.0**-8, 2.0**-33), (1.0, 2.0**-8, -2.0**-34), (1.0, 2.0**-8, 2.0**-20)]
+            (1.0, 2.0**-8, 2.0**-33), (1.0, 2.0**-8, -2.0**-34), (1.0, 2.0**-8, 2.0**-20),
+            (1.0, -1.0, 0.0), (1.0, -1.0, 2.0**-30), (-(2.0**-8), 1.0, -1.0)]
     T = len(vals)
     idx = np.tile(np.array([[0, 2, 4]], np.int32), (T, 1))      # ranks 0, 1, 2
     rows_f = np.zeros((T * K, H), np.float32)

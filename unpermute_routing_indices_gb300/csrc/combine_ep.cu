@@ -18,14 +18,15 @@
 // slot: K FMAs per element whatever the number of ranks.  A rank with no
 // routed slot would add +0 to an accumulator that is never -0, so skipping it
 // changes no bit.  GB300 runs FP64 at a small fraction of its FP32 rate, so
-// where the fp64 sum of the partials is provably exact (their magnitudes span
-// few enough binades) the same exact sum is formed in fp32 -- by plain adds,
-// or as a TwoSum pair -- and only wider spans take the fp64 additions.  Those
-// forms run the FMA chains and sums on packed fp32 pairs (f32x2: two
-// elements per instruction, each rounded as the scalar operation would be).
-// With bf16 partials, each rounded partial is added to its fp32 sum by a
-// mixed-precision add (add.rn.f32.bf16: the bf16 operand widened exactly,
-// one fp32 rounding), with no separate widening step.
+// the fp64 cross-rank forms bracket the fp64 sum between two fp32 sums
+// rounded toward -inf and +inf; where both round to the same bf16 value that
+// is the result, and only the rare elements whose bracket holds a bf16
+// midpoint take fp64 additions.  Those forms run the FMA chains and the
+// bracket on packed fp32 pairs (f32x2: two elements per instruction, each
+// rounded as the scalar operation would be).  Without the fp64 sum, bf16
+// partials are added to their fp32 sum by a mixed-precision add
+// (add.rn.f32.bf16: the bf16 operand widened exactly, one fp32 rounding),
+// with no separate widening step.
 #include <climits>
 
 #include "common.cuh"
@@ -65,28 +66,12 @@ __device__ __forceinline__ uint16_t bf16_from_f64(double d)
     return static_cast<uint16_t>(sign | keep);
 }
 
-// bf16 (round to nearest even) of the exact value a + b of two floats.  After
-// TwoSum, hi = fl(a + b) and lo = the exact error; bf16 rounding of hi is right
-// unless hi lies exactly halfway between two bf16 values, where the sign of lo
-// (the side of the tie the exact value is on) decides.
-__device__ __forceinline__ uint16_t bf16_from_pair(float a, float b)
-{
-    const float hi = __fadd_rn(a, b);
-    const float bb = __fsub_rn(hi, a);
-    const float lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
-    const uint32_t u = __float_as_uint(hi);
-    if ((u & 0xffffu) == 0x8000u && lo != 0.0f && (u & 0x7f800000u) != 0x7f800000u) {
-        const bool away = (lo > 0.0f) == (hi > 0.0f);   // exact value beyond the tie
-        return static_cast<uint16_t>((u >> 16) + (away ? 1u : 0u));
-    }
-    __nv_bfloat16 h = __float2bfloat16_rn(hi);
-    return *reinterpret_cast<uint16_t *>(&h);
-}
-
 __device__ __forceinline__ uint4 pack_bits(const uint16_t (&b)[8])
 {
-    return make_uint4((uint32_t)b[0] | ((uint32_t)b[1] << 16), (uint32_t)b[2] | ((uint32_t)b[3] << 16),
-                      (uint32_t)b[4] | ((uint32_t)b[5] << 16), (uint32_t)b[6] | ((uint32_t)b[7] << 16));
+    return make_uint4((uint32_t)b[0] | ((uint32_t)b[1] << 16),
+                      (uint32_t)b[2] | ((uint32_t)b[3] << 16),
+                      (uint32_t)b[4] | ((uint32_t)b[5] << 16),
+                      (uint32_t)b[6] | ((uint32_t)b[7] << 16));
 }
 
 __device__ __forceinline__ uint16_t pack_bits(const uint16_t (&b)[1]) { return b[0]; }
@@ -109,10 +94,17 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b)
+// The same add rounded toward -inf (rm) and toward +inf (rp).
+__device__ __forceinline__ uint64_t add2_rm(uint64_t a, uint64_t b)
 {
     uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2_rp(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rp.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
@@ -125,12 +117,6 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
 {
     uint32_t r;
     asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b)
-{
-    uint32_t r;
-    asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 // a0 += bf16 lo half of w, a1 += bf16 hi half (each one fp32 rounding, the
@@ -247,20 +233,59 @@ __device__ __forceinline__ void walk_ranks2(const uint4 (&r)[KM], const float (&
     }
 }
 
+// Element e of a vector as fp32 (exact).
+__device__ __forceinline__ float elem(const uint4 &v, int e)
+{
+    const uint32_t w = e < 2 ? v.x : (e < 4 ? v.y : (e < 6 ? v.z : v.w));
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+__device__ __forceinline__ float elem(uint16_t v, int)
+{
+    return __uint_as_float((uint32_t)v << 16);
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float x)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// The fp64 cross-rank combine of element e by its definition: per rank the
+// slot-order fp32 chain from +0 (rounded to bf16 if BF16P), the partials added
+// in rank order to an fp64 sum from +0, rounded once to bf16.
+template <bool PROBS, bool BF16P, int KM, typename V>
+__device__ __forceinline__ uint16_t rank_sum_f64(const V (&r)[KM], const float (&p)[KM],
+                                                 unsigned valid, unsigned last, int e)
+{
+    double acc = 0.0;
+    float part = 0.0f;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        if (!(valid >> j & 1u)) continue;
+        const float f = elem(r[j], e);
+        part = PROBS ? __fmaf_rn(p[j], f, part) : __fadd_rn(part, f);
+        if (last >> j & 1u) {
+            const float q = BF16P ? __bfloat162float(__float2bfloat16_rn(part)) : part;
+            acc = __dadd_rn(acc, (double)q);
+            part = 0.0f;
+        }
+    }
+    return bf16_from_f64(acc);
+}
+
 // CTAs per SM each variant is compiled for (registers are capped to fit).
 // Measured on the skewed T=16384, ep=8 combine: occupancy outweighs the
 // registers it spills (fp32 215 -> 187 us at 7 CTAs, bf16 partials 243 ->
 // 199 us); the fp64 forms, which also prefetch their next pass into L2, are
-// best at 5 (bf16 partials, 242 us) and 4 (fp32 partials, 300 us).
+// best at 5 (bf16 partials 217 us, fp32 partials 208 us; 4 and 6 were slower).
 // With up to 16 slots a thread holds twice the rows: 2 CTAs per SM (rare
 // shapes; correctness first).
-constexpr int ep_min_blocks(bool fp64, bool bf16p, int km)
+constexpr int ep_min_blocks(bool fp64, int km)
 {
-    return km > 8 ? 2 : (fp64 ? (bf16p ? 5 : 4) : 7);
+    return km > 8 ? 2 : (fp64 ? 5 : 7);
 }
 
 template <typename V, bool PROBS, bool BF16P, bool FP64, int KM>
-__global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P, KM))
+__global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, KM))
     k_unpermute_ep(const V *__restrict__ rows, const float *__restrict__ probs,
                    const int32_t *__restrict__ map, const int32_t *__restrict__ idx, int64_t T,
                    int K, int nvec, int tpt_log2, int per_rank, V *__restrict__ out)
@@ -315,192 +340,76 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, BF16P, KM))
                                  ::"l"(rows + (int64_t)rk[i] * nvec + cn));
         }
         if constexpr (FP64) {
-            // Exact cross-rank sum, then one rounding to bf16.  The partials
-            // are bf16 (BF16P) or fp32 values, each a multiple of its own
-            // quantum, and the smallest nonzero magnitude m has the smallest
-            // quantum q, with q > m / 2^8 (bf16) or m / 2^24 (fp32).  With
-            // a = the fp32 sum of |partial| (within 2^-20 of the exact one):
-            //  * bf16 partials, a <= 2^15 m: every running sum is a multiple
-            //    of q below 2^24 q, so plain fp32 adds are exact;
-            //  * a <= 2^36 m (bf16) or 2^20 m (fp32): TwoSum makes each add's
-            //    error exact, the errors (multiples of q, together below
-            //    2^24 q) add up exactly, and hi + lo is the exact sum;
-            //  * otherwise (or a > 2^120, inf, NaN): fp64 additions in rank
-            //    order, the definition itself.
-            // In the first two cases every running sum has at most 45
-            // significant bits, so the fp64 additions are exact as well and
-            // all three give the same bits.  On 16-byte vectors the partials
-            // are formed and added as packed fp32 pairs; with bf16 partials
-            // the bound uses 8 * the largest |partial| (at most 8 ranks) in
-            // place of a, from integer max / min of the bf16 magnitudes.
-            constexpr float TIER2 = BF16P ? 0x1p36f : 0x1p20f;
+            // The fp64 cross-rank sum, rounded once to bf16, without fp64
+            // arithmetic on the common path.  The partials are summed in rank
+            // order twice in fp32, every add rounded toward -inf (lo) and
+            // toward +inf (hi).  Then lo <= s <= hi for the fp64 sum s, by
+            // induction over the adds: a float rounded down (up) from x is an
+            // fp64 value <= x (>= x), so rounding x to the nearest fp64 value
+            // cannot pass it.  Rounding to bf16 is monotone, so where lo and hi
+            // round to the same bf16 value, and it is not NaN, that is the bf16
+            // of s.  An element whose bracket holds a bf16 midpoint (about 1 in
+            // 10^4 on N(0,1) rows), or that cancels exactly (lo = -0 where s is
+            // +0), or meets inf or NaN, takes the definition itself: fp64 adds
+            // in rank order, per element.  On 16-byte vectors the walk runs on
+            // packed fp32 pairs.
             uint16_t bits[L];
-            unsigned pair = 0, dbl = 0;   // elements that take the pair / fp64 sum
-            float sa[L], sb[L], sm[L];
+            unsigned open = 0;   // elements whose bracket does not decide
+            if constexpr (L == 8) {
+                uint64_t lo2[4], hi2[4];
 #pragma unroll
-            for (int e = 0; e < L; ++e) {
-                sa[e] = 0.0f;
-                sb[e] = 0.0f;
-                sm[e] = __int_as_float(0x7f800000);
-            }
-            if constexpr (BF16P && L == 8) {
-                // Largest and smallest |partial| of each element as bf16 bit
-                // patterns (ordered like magnitudes; +inf bits start the
-                // minimum, NaN patterns exceed every finite one).  With at most
-                // 8 partials, sum |p| <= 8 max, so max <= 2^12 min implies the
-                // plain-add bound and max <= 2^33 min the pair bound.
-                uint32_t mx[4], mn[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    mx[i] = 0;
-                    mn[i] = 0x7f807f80u;
-                }
+                for (int i = 0; i < 4; ++i) lo2[i] = hi2[i] = 0;
                 walk_ranks2<PROBS, KM>(r, pk, valid, last, [&](int i, uint64_t p) {
-                    float lo, hi;
-                    f2_split(p, lo, hi);
-                    const uint32_t w = pack_bf16x2(lo, hi);
-                    add_bf16x2(w, sa[2 * i], sa[2 * i + 1]);
-                    const uint32_t a = w & 0x7fff7fffu;
-                    mx[i] = max_u16x2(mx[i], a);
-                    mn[i] = min_u16x2(mn[i], a);
+                    if constexpr (BF16P) {
+                        float lo, hi;
+                        f2_split(p, lo, hi);
+                        p = bf16x2_wide(pack_bf16x2(lo, hi));
+                    }
+                    lo2[i] = add2_rm(lo2[i], p);
+                    hi2[i] = add2_rp(hi2[i], p);
                 });
+                bool any = false;
+                uint32_t wl[4], wh[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float a0 = sa[2 * i], a1 = sa[2 * i + 1];
-                    const uint32_t wb = pack_bf16x2(a0, a1);
-                    bits[2 * i] = static_cast<uint16_t>(wb & 0xffffu);
-                    bits[2 * i + 1] = static_cast<uint16_t>(wb >> 16);
-                    const float hx[2] = {bf16_lo(mx[i]), bf16_hi(mx[i])};
-                    const float hn[2] = {bf16_lo(mn[i]), bf16_hi(mn[i])};
+                    float l0, l1, h0, h1;
+                    f2_split(lo2[i], l0, l1);
+                    f2_split(hi2[i], h0, h1);
+                    wl[i] = pack_bf16x2(l0, l1);
+                    wh[i] = pack_bf16x2(h0, h1);
+                    bits[2 * i] = static_cast<uint16_t>(wl[i] & 0xffffu);
+                    bits[2 * i + 1] = static_cast<uint16_t>(wl[i] >> 16);
+                    any |= wl[i] != wh[i] ||
+                           max_u16x2(wl[i] & 0x7fff7fffu, 0x7f807f80u) != 0x7f807f80u;
+                }
+                if (any) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const bool fin = hx[h] <= 0x1p120f;
-                        if (!(fin && hx[h] <= __fmul_rn(hn[h], 0x1p12f)))
-                            (fin && hx[h] <= __fmul_rn(hn[h], 0x1p33f) ? pair : dbl) |=
-                                1u << (2 * i + h);
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t a = (e & 1) ? wl[e / 2] >> 16 : wl[e / 2] & 0xffffu;
+                        const uint32_t b = (e & 1) ? wh[e / 2] >> 16 : wh[e / 2] & 0xffffu;
+                        if (a != b || (a & 0x7fffu) > 0x7f80u) open |= 1u << e;
                     }
                 }
-                if (pair) {
-#pragma unroll
-                    for (int e = 0; e < L; ++e) {
-                        sa[e] = 0.0f;
-                        sb[e] = 0.0f;
-                    }
-                    walk_ranks<PROBS, true, L, KM>(r, pk, valid, last, [&](int e, float p) {
-                        const float s = __fadd_rn(sa[e], p);
-                        const float bb = __fsub_rn(s, sa[e]);
-                        sb[e] = __fadd_rn(sb[e], __fadd_rn(__fsub_rn(sa[e], __fsub_rn(s, bb)),
-                                                           __fsub_rn(p, bb)));
-                        sa[e] = s;
-                    });
-#pragma unroll
-                    for (int e = 0; e < L; ++e)
-                        if (pair >> e & 1u) bits[e] = bf16_from_pair(sa[e], sb[e]);
-                }
-            } else if (BF16P) {
-                walk_ranks<PROBS, true, L, KM>(r, pk, valid, last, [&](int e, float p) {
-                    sa[e] = __fadd_rn(sa[e], p);
-                    sb[e] = __fadd_rn(sb[e], fabsf(p));
-                    sm[e] = fminf(sm[e], fabsf(p));
-                });
-#pragma unroll
-                for (int e = 0; e < L; ++e) {
-                    __nv_bfloat16 h = __float2bfloat16_rn(sa[e]);
-                    bits[e] = *reinterpret_cast<uint16_t *>(&h);
-                    const bool fin = sb[e] <= 0x1p120f;
-                    if (!(fin && sb[e] <= __fmul_rn(sm[e], 0x1p15f)))
-                        (fin && sb[e] <= __fmul_rn(sm[e], TIER2) ? pair : dbl) |= 1u << e;
-                }
-                if (pair) {
-#pragma unroll
-                    for (int e = 0; e < L; ++e) {
-                        sa[e] = 0.0f;
-                        sb[e] = 0.0f;
-                    }
-                    walk_ranks<PROBS, true, L, KM>(r, pk, valid, last, [&](int e, float p) {
-                        const float s = __fadd_rn(sa[e], p);
-                        const float bb = __fsub_rn(s, sa[e]);
-                        sb[e] = __fadd_rn(sb[e], __fadd_rn(__fsub_rn(sa[e], __fsub_rn(s, bb)),
-                                                           __fsub_rn(p, bb)));
-                        sa[e] = s;
-                    });
-#pragma unroll
-                    for (int e = 0; e < L; ++e)
-                        if (pair >> e & 1u) bits[e] = bf16_from_pair(sa[e], sb[e]);
-                }
-            } else if constexpr (L == 8) {
-                uint64_t sa2[4], sl2[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) sa2[i] = sl2[i] = 0;
-                walk_ranks2<PROBS, KM>(r, pk, valid, last, [&](int i, uint64_t p) {
-                    const uint64_t s2 = add2(sa2[i], p);
-                    const uint64_t bb = sub2(s2, sa2[i]);
-                    sl2[i] = add2(sl2[i], add2(sub2(sa2[i], sub2(s2, bb)), sub2(p, bb)));
-                    sa2[i] = s2;
-                    float lo, hi;
-                    f2_split(p, lo, hi);
-                    sb[2 * i] = __fadd_rn(sb[2 * i], fabsf(lo));
-                    sb[2 * i + 1] = __fadd_rn(sb[2 * i + 1], fabsf(hi));
-                    sm[2 * i] = fminf(sm[2 * i], fabsf(lo));
-                    sm[2 * i + 1] = fminf(sm[2 * i + 1], fabsf(hi));
-                });
-                // hi = fl(sa + sl) rounds to the same bf16 as the exact sum
-                // unless it lies exactly halfway between two bf16 values (the
-                // midpoints are fp32 values, so a first rounding cannot cross
-                // one); only then is the pair's error needed.
-                unsigned tie = 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float h0, h1;
-                    f2_split(add2(sa2[i], sl2[i]), h0, h1);
-                    const uint32_t wb = pack_bf16x2(h0, h1);
-                    bits[2 * i] = static_cast<uint16_t>(wb & 0xffffu);
-                    bits[2 * i + 1] = static_cast<uint16_t>(wb >> 16);
-                    tie |= ((__float_as_uint(h0) & 0xffffu) == 0x8000u ? 1u : 0u) << (2 * i);
-                    tie |= ((__float_as_uint(h1) & 0xffffu) == 0x8000u ? 1u : 0u) << (2 * i + 1);
-                }
-                if (tie) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float a0, a1, l0, l1;
-                        f2_split(sa2[i], a0, a1);
-                        f2_split(sl2[i], l0, l1);
-                        if (tie >> (2 * i) & 1u) bits[2 * i] = bf16_from_pair(a0, l0);
-                        if (tie >> (2 * i + 1) & 1u) bits[2 * i + 1] = bf16_from_pair(a1, l1);
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < L; ++e)
-                    if (!(sb[e] <= 0x1p120f && sb[e] <= __fmul_rn(sm[e], TIER2))) dbl |= 1u << e;
             } else {
-                float sl[L];
+                float lo[L], hi[L];
 #pragma unroll
-                for (int e = 0; e < L; ++e) sl[e] = 0.0f;
-                walk_ranks<PROBS, false, L, KM>(r, pk, valid, last, [&](int e, float p) {
-                    const float s = __fadd_rn(sa[e], p);
-                    const float bb = __fsub_rn(s, sa[e]);
-                    sl[e] = __fadd_rn(sl[e], __fadd_rn(__fsub_rn(sa[e], __fsub_rn(s, bb)),
-                                                       __fsub_rn(p, bb)));
-                    sa[e] = s;
-                    sb[e] = __fadd_rn(sb[e], fabsf(p));
-                    sm[e] = fminf(sm[e], fabsf(p));
+                for (int e = 0; e < L; ++e) lo[e] = hi[e] = 0.0f;
+                walk_ranks<PROBS, BF16P, L, KM>(r, pk, valid, last, [&](int e, float p) {
+                    lo[e] = __fadd_rd(lo[e], p);
+                    hi[e] = __fadd_ru(hi[e], p);
                 });
 #pragma unroll
                 for (int e = 0; e < L; ++e) {
-                    bits[e] = bf16_from_pair(sa[e], sl[e]);
-                    if (!(sb[e] <= 0x1p120f && sb[e] <= __fmul_rn(sm[e], TIER2))) dbl |= 1u << e;
+                    const uint32_t a = bf16_bits(lo[e]), b = bf16_bits(hi[e]);
+                    bits[e] = static_cast<uint16_t>(a);
+                    if (a != b || (a & 0x7fffu) > 0x7f80u) open |= 1u << e;
                 }
             }
-            if (dbl) {
-                double acc[L];
-#pragma unroll
-                for (int e = 0; e < L; ++e) acc[e] = 0.0;
-                walk_ranks<PROBS, BF16P, L, KM>(r, pk, valid, last, [&](int e, float p) {
-                    acc[e] = __dadd_rn(acc[e], (double)p);
-                });
+            if (open) {
 #pragma unroll
                 for (int e = 0; e < L; ++e)
-                    if (dbl >> e & 1u) bits[e] = bf16_from_f64(acc[e]);
+                    if (open >> e & 1u)
+                        bits[e] = rank_sum_f64<PROBS, BF16P, KM>(r, pk, valid, last, e);
             }
             if (c < nvec) st_row(out + t * nvec + c, pack_bits(bits));
         } else {
