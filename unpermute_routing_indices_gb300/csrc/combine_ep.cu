@@ -37,6 +37,7 @@ namespace {
 constexpr int EP_THREADS = 128;
 constexpr int EP_KMAX = 16;   // slots per token: kernels for K <= 8 and for K <= 16
 
+
 // fp64 -> bf16, round to nearest even, in a single rounding, from the binary64
 // fields: keep the top 8 significant bits (1 + 7) for normal bf16 results, or
 // the bits at or above the 2^-133 quantum for subnormal ones; a carry out of
@@ -181,9 +182,9 @@ __device__ __forceinline__ void sort_slots(int32_t (&k)[N], int32_t (&r)[N], flo
 // multiply-adds (plain adds without probs) from +0 per rank, and add(e, p) at
 // each rank's last slot with the rank's partial p for element e (rounded to
 // bf16 if BF16P).  `valid` / `last` are bit masks over the sorted positions.
-template <bool PROBS, bool BF16P, int L, int KM, typename V, typename Add>
-__device__ __forceinline__ void walk_ranks(const V (&r)[KM], const float (&p)[KM],
-                                           unsigned valid, unsigned last, Add add)
+template <bool PROBS, bool BF16P, int L, int KM, typename Get, typename Add>
+__device__ __forceinline__ void walk_ranks(Get row, const float (&p)[KM], unsigned valid,
+                                           unsigned last, Add add)
 {
     float part[L];
 #pragma unroll
@@ -192,7 +193,7 @@ __device__ __forceinline__ void walk_ranks(const V (&r)[KM], const float (&p)[KM
     for (int j = 0; j < KM; ++j) {
         if (!(valid >> j & 1u)) continue;
         float f[L];
-        unpack(r[j], f);
+        unpack(row(j), f);
 #pragma unroll
         for (int e = 0; e < L; ++e)
             part[e] = PROBS ? __fmaf_rn(p[j], f[e], part[e]) : __fadd_rn(part[e], f[e]);
@@ -206,10 +207,11 @@ __device__ __forceinline__ void walk_ranks(const V (&r)[KM], const float (&p)[KM
     }
 }
 
-// walk_ranks on packed pairs: the four element pairs of a 16-byte vector.
-template <bool PROBS, int KM, typename Add>
-__device__ __forceinline__ void walk_ranks2(const uint4 (&r)[KM], const float (&p)[KM],
-                                            unsigned valid, unsigned last, Add add)
+// walk_ranks on packed pairs: the four element pairs of a 16-byte vector;
+// row(j) gives the vector of sorted slot j.
+template <bool PROBS, int KM, typename Get, typename Add>
+__device__ __forceinline__ void walk_ranks2(Get row, const float (&p)[KM], unsigned valid,
+                                            unsigned last, Add add)
 {
     uint64_t part[4];
 #pragma unroll
@@ -217,7 +219,8 @@ __device__ __forceinline__ void walk_ranks2(const uint4 (&r)[KM], const float (&
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
         if (!(valid >> j & 1u)) continue;
-        const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+        const uint4 v = row(j);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         const uint64_t pp = f2(p[j], p[j]);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -231,6 +234,11 @@ __device__ __forceinline__ void walk_ranks2(const uint4 (&r)[KM], const float (&
             }
         }
     }
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 // Element e of a vector as fp32 (exact).
@@ -252,16 +260,16 @@ __device__ __forceinline__ uint32_t bf16_bits(float x)
 // The fp64 cross-rank combine of element e by its definition: per rank the
 // slot-order fp32 chain from +0 (rounded to bf16 if BF16P), the partials added
 // in rank order to an fp64 sum from +0, rounded once to bf16.
-template <bool PROBS, bool BF16P, int KM, typename V>
-__device__ __forceinline__ uint16_t rank_sum_f64(const V (&r)[KM], const float (&p)[KM],
-                                                 unsigned valid, unsigned last, int e)
+template <bool PROBS, bool BF16P, int KM, typename Get>
+__device__ __forceinline__ uint16_t rank_sum_f64(Get row, const float (&p)[KM], unsigned valid,
+                                                 unsigned last, int e)
 {
     double acc = 0.0;
     float part = 0.0f;
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
         if (!(valid >> j & 1u)) continue;
-        const float f = elem(r[j], e);
+        const float f = elem(row(j), e);
         part = PROBS ? __fmaf_rn(p[j], f, part) : __fadd_rn(part, f);
         if (last >> j & 1u) {
             const float q = BF16P ? __bfloat162float(__float2bfloat16_rn(part)) : part;
@@ -272,20 +280,24 @@ __device__ __forceinline__ uint16_t rank_sum_f64(const V (&r)[KM], const float (
     return bf16_from_f64(acc);
 }
 
-// CTAs per SM each variant is compiled for (registers are capped to fit).
-// Measured on the skewed T=16384, ep=8 combine: occupancy outweighs the
-// registers it spills (fp32 215 -> 187 us at 7 CTAs, bf16 partials 243 ->
-// 199 us); the fp64 forms, which also prefetch their next pass into L2, are
-// best at 5 (bf16 partials 217 us, fp32 partials 208 us; 4 and 6 were slower).
-// With up to 16 slots a thread holds twice the rows: 2 CTAs per SM (rare
-// shapes; correctness first).
-constexpr int ep_min_blocks(bool fp64, int km)
+// Shared memory a CTA stages its rows in: on 16-byte vectors, KM slots x
+// EP_THREADS vectors per buffer, two buffers for K <= 8 and one for K <= 16.
+__host__ __device__ constexpr int ep_stage_bufs(int km) { return km > 8 ? 1 : 2; }
+template <typename V, int KM>
+constexpr size_t ep_stage_bytes()
 {
-    return km > 8 ? 2 : (fp64 ? 5 : 7);
+    return Lanes<V>::N == 8 ? (size_t)ep_stage_bufs(KM) * KM * EP_THREADS * 16 : 0;
 }
 
+// CTAs per SM each variant is compiled for (registers are capped to fit; the
+// two 16 KB stage buffers allow 6).  Measured on the skewed T=16384, ep=8
+// combine with the rows staged: 6 CTAs give fp32 174 us, bf16 partials 183,
+// fp64 sum 194 (fp32 partials) / 197 (bf16 partials); 5 CTAs the same within
+// 1%.  With up to 16 slots: 2 CTAs per SM (rare shapes; correctness first).
+constexpr int ep_min_blocks(int km) { return km > 8 ? 2 : 6; }
+
 template <typename V, bool PROBS, bool BF16P, bool FP64, int KM>
-__global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, KM))
+__global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(KM))
     k_unpermute_ep(const V *__restrict__ rows, const float *__restrict__ probs,
                    const int32_t *__restrict__ map, const int32_t *__restrict__ idx, int64_t T,
                    int K, int nvec, int tpt_log2, int per_rank, V *__restrict__ out)
@@ -322,16 +334,57 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, KM))
                                    (key[j] - (key[j] & (KM - 1)));
         if (!next_same) last |= 1u << j;
     }
-    for (int c0 = 0; c0 < nvec; c0 += tpt) {
-        const int c = c0 + lane;
-        V r[KM];
+    // On 16-byte vectors each pass's rows are staged in shared memory
+    // (cp.async, 16 bytes per copy) instead of registers, two passes deep:
+    // the copies of pass p + 1 are issued before pass p is computed.  Each
+    // thread copies and reads back only its own slots, so no barrier is
+    // needed; the registers the rows would hold go to more resident warps.
+    constexpr bool STAGE = L == 8;
+    constexpr int NBUF = STAGE ? ep_stage_bufs(KM) : 1;
+    extern __shared__ uint4 ep_stage[];   // [NBUF][KM][EP_THREADS] when STAGE
+    const auto issue = [&](int cc, int buf) {
+        uint4 *const dst = ep_stage + buf * KM * EP_THREADS + threadIdx.x;
 #pragma unroll
         for (int i = 0; i < KM; ++i)
-            r[i] = ((valid >> i & 1u) && c < nvec) ? ld_stream(rows + (int64_t)rk[i] * nvec + c)
-                                                   : zero_vec<V>();
-        if constexpr (FP64) {
-            // the fp64 forms compute long enough per pass to hide an L2 fill
-            // of the next pass's rows behind it
+            if (valid >> i & 1u)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                             ::"r"(smem_u32(dst + i * EP_THREADS)),
+                               "l"(rows + (int64_t)rk[i] * nvec + cc)
+                             : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if constexpr (STAGE && NBUF == 2)
+        if (lane < nvec) issue(lane, 0);
+    int pass = 0;
+    for (int c0 = 0; c0 < nvec; c0 += tpt, ++pass) {
+        const int c = c0 + lane;
+        V r[KM];
+        if constexpr (STAGE) {
+            if (c >= nvec) break;
+            if constexpr (NBUF == 2) {
+                if (c + tpt < nvec) {
+                    issue(c + tpt, (pass + 1) & 1);
+                    asm volatile("cp.async.wait_group 1;" ::: "memory");
+                } else {
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                }
+            } else {
+                issue(c, 0);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < KM; ++i)
+                r[i] = ((valid >> i & 1u) && c < nvec)
+                           ? ld_stream(rows + (int64_t)rk[i] * nvec + c) : zero_vec<V>();
+        }
+        uint4 *const mine = ep_stage + (pass & (NBUF - 1)) * KM * EP_THREADS + threadIdx.x;
+        const auto row = [&](int j) -> V {
+            if constexpr (STAGE) return mine[j * EP_THREADS];
+            else return r[j];
+        };
+        if constexpr (FP64 && NBUF == 1) {
+            // the fp64 forms without a second stage buffer compute long
+            // enough per pass to hide an L2 fill of the next pass's rows
             const int cn = c + tpt;
 #pragma unroll
             for (int i = 0; i < KM; ++i)
@@ -339,6 +392,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, KM))
                     asm volatile("prefetch.global.L2 [%0];"
                                  ::"l"(rows + (int64_t)rk[i] * nvec + cn));
         }
+        if constexpr (STAGE && NBUF == 1) asm volatile("cp.async.wait_group 0;" ::: "memory");
         if constexpr (FP64) {
             // The fp64 cross-rank sum, rounded once to bf16, without fp64
             // arithmetic on the common path.  The partials are summed in rank
@@ -359,7 +413,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, KM))
                 uint64_t lo2[4], hi2[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) lo2[i] = hi2[i] = 0;
-                walk_ranks2<PROBS, KM>(r, pk, valid, last, [&](int i, uint64_t p) {
+                walk_ranks2<PROBS, KM>(row, pk, valid, last, [&](int i, uint64_t p) {
                     if constexpr (BF16P) {
                         float lo, hi;
                         f2_split(p, lo, hi);
@@ -394,7 +448,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, KM))
                 float lo[L], hi[L];
 #pragma unroll
                 for (int e = 0; e < L; ++e) lo[e] = hi[e] = 0.0f;
-                walk_ranks<PROBS, BF16P, L, KM>(r, pk, valid, last, [&](int e, float p) {
+                walk_ranks<PROBS, BF16P, L, KM>(row, pk, valid, last, [&](int e, float p) {
                     lo[e] = __fadd_rd(lo[e], p);
                     hi[e] = __fadd_ru(hi[e], p);
                 });
@@ -409,7 +463,7 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, KM))
 #pragma unroll
                 for (int e = 0; e < L; ++e)
                     if (open >> e & 1u)
-                        bits[e] = rank_sum_f64<PROBS, BF16P, KM>(r, pk, valid, last, e);
+                        bits[e] = rank_sum_f64<PROBS, BF16P, KM>(row, pk, valid, last, e);
             }
             if (c < nvec) st_row(out + t * nvec + c, pack_bits(bits));
         } else {
@@ -417,13 +471,13 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(FP64, KM))
 #pragma unroll
             for (int e = 0; e < L; ++e) acc[e] = 0.0f;
             if constexpr (BF16P && L == 8) {
-                walk_ranks2<PROBS, KM>(r, pk, valid, last, [&](int i, uint64_t p) {
+                walk_ranks2<PROBS, KM>(row, pk, valid, last, [&](int i, uint64_t p) {
                     float lo, hi;
                     f2_split(p, lo, hi);
                     add_bf16x2(pack_bf16x2(lo, hi), acc[2 * i], acc[2 * i + 1]);
                 });
             } else {
-                walk_ranks<PROBS, BF16P, L, KM>(r, pk, valid, last,
+                walk_ranks<PROBS, BF16P, L, KM>(row, pk, valid, last,
                                             [&](int e, float p) { acc[e] = __fadd_rn(acc[e], p); });
             }
             if (c < nvec) st_row(out + t * nvec + c, pack(acc));
@@ -440,7 +494,8 @@ void launch_ep(const void *rows, const float *probs, const int32_t *map, const i
     if (l > lmax) l = lmax;
     const int64_t per_block = EP_THREADS >> l;
     const unsigned blocks = (unsigned)((T + per_block - 1) / per_block);
-    (void)launch_pdl(k_unpermute_ep<V, PROBS, BF16P, FP64, KM>, blocks, EP_THREADS, 0, s,
+    const size_t smem = ep_stage_bytes<V, KM>();
+    (void)launch_pdl(k_unpermute_ep<V, PROBS, BF16P, FP64, KM>, blocks, EP_THREADS, smem, s,
         (const V *)rows, probs, map, idx, T, K, nvec, l, per_rank, (V *)out);
 }
 
