@@ -254,6 +254,174 @@ __global__ void __launch_bounds__(ROW_THREADS)
     }
 }
 
+// Staged forms (16-byte vectors, one vector per thread per pass, K <= KB).
+// Each thread copies its own slots' row vectors (and, backward, g_y's) into
+// shared memory with cp.async and reads back only those, so no barrier is
+// needed.  Two buffers keep a pass ahead: the copies for pass p + 1 are issued
+// before pass p is computed, so the rows hold no registers while in flight
+// and twice as many bytes are requested per thread.  Same arithmetic, in the
+// same order, as k_unpermute / k_unpermute_bwd.
+constexpr int STAGE_BUFS = 2;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))), "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <bool PROBS, bool GATHER_PROBS>
+__global__ void __launch_bounds__(ROW_THREADS)
+    k_unpermute_staged(const uint4 *__restrict__ rows, const float *__restrict__ probs,
+                       const int32_t *__restrict__ map, int64_t T, int K, int nvec,
+                       int tpt_log2, uint4 *__restrict__ out,
+                       const float *__restrict__ g_out_probs, float *__restrict__ g_probs)
+{
+    pdl_trigger();
+    pdl_wait();
+    extern __shared__ uint4 row_stage[];   // [STAGE_BUFS][KB][ROW_THREADS]
+    const int tpt = 1 << tpt_log2;
+    const int lane = threadIdx.x & (tpt - 1);
+    const int64_t t = (int64_t)blockIdx.x * (ROW_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
+    if (t >= T) return;
+    const int32_t *m = map + t * K;
+    int32_t rk[KB];
+    float pk[KB];
+#pragma unroll
+    for (int i = 0; i < KB; ++i) {
+        rk[i] = (i < K) ? __ldg(m + i) : -1;
+        pk[i] = (PROBS && i < K) ? __ldg(probs + t * K + i) : 1.0f;
+    }
+    const auto issue = [&](int c, int buf) {
+        uint4 *const dst = row_stage + buf * KB * ROW_THREADS + threadIdx.x;
+#pragma unroll
+        for (int i = 0; i < KB; ++i)
+            if (rk[i] >= 0) cp_async16(dst + i * ROW_THREADS, rows + (int64_t)rk[i] * nvec + c);
+        cp_async_commit();
+    };
+    if (lane < nvec) issue(lane, 0);
+    int pass = 0;
+    for (int c = lane; c < nvec; c += tpt, ++pass) {
+        if (c + tpt < nvec) {
+            issue(c + tpt, (pass + 1) & 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        const uint4 *const mine = row_stage + (pass & 1) * KB * ROW_THREADS + threadIdx.x;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < KB; ++i) {
+            if (rk[i] < 0) continue;
+            float f[8];
+            unpack(mine[i * ROW_THREADS], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[e] = PROBS ? __fmaf_rn(pk[i], f[e], acc[e]) : __fadd_rn(acc[e], f[e]);
+        }
+        st_row(out + t * nvec + c, pack(acc));
+    }
+    if (GATHER_PROBS && lane == 0) {
+        for (int k = 0; k < K; ++k) {
+            const int32_t row = __ldg(m + k);
+            g_probs[t * K + k] = row >= 0 ? __ldg(g_out_probs + row) : 0.0f;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(ROW_THREADS)
+    k_unpermute_bwd_staged(const uint4 *__restrict__ gy, const uint4 *__restrict__ rows,
+                           const float *__restrict__ probs, const int32_t *__restrict__ map,
+                           int64_t T, int K, int nvec, int tpt_log2,
+                           uint4 *__restrict__ g_rows, float *__restrict__ g_probs)
+{
+    pdl_trigger();
+    pdl_wait();
+    extern __shared__ uint4 row_stage[];   // [STAGE_BUFS][KB + 1][ROW_THREADS]; slot KB: g_y
+    __shared__ float s_red[ROW_THREADS / 32][KB];
+    const int tpt = 1 << tpt_log2;
+    const int lane = threadIdx.x & (tpt - 1);
+    const int64_t t = (int64_t)blockIdx.x * (ROW_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
+    const bool active = t < T;
+    const int32_t *m = map + t * K;
+    int32_t rk[KB];
+    float pk[KB], dot[KB];
+#pragma unroll
+    for (int i = 0; i < KB; ++i) {
+        rk[i] = (active && i < K) ? __ldg(m + i) : -1;
+        pk[i] = (active && i < K) ? __ldg(probs + t * K + i) : 0.0f;
+        dot[i] = 0.0f;
+    }
+    const auto issue = [&](int c, int buf) {
+        uint4 *const dst = row_stage + buf * (KB + 1) * ROW_THREADS + threadIdx.x;
+        cp_async16(dst + KB * ROW_THREADS, gy + t * nvec + c);
+#pragma unroll
+        for (int i = 0; i < KB; ++i)
+            if (rk[i] >= 0) cp_async16(dst + i * ROW_THREADS, rows + (int64_t)rk[i] * nvec + c);
+        cp_async_commit();
+    };
+    if (active) {
+        if (lane < nvec) issue(lane, 0);
+        int pass = 0;
+        for (int c = lane; c < nvec; c += tpt, ++pass) {
+            if (c + tpt < nvec) {
+                issue(c + tpt, (pass + 1) & 1);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            const uint4 *const mine = row_stage + (pass & 1) * (KB + 1) * ROW_THREADS + threadIdx.x;
+            float gf[8];
+            unpack(mine[KB * ROW_THREADS], gf);
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                if (rk[i] < 0) continue;
+                float rf[8], o[8];
+                unpack(mine[i * ROW_THREADS], rf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    o[e] = __fmul_rn(pk[i], gf[e]);
+                    dot[i] = __fmaf_rn(rf[e], gf[e], dot[i]);
+                }
+                st_row(g_rows + (int64_t)rk[i] * nvec + c, pack(o));
+            }
+        }
+    }
+    // Each slot's partial reduced over the token's threads, as in k_unpermute_bwd.
+    const int width = tpt < 32 ? tpt : 32;
+#pragma unroll
+    for (int i = 0; i < KB; ++i)
+        for (int o = width >> 1; o > 0; o >>= 1) dot[i] += __shfl_xor_sync(FULL_MASK, dot[i], o);
+    if (tpt > 32) {
+        const int warp = threadIdx.x >> 5;
+        if ((threadIdx.x & 31) == 0)
+#pragma unroll
+            for (int i = 0; i < KB; ++i) s_red[warp][i] = dot[i];
+        __syncthreads();
+        if (active && lane == 0) {
+            const int w0 = warp, nw = tpt >> 5;
+            for (int i = 0; i < KB && i < K; ++i) {
+                float s = 0.0f;
+                for (int w = 0; w < nw; ++w) s += s_red[w0 + w][i];
+                g_probs[t * K + i] = rk[i] >= 0 ? s : 0.0f;
+            }
+        }
+    } else if (active && lane == 0) {
+        for (int i = 0; i < KB && i < K; ++i) g_probs[t * K + i] = rk[i] >= 0 ? dot[i] : 0.0f;
+    }
+}
+
 inline bool rows_ok(int64_t T, int32_t K, int32_t H)
 {
     return T >= 0 && K >= 1 && H >= 1 && T * (int64_t)K <= INT32_MAX;
@@ -291,6 +459,24 @@ void launch_unpermute(const void *rows, const float *probs, const int32_t *map, 
                       cudaStream_t s)
 {
     const RowGrid g = row_grid(T, nvec, VPT);
+    if constexpr (Lanes<V>::N == 8 && VPT == 1) {
+        if (K <= KB) {
+            const size_t smem = (size_t)STAGE_BUFS * KB * ROW_THREADS * sizeof(uint4);
+            if (probs != nullptr)
+                (void)launch_pdl(k_unpermute_staged<true, false>, g.blocks, ROW_THREADS, smem, s,
+                    (const uint4 *)rows, probs, map, T, K, nvec, g.tpt_log2, (uint4 *)out,
+                    nullptr, nullptr);
+            else if (g_probs != nullptr)
+                (void)launch_pdl(k_unpermute_staged<false, true>, g.blocks, ROW_THREADS, smem, s,
+                    (const uint4 *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (uint4 *)out,
+                    g_out_probs, g_probs);
+            else
+                (void)launch_pdl(k_unpermute_staged<false, false>, g.blocks, ROW_THREADS, smem,
+                    s, (const uint4 *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (uint4 *)out,
+                    nullptr, nullptr);
+            return;
+        }
+    }
     if (probs != nullptr)
         (void)launch_pdl(k_unpermute<V, VPT, true, false>, g.blocks, ROW_THREADS, 0, s,
             (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr, nullptr);
@@ -309,6 +495,15 @@ void launch_unpermute_bwd(const void *gy, const void *rows, const float *probs,
                           float *g_probs, cudaStream_t s)
 {
     const RowGrid g = row_grid(T, nvec, VPT);
+    if constexpr (Lanes<V>::N == 8 && VPT == 1) {
+        if (K <= KB) {
+            const size_t smem = (size_t)STAGE_BUFS * (KB + 1) * ROW_THREADS * sizeof(uint4);
+            (void)launch_pdl(k_unpermute_bwd_staged, g.blocks, ROW_THREADS, smem, s,
+                (const uint4 *)gy, (const uint4 *)rows, probs, map, T, K, nvec, g.tpt_log2,
+                (uint4 *)g_rows, g_probs);
+            return;
+        }
+    }
     (void)launch_pdl(k_unpermute_bwd<V, VPT>, g.blocks, ROW_THREADS, 0, s,
         (const V *)gy, (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)g_rows, g_probs);
 }
