@@ -53,9 +53,9 @@ FALLBACK_HBM_GBS = 6800.0
 # one ncu capture, keyed by op; valid only while the kernel source that was
 # profiled is unchanged (sha256 prefix of the .cu file and common.cuh).
 NCU_TRAFFIC = {
-    # one-pass capture of the full bench workload (dram__bytes_read.sum 1,209,086,464
-    # + dram__bytes_write.sum 1,019,160,576); profiles/traffic_skewed_T16384_row_kernels.md
-    "unpermute_bwd": {"bytes": 2228247040, "src": "c74e1463494b6d4d"},
+    # one-pass capture of the full bench workload (dram__bytes_read.sum 1,209,168,384
+    # + dram__bytes_write.sum 1,018,953,728); profiles/traffic_skewed_T16384_row_kernels.md
+    "unpermute_bwd": {"bytes": 2228122112, "src": "cd2151724846ad28"},
 }
 
 

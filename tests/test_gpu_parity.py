@@ -325,6 +325,42 @@ def test_full_size_sampled(name):
     np.testing.assert_array_equal(h(g_x)[sample], o_gx)
 
 
+def test_staged_row_kernels_full_compare():
+    """16,385 tokens, one per CTA (H = 1,032: 129 vectors, so a second pass
+    with one lane busy), make grids past 16,384 CTAs, which run the forms that
+    stage their rows in shared memory: unpermute, its backward and the permute
+    backward.  A tenth of the slots are unrouted.  Every output is compared
+    with the oracle in full."""
+    T, H = 16385, 1032
+    idx, probs, E = wl.routing("skewed", T=T)
+    K = idx.shape[1]
+    rng = np.random.default_rng(5)
+    idx = idx.copy()
+    idx[rng.random(idx.shape) < 0.1] = -1
+    rows = wl.random_rows(T * K, H, 21)
+    gy = wl.random_rows(T, H, 22)
+    rim, *_ = mp.mp_build_map(d(idx), E)
+    o_rim, _, _, o_offsets, _ = oracle.build_map(idx, E)
+    np.testing.assert_array_equal(h(rim), o_rim)
+    routed = int(o_offsets[-1])
+    dr, dp = d(rows), d(probs)
+
+    y = mp.mp_unpermute(dr, rim, dp)
+    np.testing.assert_array_equal(h(y), oracle.unpermute(rows, probs, o_rim, T, H))
+
+    g_rows, g_probs = mp.mp_unpermute_bwd(d(gy), rim, dr, dp)
+    o_grows, o_gp = oracle.unpermute_bwd(gy, rows, probs, o_rim)
+    np.testing.assert_array_equal(h(g_rows)[:routed], o_grows[:routed])
+    gp = h(g_probs).astype(np.float64)
+    for k in range(K):
+        bound = gprobs_bound(f32(rows)[np.maximum(o_rim[:, k], 0)], f32(gy), o_gp[:, k])
+        assert np.all(np.abs(gp[:, k] - o_gp[:, k]) <= bound)
+    assert np.all(gp[o_rim < 0] == 0)
+
+    g_x, _ = mp.mp_permute_bwd(dr, rim)
+    np.testing.assert_array_equal(h(g_x), oracle.permute_bwd(rows, None, o_rim, T, H)[0])
+
+
 def test_rows_past_int32_element_offsets():
     """T = 66,000 tokens, K = 8, H = 4,096: the permuted tensors hold 2.16e9
     elements, past 2^31, so row offsets must be formed in 64 bits.  All the

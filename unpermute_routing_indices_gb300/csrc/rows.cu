@@ -262,6 +262,17 @@ __global__ void __launch_bounds__(ROW_THREADS)
 // and twice as many bytes are requested per thread.  Same arithmetic, in the
 // same order, as k_unpermute / k_unpermute_bwd.
 constexpr int STAGE_BUFS = 2;
+// The staged forms run only on grids of at least this many CTAs, for the
+// gathers and the backward alike.  Their shared memory caps an SM at 6 CTAs
+// where the register forms run 7 (gathers) or 5 (backward).  On the skewed
+// fwd+bwd step (H=4096, one token per CTA) the staged kernels make the step
+// faster from 16,384 tokens (0.880 -> 0.870 ms; 32,768: 1.731 -> 1.695;
+// 65,536: 3.433 -> 3.350) and slower below (4,096: 0.231 -> 0.241 ms).  A
+// step that mixed register gathers with the staged backward was slower
+// than either, 0.899 ms at 16,384 tokens: the backward's early-launched
+// (programmatic dependent) CTAs hold the shared memory the gather's last
+// CTAs would have used.
+constexpr unsigned STAGE_MIN_BLOCKS = 16384;
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
 {
@@ -460,7 +471,7 @@ void launch_unpermute(const void *rows, const float *probs, const int32_t *map, 
 {
     const RowGrid g = row_grid(T, nvec, VPT);
     if constexpr (Lanes<V>::N == 8 && VPT == 1) {
-        if (K <= KB) {
+        if (K <= KB && g.blocks >= STAGE_MIN_BLOCKS) {
             const size_t smem = (size_t)STAGE_BUFS * KB * ROW_THREADS * sizeof(uint4);
             if (probs != nullptr)
                 (void)launch_pdl(k_unpermute_staged<true, false>, g.blocks, ROW_THREADS, smem, s,
@@ -496,7 +507,7 @@ void launch_unpermute_bwd(const void *gy, const void *rows, const float *probs,
 {
     const RowGrid g = row_grid(T, nvec, VPT);
     if constexpr (Lanes<V>::N == 8 && VPT == 1) {
-        if (K <= KB) {
+        if (K <= KB && g.blocks >= STAGE_MIN_BLOCKS) {
             const size_t smem = (size_t)STAGE_BUFS * (KB + 1) * ROW_THREADS * sizeof(uint4);
             (void)launch_pdl(k_unpermute_bwd_staged, g.blocks, ROW_THREADS, smem, s,
                 (const uint4 *)gy, (const uint4 *)rows, probs, map, T, K, nvec, g.tpt_log2,
