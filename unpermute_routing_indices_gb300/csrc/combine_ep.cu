@@ -12,10 +12,12 @@
 // k_unpermute_ep: one group of tpt threads per token, one 16-byte vector (8
 // elements) per thread per pass.  Each thread sorts the token's K (<= 8, or
 // <= 16 in a second form) slots by (rank, slot) once, with a fixed sorting
-// network on registers, then
-// per pass loads the rows in that order and runs one fused multiply-add chain
-// that hands the rank's partial to the cross-rank sum at each rank's last
-// slot: K FMAs per element whatever the number of ranks.  A rank with no
+// network on registers.  Per pass it copies its slots' row vectors into
+// shared memory (cp.async, the next pass in flight while this one computes;
+// the element path for odd H keeps them in registers), reads them back in
+// sorted order and runs one fused multiply-add chain that hands the rank's
+// partial to the cross-rank sum at each rank's last slot: K FMAs per element
+// whatever the number of ranks.  A rank with no
 // routed slot would add +0 to an accumulator that is never -0, so skipping it
 // changes no bit.  GB300 runs FP64 at a small fraction of its FP32 rate, so
 // the fp64 cross-rank forms bracket the fp64 sum between two fp32 sums
