@@ -58,3 +58,21 @@ def test_index_lists_every_summary():
     listed = set(re.findall(r"`([\w.]+\.md)`", index))
     present = {os.path.basename(p) for p in _summaries()}
     assert listed == present, (sorted(listed - present), sorted(present - listed))
+
+
+def test_traffic_figure_matches_its_summary():
+    """bench.py's recorded DRAM traffic of the dominant kernel is the figure
+    the traffic summary states."""
+    import importlib.util
+    import sys
+    spec = importlib.util.spec_from_file_location("bench_for_profiles",
+                                                  os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    argv, sys.argv = sys.argv, ["bench.py"]
+    try:
+        spec.loader.exec_module(bench)
+    finally:
+        sys.argv = argv
+    summary = open(os.path.join(PROFILES, "traffic_skewed_T16384_row_kernels.md")).read()
+    for rec in bench.NCU_TRAFFIC.values():
+        assert f"{rec['bytes']:,}" in summary
