@@ -50,13 +50,10 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-# one ncu capture, keyed by op; valid only while the kernel source that was
-# profiled is unchanged (sha256 prefix of the .cu file and common.cuh).
-NCU_TRAFFIC = {
-    # one-pass capture of the full bench workload (dram__bytes_read.sum 1,209,168,384
-    # + dram__bytes_write.sum 1,018,953,728); profiles/traffic_skewed_T16384_row_kernels.md
-    "unpermute_bwd": {"bytes": 2228122112, "src": "cd2151724846ad28"},
-}
+# one ncu capture of one launch of that kernel alone, keyed by (op, workload,
+# T); a figure counts only while the profiled kernel source is unchanged
+# (sha256 prefix of its .cu file and common.cuh).  No matching capture: null.
+NCU_TRAFFIC = {}
 
 
 # --------------------------------------------------------------------------
@@ -507,7 +504,7 @@ def run_gpu(args):
     dom = max(ops, key=lambda o: per_op[o])
     dom_src = {"build_map": "map.cu"}.get(dom, "rows.cu")
     traffic = None
-    tr = NCU_TRAFFIC.get(dom)
+    tr = NCU_TRAFFIC.get((dom, WORKLOAD, T))
     if tr is not None and tr["src"] == src_hash(dom_src):
         traffic = tr["bytes"]
     achieved = nbytes[dom] / (per_op[dom] * 1e-3) / 1e9
@@ -648,6 +645,16 @@ def run_gpu(args):
         call("build_map")
         call("permute")
 
+    # ---- the other routed workloads at full size (mid: T=4096, H=2048, E=64,
+    # K=6; large: T=32768, H=7168, E=256, K=8; whichever is not the headline)
+    workloads = {}
+    if rank == 0 and not args.no_extras:
+        for name in ("mid", "skewed", "large"):
+            if name != WORKLOAD:
+                workloads[name] = bench_routed(mp, wl, name, dev, flush,
+                                               max(20, min(args.steps, 100)), peak)
+                torch.cuda.empty_cache()
+
     out = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -695,6 +702,8 @@ def run_gpu(args):
         out["sort_pad_roundtrip"] = sort_pad
     if extras:
         out["extras"] = extras
+    if workloads:
+        out["extras"]["workloads"] = workloads
     if rank == 0 and not args.no_cpu:
         v, it, dt, sample = oracle_step_rate(args.cpu_seconds)
         out["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": 1,
@@ -746,6 +755,82 @@ def time_op(fn, flush, stream, n):
         evs.append((a, b))
     torch.cuda.synchronize()
     return 1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def bench_routed(mp, wl, name, dev, flush, n, peak):
+    """The whole fwd+bwd step on another routed workload (its full size, as
+    the headline step runs it): per-op device times with an event after every
+    op (L2 flushed before each step), and the step with events at its ends
+    only.  Returns per-op us, GB/s and fraction of the measured peak."""
+    import torch
+
+    w = wl.routed(name)
+    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+    R = T * K
+
+    def dev_t(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.to(dev)
+
+    idx, probs, x, gy = dev_t(w["idx"]), dev_t(w["probs"]), dev_t(w["x"]), dev_t(w["g_y"])
+    del w
+    rim = torch.empty((T, K), dtype=torch.int32, device=dev)
+    s2f = torch.empty(R, dtype=torch.int32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    ws = torch.empty(mp.mp_build_map_workspace_size(T, K, E), dtype=torch.uint8, device=dev)
+    rows = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    rows_p = torch.empty(R, dtype=torch.float32, device=dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    g_rows = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    g_probs = torch.empty((T, K), dtype=torch.float32, device=dev)
+    g_x = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ops = {
+        "build_map": lambda: mp.mp_build_map(idx, E, row_id_map=rim, sorted_to_flat=s2f,
+                                             counts=counts, offsets=offsets, workspace=ws),
+        "permute": lambda: mp.mp_permute(x, rim, probs, out=rows, out_probs=rows_p),
+        "unpermute": lambda: mp.mp_unpermute(rows, rim, probs, out=y),
+        "unpermute_bwd": lambda: mp.mp_unpermute_bwd(gy, rim, rows, probs, g_rows=g_rows,
+                                                     g_probs=g_probs),
+        "permute_bwd": lambda: mp.mp_permute_bwd(g_rows, rim, g_x=g_x),
+    }
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        for fn in ops.values():
+            fn()
+    torch.cuda.synchronize()
+    routed = int(offsets[-1].item())
+    nbytes = routed_bytes(T, H, K, E, routed)
+    ev = lambda: torch.cuda.Event(enable_timing=True)       # noqa: E731
+    per_op = [[ev() for _ in range(len(ops) + 1)] for _ in range(n)]
+    for i, es in enumerate(per_op):
+        flush(i)
+        es[0].record(stream)
+        for j, fn in enumerate(ops.values()):
+            fn()
+            es[j + 1].record(stream)
+    chained = [(ev(), ev()) for _ in range(n)]
+    for i, (a, z) in enumerate(chained):
+        flush(i)
+        a.record(stream)
+        for fn in ops.values():
+            fn()
+        z.record(stream)
+    torch.cuda.synchronize()
+    step_ms = statistics.mean(a.elapsed_time(z) for a, z in chained)
+    res = {"workload": f"{name} dispatch T={T} H={H} E={E} K={K}, fwd+bwd step",
+           "routed_rows": routed, "ms_per_step": round(step_ms, 4),
+           "GB/s": round(sum(nbytes.values()) / (step_ms * 1e-3) / 1e9, 1),
+           "frac_of_measured": round(sum(nbytes.values()) / (step_ms * 1e-3) / 1e9 / peak, 4),
+           "ops": {}}
+    for j, op in enumerate(ops):
+        us = 1e3 * statistics.mean(es[j].elapsed_time(es[j + 1]) for es in per_op)
+        gbs = nbytes[op] / (us * 1e-6) / 1e9
+        res["ops"][op] = {"us": round(us, 2), "bytes": nbytes[op], "GB/s": round(gbs, 1),
+                          "frac_of_measured": round(gbs / peak, 4)}
+    return res
 
 
 def bench_chunks(mp, wl, dev, flush, args):

@@ -156,8 +156,11 @@ mp_status_t mp_build_map_capacity(const int32_t *idx, int64_t T, int32_t K, int3
  *     to 33,292,288 routes, E=1024 up to 4,177,920).  Larger sizes return
  *     MP_ERR_UNSUPPORTED and launch nothing.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current, and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and caches it for the
+ *     life of the process; make that first call before any stream capture.
+ *     Resetting a device (cudaDeviceReset) after that first call is not
+ *     supported: the array may then move and the cached address would be
+ *     stale.
  *   - All calls share the one array.  Calls that overlap on the GPU (other
  *     streams, other threads) race on it and give wrong maps: serialise them.
  *     Nothing needs clearing between calls: every entry a call reads was

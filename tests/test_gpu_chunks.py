@@ -196,10 +196,20 @@ def test_sort_pad_roundtrip_other_token_types(dtype, H):
     assert int(h(st)[0]) == 0
     y, _ = mp.mp_unpad_restore(out, row_map, N, out_p)
     np.testing.assert_array_equal(y.cpu().numpy().view(np.uint16), x.view(np.uint16))
-    g_pad, _ = mp.mp_unpad_restore_bwd(_dev_tokens(x), row_map)
-    np.testing.assert_array_equal(g_pad.cpu().numpy().view(np.uint16), got.view(np.uint16))
-    g_x, _ = mp.mp_sort_chunks_pad_bwd(out, row_map, N)
-    np.testing.assert_array_equal(g_x.cpu().numpy().view(np.uint16), x.view(np.uint16))
+    # both backwards on independent gradients, against the oracle's backwards
+    g_y = rng.standard_normal((N, H)).astype(dtype)
+    g_y_p = rng.standard_normal(N).astype(np.float32)
+    g_pad, g_pad_p = mp.mp_unpad_restore_bwd(_dev_tokens(g_y), row_map, d(g_y_p))
+    o_gpad, o_gpad_p = oracle.unpad_restore_bwd(g_y, g_y_p, o_map, N)
+    np.testing.assert_array_equal(g_pad.cpu().numpy().view(np.uint16), o_gpad.view(np.uint16))
+    np.testing.assert_array_equal(h(g_pad_p), o_gpad_p)
+    g_out = rng.standard_normal((out_rows, H)).astype(dtype)
+    g_out_p = rng.standard_normal(out_rows).astype(np.float32)
+    g_x, g_x_p = mp.mp_sort_chunks_pad_bwd(_dev_tokens(g_out), row_map, N, d(g_out_p))
+    o_gx, o_gx_p = oracle.sort_chunks_pad_bwd(g_out, g_out_p, o_map, N)
+    got_gx = g_x.cpu().numpy()
+    np.testing.assert_array_equal(got_gx.view(np.uint16), o_gx.view(np.uint16))
+    np.testing.assert_array_equal(h(g_x_p), o_gx_p)
 
 
 @pytest.mark.parametrize("slack", ["exact", "larger", "smaller"])

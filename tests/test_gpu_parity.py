@@ -5,9 +5,8 @@ outputs of unpermute / permute_bwd / unpermute_bwd (both sides run the same
 slot-order fp32 FMA chain and one round-to-nearest-even); g_probs of
 unpermute_bwd within the fp32 summation bound against the oracle's fp64 sum
 (gpu_util.gprobs_bound).  Small and mid workloads are compared element by
-element; the full-size skewed (T=16384, H=4096, E=128, K=8) and large
-(T=32768, H=7168, E=256, K=8) workloads in full for the map and on sampled
-tokens for the rows, in the launch configuration the benchmark uses.
+element; the full-size skewed and large workloads are compared element by
+element in tests/test_gpu_fullsize.py.
 """
 from __future__ import annotations
 
@@ -266,63 +265,6 @@ def test_unpermute_ulp_fallback_not_needed():
     o = oracle.unpermute(w["rows_in"], w["probs"], o_rim, w["T"], w["H"])
     assert bf16_ulp_distance(y, o).max() <= 1
     assert bf16_ulp_distance(y, o).max() == 0
-
-
-# --------------------------------------------------------------------------
-# full-size workloads, sampled
-# --------------------------------------------------------------------------
-
-@pytest.mark.parametrize("name", ["skewed", "large"])
-def test_full_size_sampled(name):
-    w = wl.routed(name)
-    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
-    R = T * K
-    rng = np.random.default_rng(11)
-    sample = np.unique(np.concatenate([rng.choice(T, 192, replace=False), [0, T - 1]]))
-
-    idx, probs = d(w["idx"]), d(w["probs"])
-    rim, s2f, counts, offsets = mp.mp_build_map(idx, E)
-    o_rim, o_s2f, o_counts, o_offsets, _ = oracle.build_map(w["idx"], E)
-    np.testing.assert_array_equal(h(rim), o_rim)
-    np.testing.assert_array_equal(h(s2f), o_s2f)
-    np.testing.assert_array_equal(h(offsets), o_offsets)
-
-    rs = torch.from_numpy(o_rim[sample].ravel().astype(np.int64)).to(DEV)
-    # permute: every slot of a sampled token holds its row
-    out, out_p = mp.mp_permute(d(w["x"]), rim, probs)
-    got = h(out.index_select(0, rs)).reshape(len(sample), K, H)
-    np.testing.assert_array_equal(got, np.repeat(w["x"][sample][:, None, :], K, axis=1))
-    np.testing.assert_array_equal(h(out_p.index_select(0, rs)).reshape(-1, K),
-                                  w["probs"][sample])
-    del out
-
-    # unpermute of counter-based rows (any row can be rebuilt on the host)
-    seed = 77
-    rows = wl.hashed_rows_torch(R, H, seed, DEV)
-    y = h(mp.mp_unpermute(rows, rim, probs).index_select(
-        0, torch.from_numpy(sample).to(DEV)))
-    rim_s = o_rim[sample]
-    flat_rows = rim_s.ravel()
-    rows_s = wl.hashed_rows(flat_rows, H, seed)
-    local = np.arange(flat_rows.size, dtype=np.int32).reshape(rim_s.shape)
-    np.testing.assert_array_equal(
-        y, oracle.unpermute(rows_s, w["probs"][sample], local, len(sample), H))
-
-    # unpermute backward (probs gradient within the fp32 bound)
-    gy = d(w["g_y"])
-    g_rows, g_probs = mp.mp_unpermute_bwd(gy, rim, rows, probs)
-    o_grows, o_gp = oracle.unpermute_bwd(w["g_y"][sample], rows_s, w["probs"][sample], local)
-    got = h(g_rows.index_select(0, rs))
-    np.testing.assert_array_equal(got, o_grows)
-    gp = h(g_probs)[sample].astype(np.float64)
-    bound = gprobs_bound(f32(rows_s).reshape(len(sample), K, H),
-                         f32(w["g_y"][sample])[:, None, :], o_gp)
-    assert np.all(np.abs(gp - o_gp) <= bound)
-
-    # permute backward of the same counter-based rows
-    g_x, _ = mp.mp_permute_bwd(rows, rim)
-    o_gx, _ = oracle.permute_bwd(rows_s, None, local, len(sample), H)
-    np.testing.assert_array_equal(h(g_x)[sample], o_gx)
 
 
 def test_staged_row_kernels_full_compare():

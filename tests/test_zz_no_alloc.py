@@ -51,8 +51,11 @@ def test_noalloc_map_matches_the_workspace_map_on_consecutive_calls():
     torch.cuda.init()
     cases = [wl.routing("skewed"), wl.routing("mid"), wl.routing("skewed", seed=4242)]
     rng = np.random.default_rng(8)
-    idx_bad = rng.integers(0, 40, size=(2999, 3)).astype(np.int32)
+    # more than 32,768 routes, so the count and rank kernels (which keep their
+    # tile counts in the static array) see the bad expert
+    idx_bad = rng.integers(0, 40, size=(20000, 3)).astype(np.int32)
     idx_bad[5, 1] = 99                                  # bad expert: status bit
+    idx_bad[19997, 2] = -3
     cases.append((idx_bad, None, 40))
     for idx_np, _, E in cases:
         idx = torch.from_numpy(idx_np).to(DEV)

@@ -273,6 +273,13 @@ constexpr int STAGE_BUFS = 2;
 // (programmatic dependent) CTAs hold the shared memory the gather's last
 // CTAs would have used.
 constexpr unsigned STAGE_MIN_BLOCKS = 16384;
+// The staged kernels are launched without raising their dynamic shared memory
+// limit, so both stage sizes must fit the default 48 KB (an MP_ROW_THREADS or
+// MP_SLOT_BATCH override that breaks this fails to compile, not to launch).
+static_assert((size_t)STAGE_BUFS * KB * ROW_THREADS * sizeof(uint4) <= 48 * 1024,
+              "forward stage buffers exceed the default dynamic shared memory limit");
+static_assert((size_t)STAGE_BUFS * (KB + 1) * ROW_THREADS * sizeof(uint4) <= 48 * 1024,
+              "backward stage buffers exceed the default dynamic shared memory limit");
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
 {
