@@ -878,9 +878,12 @@ def bench_chunks(mp, wl, dev, flush, args):
             mp.mp_unpad_restore(out, row_map, N, out_p, y=y, y_probs=y_p)
             e[2].record(stream)
         torch.cuda.synchronize()
-        sp = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
-        ur = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
-        rt = statistics.median(e[0].elapsed_time(e[2]) for e in evs)
+        # Means: the event timer ticks in steps of about 1 us here, so the
+        # median of short ops sits on a tick while the mean of many samples
+        # resolves below it.
+        sp = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+        ur = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        rt = statistics.mean(e[0].elapsed_time(e[2]) for e in evs)
         # the same roundtrip with events at its ends only: the restore's launch
         # then overlaps the tail of sort+pad (programmatic dependent launch)
         cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -891,7 +894,7 @@ def bench_chunks(mp, wl, dev, flush, args):
             roundtrip()
             z.record(stream)
         torch.cuda.synchronize()
-        rt_chained = statistics.median(a.elapsed_time(z) for a, z in cev)
+        rt_chained = statistics.mean(a.elapsed_time(z) for a, z in cev)
         padded = int(goff[-1].item())
         b = chunk_bytes(N, H * esize // 2, padded, out_rows)
         key = str(N) if tdt == torch.bfloat16 else f"{N} fp32"
@@ -908,13 +911,15 @@ def bench_chunks(mp, wl, dev, flush, args):
                 z.record(stream)
                 ev.append((a, z))
             torch.cuda.synchronize()
-            return statistics.median(a.elapsed_time(z) for a, z in ev) * 1e3
+            v = [a.elapsed_time(z) * 1e3 for a, z in ev]
+            return statistics.mean(v), statistics.median(v)
 
-        sp_alone = alone(lambda: mp.mp_sort_chunks_pad(x, sz, od, G, align, out_rows, p, out=out,
-                                                       out_probs=out_p, row_map=row_map,
-                                                       group_off=goff))
-        ur_alone = alone(lambda: mp.mp_unpad_restore(out, row_map, N, out_p, y=y, y_probs=y_p))
-        copy_us = alone(lambda: y.copy_(x))
+        sp_alone, sp_alone_med = alone(lambda: mp.mp_sort_chunks_pad(
+            x, sz, od, G, align, out_rows, p, out=out, out_probs=out_p, row_map=row_map,
+            group_off=goff))
+        ur_alone, ur_alone_med = alone(lambda: mp.mp_unpad_restore(out, row_map, N, out_p, y=y,
+                                                                   y_probs=y_p))
+        copy_us, copy_us_med = alone(lambda: y.copy_(x))
         res[key] = {"roundtrip_ms": round(rt, 4), "sort_pad_us": round(sp * 1e3, 2),
                     "unpad_restore_us": round(ur * 1e3, 2),
                     "roundtrip_GB/s": round((b["sort_chunks_pad"] + b["unpad_restore"])
@@ -925,6 +930,10 @@ def bench_chunks(mp, wl, dev, flush, args):
                     "sort_pad_alone_GB/s": round(b["sort_chunks_pad"] / sp_alone / 1e3, 1),
                     "unpad_restore_alone_GB/s": round(b["unpad_restore"] / ur_alone / 1e3, 1),
                     "plain_copy_us": round(copy_us, 2),
+                    "medians_us": {"sort_pad_alone": round(sp_alone_med, 2),
+                                   "unpad_restore_alone": round(ur_alone_med, 2),
+                                   "plain_copy": round(copy_us_med, 2)},
+                    "timing": f"means of {n} samples, each after an L2 flush",
                     "out_rows": out_rows, "padded_rows": padded}
         if tdt == torch.bfloat16:
             res[key]["published_b200_fused_ms"] = {8192: 0.1717, 32768: 0.2029}[N]

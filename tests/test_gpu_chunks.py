@@ -86,6 +86,8 @@ def _meta(seed, G, R, max_size=40, empty_group=False):
     (8, 4, 64, 512, True, 7),       # 64 vectors per row, a partial unrolled pass
     (4, 4, 16, 7168, False, 3),     # 896 vectors per row, several passes
     (2, 2, 4, 24576, True, 0),      # 3072 vectors per row
+    (64, 2, 4, 2048, True, 9),      # G = 64 > 32 groups with C = 128: metadata by the whole CTA
+    (48, 2, 8, 256, False, 3),      # the same for rows of 32 vectors (the per-CTA-rows kernel)
 ])
 def test_sort_pad_edges(G, R, align, H, empty_group, extra):
     sizes, order = _meta(G * 100 + R, G, R, empty_group=empty_group)
@@ -130,6 +132,24 @@ def test_sort_pad_status_bits():
              expect_flags=("rows_overflow",))
     run_case(x, p, np.array([3, 3, 3, 3], np.int32), np.array([0, 7, 2, 3], np.int32), 2, 2,
              16, expect_flags=("bad_order",))
+
+
+@pytest.mark.parametrize("H", [2048, 64])
+def test_sort_pad_order_naming_a_chunk_twice(H):
+    """chunk_order need not be a permutation: a chunk named at two positions is
+    copied to both, a chunk named nowhere is not copied, and an entry out of
+    range names nothing (status bit).  Rows of 256 vectors go through the
+    kernel that scatters input rows; rows of 8 through the one that gathers."""
+    G, R, align = 4, 4, 8
+    sizes, order = _meta(71, G, R, max_size=50)
+    order = order.copy()
+    order[5] = order[2]                 # named twice; the old order[5] named nowhere
+    order[9] = 99                       # out of range
+    N = int(sizes.sum()) + 7            # rows past the named ones are never read
+    x = wl.random_rows(N, H, 8)
+    probs = np.random.default_rng(3).random(N).astype(np.float32)
+    out_rows = N + int(sizes[order[5]]) + G * (align - 1) + 4
+    run_case(x, probs, sizes, order, G, align, out_rows, expect_flags=("bad_order",))
 
 
 def test_restore_bad_row_sets_status():

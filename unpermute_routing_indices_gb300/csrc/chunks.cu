@@ -6,8 +6,9 @@
 //   k_sort_pad     one launch for map + copy.  Every CTA rebuilds the small
 //                  chunk metadata in shared memory (C <= MP_MAX_CHUNKS sizes:
 //                  input starts, output-order starts, group rows, padded group
-//                  offsets) -- one warp with shuffle scans for up to 256
-//                  chunks, the whole CTA beyond -- then resolves the source
+//                  offsets) -- one warp with register-segment shuffle scans
+//                  for up to 256 chunks in up to 32 groups, the whole CTA
+//                  beyond -- then resolves the source
 //                  row of each of its SP_ROWS output rows by two binary
 //                  searches and copies the rows (zero for padding).  CTA 0
 //                  also writes group_off and the status bits.  Nothing is
@@ -43,8 +44,15 @@ constexpr int CH_THREADS = 256;
 constexpr int CH_WARPS = CH_THREADS / 32;
 constexpr int CH_ROWS = MP_CH_ROWS;      // output rows per CTA (restore kernels)
 constexpr int SP_ROWS = MP_SP_ROWS;      // output rows per CTA (sort+pad)
+#ifndef MP_SP_SMALL_THREADS
+#define MP_SP_SMALL_THREADS 128
+#endif
+#ifndef MP_SP_SMALL_ROWS
+#define MP_SP_SMALL_ROWS 16
+#endif
+constexpr int SP_SMALL_THREADS = MP_SP_SMALL_THREADS;  // sort+pad CTA, small outputs
+constexpr int SP_SMALL_ROWS = MP_SP_SMALL_ROWS;
 constexpr int CH_UNROLL = MP_CH_UNROLL;  // vectors in flight per thread
-constexpr int SP_WARP_META_MAX_C = 256;  // chunk counts whose metadata one warp builds
 
 // In-place exclusive scan of a[0..n), n <= 4 * CH_THREADS, in shared memory.
 // Returns the total.  Every thread of the CTA must call it.
@@ -82,29 +90,6 @@ __device__ int64_t cta_exclusive_scan(int64_t *a, int n, int64_t *s_warp)
     return total;
 }
 
-// In-place exclusive scan of a[0..n) in shared memory by one warp (32 entries
-// per round, carried across rounds).  Returns the total to every lane.  All 32
-// lanes must call it; entries written by other lanes must be fenced with
-// __syncwarp() before and after.
-__device__ int64_t warp_exclusive_scan(int64_t *a, int n)
-{
-    const int lane = threadIdx.x & 31;
-    int64_t carry = 0;
-    for (int base = 0; base < n; base += 32) {
-        const int i = base + lane;
-        const int64_t v = i < n ? a[i] : 0;
-        int64_t incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int64_t y = __shfl_up_sync(FULL_MASK, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (i < n) a[i] = carry + incl - v;
-        carry += __shfl_sync(FULL_MASK, incl, 31);
-    }
-    return carry;
-}
-
 // Largest i in [lo, hi) with a[i] <= key (a non-decreasing, a[lo] <= key).
 __device__ __forceinline__ int last_le(const int64_t *a, int lo, int hi, int64_t key)
 {
@@ -120,14 +105,14 @@ __device__ __forceinline__ int last_le(const int64_t *a, int lo, int hi, int64_t
 // Rows of at least 32 vectors go one warp per row, the lanes across the row
 // (CH_UNROLL vectors in flight per lane, addresses by immediate offsets from
 // the row base); narrower rows are spread over the CTA as one flat range.
-template <typename V, bool SCATTER, int RP = 1>
+template <typename V, bool SCATTER, int RP = 1, int THREADS = CH_THREADS>
 __device__ __forceinline__ void copy_rows(const V *__restrict__ in, V *__restrict__ out,
                                           const int32_t *s_map, int64_t row0, int nrows, int nvec)
 {
     if (nvec >= 32) {
         // One warp per RP rows at a time: RP * CH_UNROLL vectors in flight per lane.
         const int lane = threadIdx.x & 31;
-        for (int r0 = (threadIdx.x >> 5) * RP; r0 < nrows; r0 += CH_WARPS * RP) {
+        for (int r0 = (threadIdx.x >> 5) * RP; r0 < nrows; r0 += (THREADS / 32) * RP) {
             const V *src[RP];
             V *dst[RP];
             bool live[RP], zero[RP];
@@ -162,12 +147,12 @@ __device__ __forceinline__ void copy_rows(const V *__restrict__ in, V *__restric
         return;
     }
     const int total = nrows * nvec;
-    for (int w0 = 0; w0 < total; w0 += CH_THREADS * CH_UNROLL) {
+    for (int w0 = 0; w0 < total; w0 += THREADS * CH_UNROLL) {
         V v[CH_UNROLL];
         int64_t dst_off[CH_UNROLL];
 #pragma unroll
         for (int u = 0; u < CH_UNROLL; ++u) {
-            const int w = w0 + u * CH_THREADS + threadIdx.x;
+            const int w = w0 + u * THREADS + threadIdx.x;
             dst_off[u] = -1;
             v[u] = zero_vec<V>();
             if (w < total) {
@@ -219,39 +204,96 @@ __device__ __forceinline__ int sort_pad_group_rows(const SortPadMeta &m, int g, 
     return flags;
 }
 
-__device__ void sort_pad_meta_warp(const SortPadMeta &m, const int32_t *split,
+// Inclusive warp scan of a 64-bit value (5 shuffle steps of two words each).
+__device__ __forceinline__ int64_t warp_inclusive_scan64(int64_t v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(FULL_MASK, v, o);
+        if (lane >= o) v += y;
+    }
+    return v;
+}
+
+// The metadata built by one warp, for C <= 256 and G <= 32, with a short
+// dependency chain: lane l owns the q = ceil(C/32) consecutive chunk
+// positions [l*q, l*q + q), sums them in registers, and the input-order and
+// output-order scans are two independent 5-step warp scans (interleaved by
+// the compiler) instead of rounds of 32.  The group offsets are one more
+// warp scan (lane g holds group g).
+constexpr int SP_FAST_META_MAX_Q = 8;   // C <= 256
+__device__ void sort_pad_meta_fast(const SortPadMeta &m, const int32_t *split,
                                    const int32_t *order, const int32_t *padded_sizes, int C,
                                    int G, int align, int64_t N, int64_t out_rows,
                                    int64_t *group_off, int32_t *status)
 {
     const int lane = threadIdx.x & 31;
+    const int q = (C + 31) >> 5;
+    const int lo = lane * q;
     int flags = 0;
-    for (int c = lane; c < C; c += 32) {   // every metadata load issued together
-        int64_t v = split[c];
-        m.s_chunk[c] = order[c];
-        if (v < 0) { flags |= MP_STATUS_BAD_SPLIT; v = 0; }
-        m.s_start[c] = v;
+    int32_t sz[SP_FAST_META_MAX_Q], od[SP_FAST_META_MAX_Q];
+#pragma unroll
+    for (int j = 0; j < SP_FAST_META_MAX_Q; ++j) {   // every metadata load issued together
+        const int c = lo + j;
+        const bool in = j < q && c < C;
+        sz[j] = in ? split[c] : 0;
+        od[j] = in ? order[c] : -1;
     }
-    if (padded_sizes != nullptr)
-        for (int g = lane; g < G; g += 32) m.s_goff[g] = padded_sizes[g];
-    __syncwarp();
-    const int64_t total_in = warp_exclusive_scan(m.s_start, C);
-    __syncwarp();
-    for (int p = lane; p < C; p += 32) {
-        const int32_t c = m.s_chunk[p];
-        const bool ok = c >= 0 && c < C;
-        if (!ok) flags |= MP_STATUS_BAD_ORDER;
-        m.s_chunk[p] = ok ? c : -1;
-        m.s_cum[p] = ok ? ((c + 1 < C ? m.s_start[c + 1] : total_in) - m.s_start[c]) : 0;
+    const int32_t ps = (padded_sizes != nullptr && lane < G) ? padded_sizes[lane] : 0;
+    int64_t sum_in = 0;
+#pragma unroll
+    for (int j = 0; j < SP_FAST_META_MAX_Q; ++j) {
+        const int c = lo + j;
+        if (j < q && c < C) {
+            if (sz[j] < 0) { flags |= MP_STATUS_BAD_SPLIT; sz[j] = 0; }
+            m.s_start[c] = sz[j];                    // sizes by chunk id, for the gather
+            const bool ok = od[j] >= 0 && od[j] < C;
+            if (!ok) { flags |= MP_STATUS_BAD_ORDER; od[j] = -1; }
+            m.s_chunk[c] = od[j];
+            sum_in += sz[j];
+        }
     }
     __syncwarp();
-    const int64_t total_ord = warp_exclusive_scan(m.s_cum, C);
+    int64_t so[SP_FAST_META_MAX_Q];
+    int64_t sum_out = 0;
+#pragma unroll
+    for (int j = 0; j < SP_FAST_META_MAX_Q; ++j) {   // size of the chunk at position lo + j
+        so[j] = (j < q && lo + j < C && od[j] >= 0) ? m.s_start[od[j]] : 0;
+        sum_out += so[j];
+    }
+    __syncwarp();                                    // every gather done before the overwrite
+    const int64_t inc_in = warp_inclusive_scan64(sum_in);
+    const int64_t inc_out = warp_inclusive_scan64(sum_out);
+    int64_t run_in = inc_in - sum_in, run_out = inc_out - sum_out;
+#pragma unroll
+    for (int j = 0; j < SP_FAST_META_MAX_Q; ++j) {
+        const int c = lo + j;
+        if (j < q && c < C) {
+            m.s_start[c] = run_in;
+            m.s_cum[c] = run_out;
+            run_in += sz[j];
+            run_out += so[j];
+        }
+    }
+    const int64_t total_in = __shfl_sync(FULL_MASK, inc_in, 31);
+    const int64_t total_ord = __shfl_sync(FULL_MASK, inc_out, 31);
     if (lane == 0) m.s_cum[C] = total_ord;
     __syncwarp();
     const int per_group = C / G;
-    for (int g = lane; g < G; g += 32) flags |= sort_pad_group_rows(m, g, per_group, align, padded_sizes);
-    __syncwarp();
-    const int64_t total_pad = warp_exclusive_scan(m.s_goff, G);
+    int64_t padded = 0;
+    if (lane < G) {
+        const int64_t rows = m.s_cum[(lane + 1) * per_group] - m.s_cum[lane * per_group];
+        m.s_grows[lane] = rows;
+        padded = (rows + align - 1) / align * align;
+        if (padded_sizes != nullptr) {
+            padded = ps < 0 ? 0 : ps;
+            if (padded < rows) flags |= MP_STATUS_BAD_PADDED;
+        }
+    }
+    const int64_t inc_pad = warp_inclusive_scan64(padded);
+    if (lane < G) m.s_goff[lane] = inc_pad - padded;
+    const int64_t total_pad = __shfl_sync(FULL_MASK, inc_pad, 31);
     if (lane == 0) m.s_goff[G] = total_pad;
     flags = __reduce_or_sync(FULL_MASK, flags);
     __syncwarp();
@@ -313,8 +355,8 @@ __device__ void sort_pad_meta_cta(const SortPadMeta &m, const int32_t *split,
     }
 }
 
-template <typename V, bool WARP_META, int RP>
-__global__ void __launch_bounds__(CH_THREADS, MP_CH_MIN_BLOCKS)
+template <typename V, bool FAST_META, int RP, int THREADS, int ROWS>
+__global__ void __launch_bounds__(THREADS, MP_CH_MIN_BLOCKS)
     k_sort_pad(const V *__restrict__ x, const float *__restrict__ probs,
                const int32_t *__restrict__ split, const int32_t *__restrict__ order,
                const int32_t *__restrict__ padded_sizes, int C, int G,
@@ -332,13 +374,16 @@ __global__ void __launch_bounds__(CH_THREADS, MP_CH_MIN_BLOCKS)
     m.s_grows = m.s_goff + G + 1;        // [G]
     m.s_warp = m.s_grows + G;            // [CH_WARPS]
     m.s_chunk = reinterpret_cast<int32_t *>(m.s_warp + CH_WARPS);  // [C]
-    int32_t *s_src = m.s_chunk + C;      // [SP_ROWS]
+    int32_t *s_src = m.s_chunk + C;      // [ROWS]
     __shared__ int s_flags;
+    // The whole-CTA metadata and the row resolve assume these shapes.
+    static_assert(FAST_META || THREADS == CH_THREADS, "CTA metadata needs CH_THREADS threads");
+    static_assert(ROWS <= THREADS && THREADS % 32 == 0, "one thread resolves each row");
 
     const int tid = threadIdx.x;
-    if (WARP_META) {
+    if (FAST_META) {
         if (tid < 32)
-            sort_pad_meta_warp(m, split, order, padded_sizes, C, G, align, N, out_rows,
+            sort_pad_meta_fast(m, split, order, padded_sizes, C, G, align, N, out_rows,
                                group_off, status);
         __syncthreads();
     } else {
@@ -348,9 +393,9 @@ __global__ void __launch_bounds__(CH_THREADS, MP_CH_MIN_BLOCKS)
     const int64_t total_pad = m.s_goff[G];
     const int per_group = C / G;
 
-    const int64_t row0 = (int64_t)blockIdx.x * SP_ROWS;
+    const int64_t row0 = (int64_t)blockIdx.x * ROWS;
     const int64_t left = out_rows - row0;
-    const int nrows = left < SP_ROWS ? (int)left : SP_ROWS;
+    const int nrows = left < ROWS ? (int)left : ROWS;
     float pv = 0.0f;   // this row's prob: loaded now, stored after the copy
     if (tid < nrows) {
         const int64_t d = row0 + tid;
@@ -370,7 +415,7 @@ __global__ void __launch_bounds__(CH_THREADS, MP_CH_MIN_BLOCKS)
         if (out_probs != nullptr && src >= 0) pv = __ldg(probs + src);
     }
     __syncthreads();
-    if (nrows > 0) copy_rows<V, false, RP>(x, out, s_src, row0, nrows, nvec);
+    if (nrows > 0) copy_rows<V, false, RP, THREADS>(x, out, s_src, row0, nrows, nvec);
     if (out_probs != nullptr && tid < nrows) out_probs[row0 + tid] = pv;
 }
 
@@ -421,10 +466,10 @@ inline bool chunk_vec_ok(int32_t H, std::initializer_list<const void *> ptrs)
     return true;
 }
 
-inline size_t sort_pad_smem(int C, int G)
+inline size_t sort_pad_smem(int C, int G, int rows)
 {
     return sizeof(int64_t) * (size_t)(C + (C + 1) + (G + 1) + G + CH_WARPS) +
-           sizeof(int32_t) * (size_t)(C + SP_ROWS);
+           sizeof(int32_t) * (size_t)(C + rows);
 }
 
 // Rows are H 16-bit units wide.
@@ -490,25 +535,29 @@ mp_status_t sort_pad_impl(const void *x, const float *probs, const int32_t *spli
     if ((probs == nullptr) != (out_probs == nullptr)) return MP_ERR_INVALID_ARG;
     if (out_rows > 0 && (out == nullptr || row_map == nullptr)) return MP_ERR_INVALID_ARG;
     if (N > 0 && x == nullptr) return MP_ERR_INVALID_ARG;
-    const unsigned blocks = out_rows > 0 ? (unsigned)((out_rows + SP_ROWS - 1) / SP_ROWS) : 1u;
-    const size_t smem = sort_pad_smem(C, G);
     const int32_t w = (int32_t)W;
-    const bool warp_meta = C <= SP_WARP_META_MAX_C;
+    const bool fast_meta = C <= 32 * SP_FAST_META_MAX_Q && G <= 32;
+    const bool vec = chunk_vec_ok(w, {x, out});
     // Small outputs (about one wave of CTAs) keep two rows per warp in
-    // flight; larger ones keep one, for more resident CTAs.
+    // flight; larger ones keep one, for more resident CTAs.  Small outputs
+    // whose metadata one warp builds run in CTAs of SP_SMALL_THREADS threads
+    // and SP_SMALL_ROWS rows, so that the grid is one wave.
     const bool two = out_rows <= MP_SP_RP2_MAX_ROWS;
-#define MP_SORT_PAD_LAUNCH(VT, WM, RPV, NV)                                                  \
-    (void)launch_pdl(k_sort_pad<VT, WM, RPV>, blocks, CH_THREADS, smem, s, (const VT *)x,   \
-                     probs, split_sizes, chunk_order, padded_sizes, C, G, align, N, out_rows,  \
-                     NV, (VT *)out, out_probs, row_map, group_off, dev_status)
-    if (chunk_vec_ok(w, {x, out})) {
-        if (warp_meta && two) MP_SORT_PAD_LAUNCH(uint4, true, 2, w / 8);
-        else if (warp_meta) MP_SORT_PAD_LAUNCH(uint4, true, 1, w / 8);
-        else if (two) MP_SORT_PAD_LAUNCH(uint4, false, 2, w / 8);
-        else MP_SORT_PAD_LAUNCH(uint4, false, 1, w / 8);
+#define MP_SORT_PAD_LAUNCH(VT, FM, RPV, TH, RW, NV)                                           \
+    (void)launch_pdl(k_sort_pad<VT, FM, RPV, TH, RW>,                                        \
+                     out_rows > 0 ? (unsigned)((out_rows + RW - 1) / RW) : 1u, TH,           \
+                     sort_pad_smem(C, G, RW), s, (const VT *)x, probs, split_sizes,          \
+                     chunk_order, padded_sizes, C, G, align, N, out_rows, NV, (VT *)out,     \
+                     out_probs, row_map, group_off, dev_status)
+    if (vec) {
+        if (fast_meta && two)
+            MP_SORT_PAD_LAUNCH(uint4, true, 2, SP_SMALL_THREADS, SP_SMALL_ROWS, w / 8);
+        else if (fast_meta) MP_SORT_PAD_LAUNCH(uint4, true, 1, CH_THREADS, SP_ROWS, w / 8);
+        else if (two) MP_SORT_PAD_LAUNCH(uint4, false, 2, CH_THREADS, SP_ROWS, w / 8);
+        else MP_SORT_PAD_LAUNCH(uint4, false, 1, CH_THREADS, SP_ROWS, w / 8);
     } else {
-        if (warp_meta) MP_SORT_PAD_LAUNCH(uint16_t, true, 1, w);
-        else MP_SORT_PAD_LAUNCH(uint16_t, false, 1, w);
+        if (fast_meta) MP_SORT_PAD_LAUNCH(uint16_t, true, 1, CH_THREADS, SP_ROWS, w);
+        else MP_SORT_PAD_LAUNCH(uint16_t, false, 1, CH_THREADS, SP_ROWS, w);
     }
 #undef MP_SORT_PAD_LAUNCH
     return check_launch();
