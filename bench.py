@@ -53,7 +53,19 @@ FALLBACK_HBM_GBS = 6800.0
 # one ncu capture of one launch of that kernel alone, keyed by (op, workload,
 # T); a figure counts only while the profiled kernel source is unchanged
 # (sha256 prefix of its .cu file and common.cuh).  No matching capture: null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+    #     -k regex:"^<kernel>$" -s <n> -c 1 python bench.py --workload <w> --steps 3
+    #     --warmup 3 --no-cpu --no-chunks --no-extras   (one pass per launch)
+    ("permute", "skewed", 16384): {"bytes": 135335680 + 1013217280, "src": "dab27408089bd60d"},
+    ("unpermute", "skewed", 16384): {"bytes": 1074811648 + 124241664, "src": "dab27408089bd60d"},
+    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209064704 + 1021931520, "src": "dab27408089bd60d"},
+    ("permute_bwd", "skewed", 16384): {"bytes": 1074286336 + 124208128, "src": "dab27408089bd60d"},
+    ("permute", "large", 32768): {"bytes": 472273664 + 3699056128, "src": "dab27408089bd60d"},
+    ("unpermute", "large", 32768): {"bytes": 3760316160 + 459798528, "src": "dab27408089bd60d"},
+    ("unpermute_bwd", "large", 32768): {"bytes": 4230583808 + 3709066496, "src": "dab27408089bd60d"},
+    ("permute_bwd", "large", 32768): {"bytes": 3759203840 + 459582464, "src": "dab27408089bd60d"},
+}
 
 
 # --------------------------------------------------------------------------
@@ -107,6 +119,14 @@ def map_launches(routes: int, E: int) -> int:
         f *= 2
     tiles = -(-routes // (2048 * f))
     return 2 if (E + 1) * tiles <= 32768 else 3
+
+
+def ncu_traffic(op, workload, T):
+    """DRAM bytes of one launch of op's kernel from its ncu capture at this
+    workload and size, or None (no capture, or the kernel source changed)."""
+    tr = NCU_TRAFFIC.get((op, workload, T))
+    src = {"build_map": "map.cu"}.get(op, "rows.cu")
+    return tr["bytes"] if tr is not None and tr["src"] == src_hash(src) else None
 
 
 def src_hash(name):
@@ -499,14 +519,15 @@ def run_gpu(args):
     warm_op = {op: statistics.median(wev[i][j].elapsed_time(wev[i][j + 1]) for i in range(warm_n))
                for j, op in enumerate(ops)}
 
+    # the cost of any launch under the same timing: a one-element torch kernel
+    # between two events after the same L2 flush
+    tiny = torch.zeros(1, device=dev)
+    floor_us = time_op(lambda: tiny.fill_(1.0), flush, stream, 50)
+
     peak, peak_kind = measured_peaks()
     gbs = job_throughput(step_bytes, world, ms)
     dom = max(ops, key=lambda o: per_op[o])
-    dom_src = {"build_map": "map.cu"}.get(dom, "rows.cu")
-    traffic = None
-    tr = NCU_TRAFFIC.get((dom, WORKLOAD, T))
-    if tr is not None and tr["src"] == src_hash(dom_src):
-        traffic = tr["bytes"]
+    traffic = ncu_traffic(dom, WORKLOAD, T)
     achieved = nbytes[dom] / (per_op[dom] * 1e-3) / 1e9
 
     # ---- e2e through host buffers (pinned), same calls.  Serial: every copy
@@ -671,10 +692,15 @@ def run_gpu(args):
         "tokens_per_s": round(world * T / (ms * 1e-3), 1),
         "ms_per_step_serialised": round(ms_serialised, 4),
         "ops_timing": "each op alone: the same steps again with an event after every op",
+        "launch_floor_us": {"value": round(floor_us, 2),
+                            "how": "a one-element torch kernel timed the same way (events "
+                                   "around it after an L2 flush): the part of every short "
+                                   "op's time that is launch and event overhead"},
         "ops": {op: {"us": round(per_op[op] * 1e3, 2), "us_median": round(med_op[op] * 1e3, 2),
                      "us_warm_median": round(warm_op[op] * 1e3, 2), "bytes": nbytes[op],
                      "GB/s": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9, 1),
-                     "frac_of_measured": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9 / peak, 4)}
+                     "frac_of_measured": round(nbytes[op] / (per_op[op] * 1e-3) / 1e9 / peak, 4),
+                     "dram_traffic": ncu_traffic(op, WORKLOAD, T)}
                 for op in ops},
         "permute_incl_map": {
             "us": round((per_op["build_map"] + per_op["permute"]) * 1e3, 2),
@@ -829,7 +855,8 @@ def bench_routed(mp, wl, name, dev, flush, n, peak):
         us = 1e3 * statistics.mean(es[j].elapsed_time(es[j + 1]) for es in per_op)
         gbs = nbytes[op] / (us * 1e-6) / 1e9
         res["ops"][op] = {"us": round(us, 2), "bytes": nbytes[op], "GB/s": round(gbs, 1),
-                          "frac_of_measured": round(gbs / peak, 4)}
+                          "frac_of_measured": round(gbs / peak, 4),
+                          "dram_traffic": ncu_traffic(op, name, T)}
     return res
 
 

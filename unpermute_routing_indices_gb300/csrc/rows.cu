@@ -269,10 +269,23 @@ constexpr int STAGE_BUFS = 2;
 // faster from 16,384 tokens (0.880 -> 0.870 ms; 32,768: 1.731 -> 1.695;
 // 65,536: 3.433 -> 3.350) and slower below (4,096: 0.231 -> 0.241 ms).  A
 // step that mixed register gathers with the staged backward was slower
-// than either, 0.899 ms at 16,384 tokens: the backward's early-launched
-// (programmatic dependent) CTAs hold the shared memory the gather's last
-// CTAs would have used.
-constexpr unsigned STAGE_MIN_BLOCKS = 16384;
+// than either, 0.899 ms at 16,384 tokens.  Switching between the two forms
+// costs: an SM changes its L1 / shared-memory split only when idle, and the
+// staged forms want most of it as shared memory.  On the T=4,096, H=2,048,
+// K=6 step the staged backward alone is faster (41.0 -> 36.9 us) but the
+// register-form kernel after it slows by 3 us even with an event between
+// them, and the step gets slower (0.097 -> 0.100 ms).  Preferring the
+// largest shared split for every kernel instead makes the register forms
+// slower still (T=8,192, H=4,096: unpermute 95 -> 112 us; the smaller L1
+// holds fewer loads in flight).  The overrides are for tuning sweeps.
+#ifndef MP_STAGE_MIN_BLOCKS
+#define MP_STAGE_MIN_BLOCKS 16384
+#endif
+#ifndef MP_STAGE_MIN_BLOCKS_BWD
+#define MP_STAGE_MIN_BLOCKS_BWD MP_STAGE_MIN_BLOCKS
+#endif
+constexpr unsigned STAGE_MIN_BLOCKS = MP_STAGE_MIN_BLOCKS;
+constexpr unsigned STAGE_MIN_BLOCKS_BWD = MP_STAGE_MIN_BLOCKS_BWD;
 // The staged kernels are launched without raising their dynamic shared memory
 // limit, so both stage sizes must fit the default 48 KB (an MP_ROW_THREADS or
 // MP_SLOT_BATCH override that breaks this fails to compile, not to launch).
@@ -514,7 +527,7 @@ void launch_unpermute_bwd(const void *gy, const void *rows, const float *probs,
 {
     const RowGrid g = row_grid(T, nvec, VPT);
     if constexpr (Lanes<V>::N == 8 && VPT == 1) {
-        if (K <= KB && g.blocks >= STAGE_MIN_BLOCKS) {
+        if (K <= KB && g.blocks >= STAGE_MIN_BLOCKS_BWD) {
             const size_t smem = (size_t)STAGE_BUFS * (KB + 1) * ROW_THREADS * sizeof(uint4);
             (void)launch_pdl(k_unpermute_bwd_staged, g.blocks, ROW_THREADS, smem, s,
                 (const uint4 *)gy, (const uint4 *)rows, probs, map, T, K, nvec, g.tpt_log2,
