@@ -739,6 +739,7 @@ def run_gpu(args):
         out["cpu_baseline_threads"] = {"value": round(v, 4), "unit": "GB/s", "cores": n,
                                        "kind": "oracle", "sample": sample}
     if world > 1:
+        barrier()   # rank 0 ran the chunk, extra and other-workload timings alone
         dist.destroy_process_group()
     return out if rank == 0 else None
 
