@@ -8,12 +8,13 @@
 //                  input starts, output-order starts, group rows, padded group
 //                  offsets) -- one warp with register-segment shuffle scans
 //                  for up to 256 chunks in up to 32 groups, the whole CTA
-//                  beyond -- then resolves the source
-//                  row of each of its SP_ROWS output rows by two binary
-//                  searches and copies the rows (zero for padding).  CTA 0
-//                  also writes group_off and the status bits.  Nothing is
-//                  carried between CTAs, so the grid depends on out_rows only
-//                  and sizes are runtime data.
+//                  beyond -- then resolves the source row of each of its
+//                  output rows (SP_ROWS per CTA; SP_SMALL_ROWS per smaller CTA
+//                  for outputs of up to MP_SP_RP2_MAX_ROWS rows with one-warp
+//                  metadata) by two binary searches and copies the rows (zero
+//                  for padding).  CTA 0 also writes group_off and the status
+//                  bits.  Nothing is carried between CTAs, so the grid depends
+//                  on out_rows only and sizes are runtime data.
 //   k_rows_remap   through a saved row map: out[d] = in[map[d]] or zero
 //                  (gather: unpad+restore backward) or out[map[d]] = in[d]
 //                  (scatter: unpad+restore and the sort+pad backward).

@@ -322,6 +322,12 @@ __device__ int32_t cta_exclusive_scan(int32_t *a, int n, int32_t *s_warp)
 inline size_t rank_smem(int E) { return ((size_t)(MAP_WARPS + 3) * (E + 1) + MAP_WARPS) * sizeof(int32_t); }
 
 constexpr int MAP_CACHE_F = 2;   // tiles of up to 2 warp groups keep their ranks in registers
+// Buckets each warp reads at once for the totals: 16 warps x 9 cover E + 1 =
+// 129 in one round trip to L2 (build_map alone on the skewed T=16,384 map:
+// 12.2 us with 8 per warp, 11.1 with 9, 12.4 with 17).
+#ifndef MP_MAP_TOTALS_BU
+#define MP_MAP_TOTALS_BU 9
+#endif
 
 // How k_map_rank gets each bucket's totals and earlier-tile counts:
 //   MAP_MODE_PDL     from the tile counts of k_map_count, reduced in every
@@ -469,11 +475,11 @@ __global__ void __launch_bounds__(MAP_THREADS)
         if (tile == 0)
             for (int b = tid; b <= E; b += MAP_THREADS) offsets[b] = s_off[b];
     } else if constexpr (MODE == MAP_MODE_PDL) {
-        // Warp w sums buckets w, w+8, ...: its lanes read the bucket's row of
+        // Warp w sums buckets w, w+16, ...: its lanes read the bucket's row of
         // the expert-major count matrix (consecutive tiles, coalesced) and
         // two warp reductions give the bucket's total and the routes of
-        // earlier tiles.  Eight buckets are read before any is reduced.
-        constexpr int BU = 8;
+        // earlier tiles.  BU buckets are read before any is reduced.
+        constexpr int BU = MP_MAP_TOTALS_BU;
         for (int b0 = warp; b0 <= E; b0 += MAP_WARPS * BU) {
             int32_t v0[BU], v1[BU];
 #pragma unroll
@@ -486,6 +492,7 @@ __global__ void __launch_bounds__(MAP_THREADS)
 #pragma unroll
             for (int u = 0; u < BU; ++u) {
                 const int b = b0 + u * MAP_WARPS;
+                if (b > E) break;   // warp-uniform: no reductions for absent buckets
                 int32_t tot = v0[u] + v1[u];
                 int32_t pre = (lane < tile ? v0[u] : 0) + (lane + 32 < tile ? v1[u] : 0);
                 if (b <= E)
