@@ -1,7 +1,11 @@
 """Parity of the fused top-k softmax router with the oracle: expert choices
-bit-exact; probabilities within 8 fp32 ulps (CUDA's expf and the C library's
+bit-exact; probabilities within 7 fp32 ulps (CUDA's expf and the C library's
 expf may differ by a few ulps; the rest of the arithmetic is the same IEEE
-sequence); the backward bit-exact from the same forward probabilities."""
+sequence); the backward bit-exact from the same forward probabilities.
+
+7 ulps is the largest distance measured over these cases with four seeds
+each and the four workloads' routers: 2.47 million probabilities, 70% equal,
+99.5% within 2 ulps, 7 ulps once (K = 32), at most 6 with K = 8."""
 from __future__ import annotations
 
 import numpy as np
@@ -15,7 +19,7 @@ from tests.gpu_util import DEV, d, h
 
 pytestmark = pytest.mark.gpu
 
-ULP_TOL = 8
+ULP_TOL = 7
 
 
 def _logits(T, E, seed, ties=False, skew=False):
