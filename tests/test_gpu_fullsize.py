@@ -137,3 +137,65 @@ def test_full_size_every_element(name):
             if len(failures) > 20:
                 break
     assert not failures, f"mismatches (op, first token, end token): {failures[:20]}"
+
+
+def _check_ep_subrange(a, b, blk, w, modes):
+    """Oracle's rank-ordered combine (ep = 8) on tokens [a, b) of a block, in
+    every mode, against the device outputs of the block."""
+    K, H, E = w["K"], w["H"], w["E"]
+    rim = blk["rim"][a:b]
+    n = b - a
+    local = np.where(rim >= 0, np.arange(n * K, dtype=np.int32).reshape(n, K), -1)
+    rows_in = blk["rows_in"][a * K:b * K]
+    t0 = blk["t0"]
+    bad = []
+    for m, (bf16p, fp64) in enumerate(modes):
+        want = oracle.unpermute_ep(rows_in, w["probs"][t0 + a:t0 + b], local,
+                                   w["idx"][t0 + a:t0 + b], n, H, E, 8, bf16p, fp64)
+        if not np.array_equal(blk["y"][m][a:b], want):
+            bad.append((f"unpermute_ep(bf16_partials={bf16p}, fp64_cross_rank={fp64})", a, b))
+    return bad
+
+
+@pytest.mark.parametrize("name", ["skewed", "large"])
+def test_full_size_ep_every_element(name):
+    """The rank-ordered combine over 8 simulated EP ranks ("core.transformer.
+    moe.batch_invariant", `_rank_tree_unpermute_kernel`: per-rank slot-order
+    FMA partials, optionally rounded to bf16, added in rank order in fp32 or
+    fp64, one bf16 rounding) at full size, every element of every mode."""
+    w = wl.routed(name, grads=False)
+    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
+    R = T * K
+    idx, probs = d(w["idx"]), d(w["probs"])
+    rim, *_ = mp.mp_build_map(idx, E)
+    o_rim, *_ = oracle.build_map(w["idx"], E)
+    np.testing.assert_array_equal(h(rim), o_rim)
+    rows_in = wl.hashed_rows_torch(R, H, ROWS_SEED + 1, DEV)
+    modes = [(False, False), (True, False), (False, True), (True, True)]
+    ys = [mp.mp_unpermute_ep(rows_in, rim, idx, E, 8, probs, bf16_partials=b16,
+                             fp64_cross_rank=f64) for b16, f64 in modes]
+    torch.cuda.synchronize()
+
+    threads = max(1, min(32, os.cpu_count() or 1))
+    bt = BLOCK[name]
+    failures = []
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        for t0 in range(0, T, bt):
+            t1 = min(T, t0 + bt)
+            rim_b = o_rim[t0:t1]
+            sel = torch.from_numpy(np.maximum(rim_b, 0).ravel().astype(np.int64)).to(DEV)
+            blk = {"t0": t0, "rim": rim_b, "rows_in": h(rows_in.index_select(0, sel)),
+                   "y": [h(y[t0:t1]) for y in ys]}
+            ends = np.concatenate([rim_b.ravel()[:4], rim_b.ravel()[-4:]])
+            np.testing.assert_array_equal(
+                np.concatenate([blk["rows_in"][:4], blk["rows_in"][-4:]]),
+                wl.hashed_rows(ends, H, ROWS_SEED + 1))
+            n = t1 - t0
+            edges = [n * i // threads for i in range(threads + 1)]
+            parts = [(a, b) for a, b in zip(edges[:-1], edges[1:]) if b > a]
+            for bad in pool.map(lambda ab: _check_ep_subrange(ab[0], ab[1], blk, w, modes),
+                                parts):
+                failures.extend((what, t0 + a, t0 + b) for what, a, b in bad)
+            if len(failures) > 20:
+                break
+    assert not failures, f"mismatches (mode, first token, end token): {failures[:20]}"

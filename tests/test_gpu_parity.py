@@ -454,25 +454,6 @@ def test_unpermute_ep_one_rank_is_unpermute():
     assert torch.equal(a, mp.mp_unpermute(rows, rim, probs))
 
 
-def test_unpermute_ep_full_size_sampled():
-    w = wl.routed("large")
-    T, H, E, K = w["T"], w["H"], w["E"], w["K"]
-    rim, *_ = mp.mp_build_map(d(w["idx"]), E)
-    o_rim, *_ = oracle.build_map(w["idx"], E)
-    seed = 91
-    rows = wl.hashed_rows_torch(T * K, H, seed, DEV)
-    sample = np.unique(np.random.default_rng(3).choice(T, 64, replace=False))
-    rim_s = o_rim[sample]
-    rows_s = wl.hashed_rows(rim_s.ravel(), H, seed)
-    local = np.arange(rim_s.size, dtype=np.int32).reshape(rim_s.shape)
-    for bf16p, fp64 in ((True, False), (True, True)):
-        got = mp.mp_unpermute_ep(rows, rim, d(w["idx"]), E, 8, d(w["probs"]),
-                                 bf16_partials=bf16p, fp64_cross_rank=fp64)
-        want = oracle.unpermute_ep(rows_s, w["probs"][sample], local, w["idx"][sample],
-                                   len(sample), H, E, 8, bf16p, fp64)
-        np.testing.assert_array_equal(h(got)[sample], want)
-
-
 def test_unpermute_ep_wide_ranging_partials():
     """Rows whose values span ~130 binades, so the per-element rank partials
     often range past what an fp32 sum holds exactly: the fp64 cross-rank sum
