@@ -406,7 +406,9 @@ def test_build_map_capacity_three_launch_path_and_dropped_rows_downstream():
 # --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name,T,H,ep", [("mid", 2000, None, 8), ("skewed", 3000, 264, 16),
-                                          ("tiny", None, None, 4), ("mid", 1500, 37, 2)])
+                                          ("tiny", None, None, 4), ("mid", 1500, 37, 2),
+                                          # one token per CTA, a ragged last pass
+                                          ("mid", 700, 1032, 8), ("skewed", 400, 1160, 4)])
 @pytest.mark.parametrize("bf16p,fp64", [(False, False), (True, False), (False, True),
                                          (True, True)])
 def test_unpermute_ep(name, T, H, ep, bf16p, fp64):
@@ -454,12 +456,13 @@ def test_unpermute_ep_one_rank_is_unpermute():
     assert torch.equal(a, mp.mp_unpermute(rows, rim, probs))
 
 
-def test_unpermute_ep_wide_ranging_partials():
+@pytest.mark.parametrize("T,H", [(700, 64), (300, 1024)])   # token groups; a token per CTA
+def test_unpermute_ep_wide_ranging_partials(T, H):
     """Rows whose values span ~130 binades, so the per-element rank partials
     often range past what an fp32 sum holds exactly: the fp64 cross-rank sum
     must still match the oracle bit for bit."""
     rng = np.random.default_rng(31)
-    T, K, E, H, ep = 700, 8, 64, 64, 8
+    K, E, ep = 8, 64, 8
     idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
     probs = rng.dirichlet(np.ones(K), size=T).astype(np.float32)
     ex = rng.integers(60, 191, size=(T * K, H)).astype(np.uint16)
@@ -474,8 +477,9 @@ def test_unpermute_ep_wide_ranging_partials():
         np.testing.assert_array_equal(h(got), want)
 
 
+@pytest.mark.parametrize("H", [8, 1032])   # token groups; a token per CTA, ragged last pass
 @pytest.mark.parametrize("bf16p", [True, False])
-def test_unpermute_ep_fp64_sum_on_bf16_ties(bf16p):
+def test_unpermute_ep_fp64_sum_on_bf16_ties(bf16p, H):
     """Rank partials 1, 2^-8 (together exactly halfway between two bf16 values)
     and a small third partial on a third rank that decides the rounding, from
     2^-12 to 2^-40 of the first, either sign, or zero.  A third partial
@@ -485,7 +489,7 @@ def test_unpermute_ep_fp64_sum_on_bf16_ties(bf16p):
     decides alone.  The oracle's rounding of some rows is pinned below.  The last
     rows cancel exactly: a sum rounded toward -inf gives -0 there, where the
     fp64 sum is +0."""
-    E, ep, K, H = 8, 4, 3, 8
+    E, ep, K = 8, 4, 3
     vals = [(1.0, 2.0**-8, 2.0**-30), (1.0, 2.0**-8, -2.0**-30), (1.0, 2.0**-8, 2.0**-40),
             (1.0, 2.0**-8, -2.0**-40), (1.0, 2.0**-8, 0.0), (-1.0, -(2.0**-8), -(2.0**-30)),
             (3.0, 2.0**-7, 2.0**-33), (2.0**-30, 1.0, 2.0**-8),

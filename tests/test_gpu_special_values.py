@@ -61,11 +61,12 @@ def test_row_ops_on_special_values(seed):
     assert np.any((y & 0x7F80) == 0) and np.any(y == 0x0000)     # subnormal / zero results
 
 
-@pytest.mark.parametrize("K", [6, 12])   # the 8-slot and 16-slot kernel forms
+# the 8-slot and 16-slot forms on token groups, and one token per CTA
+@pytest.mark.parametrize("K,H", [(6, 64), (12, 64), (6, 1032)])
 @pytest.mark.parametrize("bf16p,fp64", [(False, False), (True, False), (False, True),
                                          (True, True)])
-def test_ep_combine_on_special_values(bf16p, fp64, K):
-    idx, probs, rows, _, _, E = _case(7, K=K, E=24)
+def test_ep_combine_on_special_values(bf16p, fp64, K, H):
+    idx, probs, rows, _, _, E = _case(7, K=K, E=24, H=H)
     T, H = idx.shape[0], rows.shape[1]
     rim, *_ = mp.mp_build_map(d(idx), E)
     o_rim, *_ = oracle.build_map(idx, E)

@@ -9,12 +9,13 @@
 // optionally in FP64 (CROSS_RANK_FP64, _rank_tree_unpermute_kernel).  Here the
 // EP ranks are simulated: rank r owns experts [r*E/ep, (r+1)*E/ep).
 //
-// k_unpermute_ep: one group of tpt threads per token, one 16-byte vector (8
-// elements) per thread per pass.  Each thread sorts the token's K (<= 8, or
-// <= 16 in a second form) slots by (rank, slot) once, with a fixed sorting
-// network on registers.  Per pass it copies its slots' row vectors into
-// shared memory (cp.async, the next pass in flight while this one computes;
-// the element path for odd H keeps them in registers), reads them back in
+// k_unpermute_ep_token (rows of 1,024 elements or more, K <= 8): one token
+// per CTA of 128 threads.  k_unpermute_ep (shorter rows, odd H, or K <= 16):
+// one group of tpt threads per token.  Both: one 16-byte vector (8 elements)
+// per thread per pass.  Each thread sorts the token's K slots by (rank, slot)
+// once, with a fixed sorting network on registers.  Per pass it copies its slots' row vectors into
+// shared memory (cp.async; the element path for odd H keeps them in
+// registers), reads them back in
 // sorted order and runs one fused multiply-add chain that hands the rank's
 // partial to the cross-rank sum at each rank's last slot: K FMAs per element
 // whatever the number of ranks.  A rank with no
@@ -37,6 +38,8 @@ namespace mp {
 namespace {
 
 constexpr int EP_THREADS = 128;
+constexpr int EP_THREADS_LOG2 = 7;
+static_assert((1 << EP_THREADS_LOG2) == EP_THREADS, "EP_THREADS is a power of two");
 constexpr int EP_KMAX = 16;   // slots per token: kernels for K <= 8 and for K <= 16
 
 
@@ -291,12 +294,184 @@ constexpr size_t ep_stage_bytes()
     return Lanes<V>::N == 8 ? (size_t)ep_stage_bufs(KM) * KM * EP_THREADS * 16 : 0;
 }
 
-// CTAs per SM each variant is compiled for (registers are capped to fit; the
-// two 16 KB stage buffers allow 6).  Measured on the skewed T=16384, ep=8
-// combine with the rows staged: 6 CTAs give fp32 174 us, bf16 partials 183,
-// fp64 sum 194 (fp32 partials) / 197 (bf16 partials); 5 CTAs the same within
-// 1%.  With up to 16 slots: 2 CTAs per SM (rare shapes; correctness first).
+// CTAs per SM each form of the general kernel is compiled for (registers are
+// capped to fit; the two 16 KB stage buffers allow 6).  On the skewed
+// T=16384, ep=8 combine (before the one-token kernel took those rows), 6 CTAs
+// gave fp32 174 us, bf16 partials 183, fp64 sum 194 (fp32 partials) / 197
+// (bf16 partials); 5 CTAs the same within 1%.  With up to 16 slots: 2 CTAs
+// per SM (rare shapes; correctness first).
 constexpr int ep_min_blocks(int km) { return km > 8 ? 2 : 6; }
+
+// A token's K map entries, expert ids and probabilities as loaded.
+template <int KM>
+struct EpRaw {
+    int32_t row[KM], expert[KM];
+    float p[KM];
+};
+
+// The token's routed slots sorted by (rank, slot), unrouted slots last: the
+// row and probability of each sorted position, and bit masks over the sorted
+// positions of the routed slots (valid) and of each rank's last slot (last).
+template <int KM>
+struct EpSlots {
+    int32_t rk[KM];
+    float pk[KM];
+    unsigned valid, last;
+};
+
+template <bool PROBS, int KM>
+__device__ __forceinline__ void ep_load(EpRaw<KM> &r, const int32_t *__restrict__ map,
+                                        const int32_t *__restrict__ idx,
+                                        const float *__restrict__ probs, int64_t t, int K)
+{
+#pragma unroll
+    for (int i = 0; i < KM; ++i) {
+        const bool in = i < K;
+        r.row[i] = in ? __ldg(map + t * K + i) : -1;
+        r.expert[i] = in ? __ldg(idx + t * K + i) : 0;
+        r.p[i] = (PROBS && in) ? __ldg(probs + t * K + i) : 1.0f;
+    }
+}
+
+template <int KM>
+__device__ __forceinline__ void ep_prepare(const EpRaw<KM> &r, int per_rank, EpSlots<KM> &s)
+{
+    int32_t key[KM];
+#pragma unroll
+    for (int i = 0; i < KM; ++i) {
+        int32_t rank = r.expert[i] / per_rank;
+        rank = rank < -(1 << 20) ? -(1 << 20) : (rank > (1 << 20) ? (1 << 20) : rank);
+        key[i] = r.row[i] >= 0 ? rank * KM + i : INT_MAX;
+        s.rk[i] = r.row[i];
+        s.pk[i] = r.p[i];
+    }
+    sort_slots<KM>(key, s.rk, s.pk);
+    s.valid = 0;
+    s.last = 0;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        if (key[j] == INT_MAX) continue;
+        s.valid |= 1u << j;
+        const bool next_same = j + 1 < KM && key[j + 1] != INT_MAX &&
+                               (key[j + 1] - (key[j + 1] & (KM - 1))) ==
+                                   (key[j] - (key[j] & (KM - 1)));
+        if (!next_same) s.last |= 1u << j;
+    }
+}
+
+// One output vector of the rank-ordered combine; row(j) gives the vector of
+// sorted slot j.
+template <typename V, bool PROBS, bool BF16P, bool FP64, int KM, typename Get>
+__device__ __forceinline__ V ep_vec(Get row, const EpSlots<KM> &s)
+{
+    constexpr int L = Lanes<V>::N;
+    if constexpr (FP64) {
+        // The fp64 cross-rank sum, rounded once to bf16, without fp64
+        // arithmetic on the common path.  The partials are summed in rank
+        // order twice in fp32, every add rounded toward -inf (lo) and toward
+        // +inf (hi).  Then lo <= s <= hi for the fp64 sum s, by induction
+        // over the adds: a float rounded down (up) from x is an fp64 value
+        // <= x (>= x), so rounding x to the nearest fp64 value cannot pass
+        // it.  Rounding to bf16 is monotone, so where lo and hi round to the
+        // same bf16 value, and it is not NaN, that is the bf16 of s.  An
+        // element whose bracket holds a bf16 midpoint (about 1 in 10^4 on
+        // N(0,1) rows), or that cancels exactly (lo = -0 where s is +0), or
+        // meets inf or NaN, takes the definition itself: fp64 adds in rank
+        // order, per element.  On 16-byte vectors the walk runs on packed
+        // fp32 pairs.
+        uint16_t bits[L];
+        unsigned open = 0;   // elements whose bracket does not decide
+        if constexpr (L == 8) {
+            uint64_t lo2[4], hi2[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) lo2[i] = hi2[i] = 0;
+            walk_ranks2<PROBS, KM>(row, s.pk, s.valid, s.last, [&](int i, uint64_t p) {
+                if constexpr (BF16P) {
+                    float lo, hi;
+                    f2_split(p, lo, hi);
+                    p = bf16x2_wide(pack_bf16x2(lo, hi));
+                }
+                lo2[i] = add2_rm(lo2[i], p);
+                hi2[i] = add2_rp(hi2[i], p);
+            });
+            bool any = false;
+            uint32_t wl[4], wh[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float l0, l1, h0, h1;
+                f2_split(lo2[i], l0, l1);
+                f2_split(hi2[i], h0, h1);
+                wl[i] = pack_bf16x2(l0, l1);
+                wh[i] = pack_bf16x2(h0, h1);
+                bits[2 * i] = static_cast<uint16_t>(wl[i] & 0xffffu);
+                bits[2 * i + 1] = static_cast<uint16_t>(wl[i] >> 16);
+                any |= wl[i] != wh[i] ||
+                       max_u16x2(wl[i] & 0x7fff7fffu, 0x7f807f80u) != 0x7f807f80u;
+            }
+            if (any) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t a = (e & 1) ? wl[e / 2] >> 16 : wl[e / 2] & 0xffffu;
+                    const uint32_t b = (e & 1) ? wh[e / 2] >> 16 : wh[e / 2] & 0xffffu;
+                    if (a != b || (a & 0x7fffu) > 0x7f80u) open |= 1u << e;
+                }
+            }
+        } else {
+            float lo[L], hi[L];
+#pragma unroll
+            for (int e = 0; e < L; ++e) lo[e] = hi[e] = 0.0f;
+            walk_ranks<PROBS, BF16P, L, KM>(row, s.pk, s.valid, s.last, [&](int e, float p) {
+                lo[e] = __fadd_rd(lo[e], p);
+                hi[e] = __fadd_ru(hi[e], p);
+            });
+#pragma unroll
+            for (int e = 0; e < L; ++e) {
+                const uint32_t a = bf16_bits(lo[e]), b = bf16_bits(hi[e]);
+                bits[e] = static_cast<uint16_t>(a);
+                if (a != b || (a & 0x7fffu) > 0x7f80u) open |= 1u << e;
+            }
+        }
+        if (open) {
+#pragma unroll
+            for (int e = 0; e < L; ++e)
+                if (open >> e & 1u)
+                    bits[e] = rank_sum_f64<PROBS, BF16P, KM>(row, s.pk, s.valid, s.last, e);
+        }
+        return pack_bits(bits);
+    } else {
+        float acc[L];
+#pragma unroll
+        for (int e = 0; e < L; ++e) acc[e] = 0.0f;
+        if constexpr (BF16P && L == 8) {
+            walk_ranks2<PROBS, KM>(row, s.pk, s.valid, s.last, [&](int i, uint64_t p) {
+                float lo, hi;
+                f2_split(p, lo, hi);
+                add_bf16x2(pack_bf16x2(lo, hi), acc[2 * i], acc[2 * i + 1]);
+            });
+        } else {
+            walk_ranks<PROBS, BF16P, L, KM>(row, s.pk, s.valid, s.last,
+                                            [&](int e, float p) { acc[e] = __fadd_rn(acc[e], p); });
+        }
+        return pack(acc);
+    }
+}
+
+// Copies this thread's vector cc of every routed sorted slot into its column
+// of a stage buffer (cp.async, 16 bytes each), as one commit group.
+template <int KM>
+__device__ __forceinline__ void ep_issue(uint4 *buf, const uint4 *__restrict__ rows,
+                                         const EpSlots<KM> &s, int nvec, int cc)
+{
+    uint4 *const dst = buf + threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < KM; ++i)
+        if (s.valid >> i & 1u)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                         ::"r"(smem_u32(dst + i * EP_THREADS)),
+                           "l"(rows + (int64_t)s.rk[i] * nvec + cc)
+                         : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
 
 template <typename V, bool PROBS, bool BF16P, bool FP64, int KM>
 __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(KM))
@@ -312,29 +487,11 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(KM))
     const int64_t t = (int64_t)blockIdx.x * (EP_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
     if (t >= T) return;
 
-    // The token's routed slots sorted by (rank, slot); unrouted slots last.
-    int32_t key[KM], rk[KM];
-    float pk[KM];
-#pragma unroll
-    for (int i = 0; i < KM; ++i) {
-        const bool in = i < K;
-        const int32_t row = in ? __ldg(map + t * K + i) : -1;
-        int32_t rank = in ? __ldg(idx + t * K + i) / per_rank : 0;
-        rank = rank < -(1 << 20) ? -(1 << 20) : (rank > (1 << 20) ? (1 << 20) : rank);
-        key[i] = row >= 0 ? rank * KM + i : INT_MAX;
-        rk[i] = row;
-        pk[i] = (PROBS && in) ? __ldg(probs + t * K + i) : 1.0f;
-    }
-    sort_slots<KM>(key, rk, pk);
-    unsigned valid = 0, last = 0;
-#pragma unroll
-    for (int j = 0; j < KM; ++j) {
-        if (key[j] == INT_MAX) continue;
-        valid |= 1u << j;
-        const bool next_same = j + 1 < KM && key[j + 1] != INT_MAX &&
-                               (key[j + 1] - (key[j + 1] & (KM - 1))) ==
-                                   (key[j] - (key[j] & (KM - 1)));
-        if (!next_same) last |= 1u << j;
+    EpSlots<KM> sl;
+    {
+        EpRaw<KM> raw;
+        ep_load<PROBS, KM>(raw, map, idx, probs, t, K);
+        ep_prepare<KM>(raw, per_rank, sl);
     }
     // On 16-byte vectors each pass's rows are staged in shared memory
     // (cp.async, 16 bytes per copy) instead of registers, two passes deep:
@@ -344,19 +501,9 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(KM))
     constexpr bool STAGE = L == 8;
     constexpr int NBUF = STAGE ? ep_stage_bufs(KM) : 1;
     extern __shared__ uint4 ep_stage[];   // [NBUF][KM][EP_THREADS] when STAGE
-    const auto issue = [&](int cc, int buf) {
-        uint4 *const dst = ep_stage + buf * KM * EP_THREADS + threadIdx.x;
-#pragma unroll
-        for (int i = 0; i < KM; ++i)
-            if (valid >> i & 1u)
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                             ::"r"(smem_u32(dst + i * EP_THREADS)),
-                               "l"(rows + (int64_t)rk[i] * nvec + cc)
-                             : "memory");
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
+    const auto *const vrows = reinterpret_cast<const uint4 *>(rows);
     if constexpr (STAGE && NBUF == 2)
-        if (lane < nvec) issue(lane, 0);
+        if (lane < nvec) ep_issue<KM>(ep_stage, vrows, sl, nvec, lane);
     int pass = 0;
     for (int c0 = 0; c0 < nvec; c0 += tpt, ++pass) {
         const int c = c0 + lane;
@@ -365,19 +512,20 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(KM))
             if (c >= nvec) break;
             if constexpr (NBUF == 2) {
                 if (c + tpt < nvec) {
-                    issue(c + tpt, (pass + 1) & 1);
+                    ep_issue<KM>(ep_stage + ((pass + 1) & 1) * KM * EP_THREADS, vrows, sl, nvec,
+                                 c + tpt);
                     asm volatile("cp.async.wait_group 1;" ::: "memory");
                 } else {
                     asm volatile("cp.async.wait_group 0;" ::: "memory");
                 }
             } else {
-                issue(c, 0);
+                ep_issue<KM>(ep_stage, vrows, sl, nvec, c);
             }
         } else {
 #pragma unroll
             for (int i = 0; i < KM; ++i)
-                r[i] = ((valid >> i & 1u) && c < nvec)
-                           ? ld_stream(rows + (int64_t)rk[i] * nvec + c) : zero_vec<V>();
+                r[i] = ((sl.valid >> i & 1u) && c < nvec)
+                           ? ld_stream(rows + (int64_t)sl.rk[i] * nvec + c) : zero_vec<V>();
         }
         uint4 *const mine = ep_stage + (pass & (NBUF - 1)) * KM * EP_THREADS + threadIdx.x;
         const auto row = [&](int j) -> V {
@@ -390,99 +538,91 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(KM))
             const int cn = c + tpt;
 #pragma unroll
             for (int i = 0; i < KM; ++i)
-                if ((valid >> i & 1u) && cn < nvec)
+                if ((sl.valid >> i & 1u) && cn < nvec)
                     asm volatile("prefetch.global.L2 [%0];"
-                                 ::"l"(rows + (int64_t)rk[i] * nvec + cn));
+                                 ::"l"(rows + (int64_t)sl.rk[i] * nvec + cn));
         }
         if constexpr (STAGE && NBUF == 1) asm volatile("cp.async.wait_group 0;" ::: "memory");
-        if constexpr (FP64) {
-            // The fp64 cross-rank sum, rounded once to bf16, without fp64
-            // arithmetic on the common path.  The partials are summed in rank
-            // order twice in fp32, every add rounded toward -inf (lo) and
-            // toward +inf (hi).  Then lo <= s <= hi for the fp64 sum s, by
-            // induction over the adds: a float rounded down (up) from x is an
-            // fp64 value <= x (>= x), so rounding x to the nearest fp64 value
-            // cannot pass it.  Rounding to bf16 is monotone, so where lo and hi
-            // round to the same bf16 value, and it is not NaN, that is the bf16
-            // of s.  An element whose bracket holds a bf16 midpoint (about 1 in
-            // 10^4 on N(0,1) rows), or that cancels exactly (lo = -0 where s is
-            // +0), or meets inf or NaN, takes the definition itself: fp64 adds
-            // in rank order, per element.  On 16-byte vectors the walk runs on
-            // packed fp32 pairs.
-            uint16_t bits[L];
-            unsigned open = 0;   // elements whose bracket does not decide
-            if constexpr (L == 8) {
-                uint64_t lo2[4], hi2[4];
+        const V v = ep_vec<V, PROBS, BF16P, FP64, KM>(row, sl);
+        if (c < nvec) st_row(out + t * nvec + c, v);
+    }
+}
+
+// One token per CTA, for rows of EP_THREADS 16-byte vectors or more with
+// K <= 8: the CTA's threads cover the row in passes of EP_THREADS vectors,
+// and the token index is the block index.  The token's slot data is then the
+// same in every thread of the CTA, and the kernel has no token-group
+// arithmetic.  The fp32-sum forms keep two stage buffers (the next pass's
+// copies in flight while this one computes) at 6 CTAs per SM.  The fp64
+// forms need fewer registers here (50 against 76-78), and run one stage
+// buffer at 8 CTAs per SM: each pass's copies are waited for at once, while
+// the next pass's rows are prefetched into L2 (prefetch.global.L2), so that
+// its copies hit in L2.  Measured on the skewed T=16384, H=4096, ep=8
+// combine, against the general kernel: fp32 174.5 -> 171.5 us, bf16
+// partials 183.5 -> 174.7, fp64 sum with fp32 / bf16 partials 192.9 / 200.0
+// -> 179.3 / 187.0 (two buffers at 6 CTAs: 186.4 / 197.4; one buffer at 7,
+// 9 or 10 CTAs: 181.8-190.1 / 187.0-202.9).
+template <bool FP64>
+__host__ __device__ constexpr int ep_token_bufs() { return FP64 ? 1 : 2; }
+template <bool FP64>
+constexpr size_t ep_token_stage_bytes() { return (size_t)ep_token_bufs<FP64>() * 8 * EP_THREADS * 16; }
+
+template <bool PROBS, bool BF16P, bool FP64>
+__global__ void __launch_bounds__(EP_THREADS, FP64 ? 8 : 6)
+    k_unpermute_ep_token(const uint4 *__restrict__ rows, const float *__restrict__ probs,
+                         const int32_t *__restrict__ map, const int32_t *__restrict__ idx,
+                         int64_t T, int K, int nvec, int per_rank, uint4 *__restrict__ out)
+{
+    constexpr int KM = 8;
+    pdl_trigger();
+    pdl_wait();
+    const int64_t t = blockIdx.x;
+    if (t >= T) return;
+    const int lane = threadIdx.x;
+    extern __shared__ uint4 ep_stage[];   // [ep_token_bufs][KM][EP_THREADS]
+
+    EpSlots<KM> sl;
+    {
+        EpRaw<KM> raw;
+        ep_load<PROBS, KM>(raw, map, idx, probs, t, K);
+        ep_prepare<KM>(raw, per_rank, sl);
+    }
+    const uint4 *const mine0 = ep_stage + threadIdx.x;
+    if constexpr (ep_token_bufs<FP64>() == 1) {
+        for (int c = lane; c < nvec; c += EP_THREADS) {
+            ep_issue<KM>(ep_stage, rows, sl, nvec, c);
+            const int cn = c + EP_THREADS;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) lo2[i] = hi2[i] = 0;
-                walk_ranks2<PROBS, KM>(row, pk, valid, last, [&](int i, uint64_t p) {
-                    if constexpr (BF16P) {
-                        float lo, hi;
-                        f2_split(p, lo, hi);
-                        p = bf16x2_wide(pack_bf16x2(lo, hi));
-                    }
-                    lo2[i] = add2_rm(lo2[i], p);
-                    hi2[i] = add2_rp(hi2[i], p);
-                });
-                bool any = false;
-                uint32_t wl[4], wh[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float l0, l1, h0, h1;
-                    f2_split(lo2[i], l0, l1);
-                    f2_split(hi2[i], h0, h1);
-                    wl[i] = pack_bf16x2(l0, l1);
-                    wh[i] = pack_bf16x2(h0, h1);
-                    bits[2 * i] = static_cast<uint16_t>(wl[i] & 0xffffu);
-                    bits[2 * i + 1] = static_cast<uint16_t>(wl[i] >> 16);
-                    any |= wl[i] != wh[i] ||
-                           max_u16x2(wl[i] & 0x7fff7fffu, 0x7f807f80u) != 0x7f807f80u;
-                }
-                if (any) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const uint32_t a = (e & 1) ? wl[e / 2] >> 16 : wl[e / 2] & 0xffffu;
-                        const uint32_t b = (e & 1) ? wh[e / 2] >> 16 : wh[e / 2] & 0xffffu;
-                        if (a != b || (a & 0x7fffu) > 0x7f80u) open |= 1u << e;
-                    }
-                }
+            for (int i = 0; i < KM; ++i)
+                if ((sl.valid >> i & 1u) && cn < nvec)
+                    asm volatile("prefetch.global.L2 [%0];"
+                                 ::"l"(rows + (int64_t)sl.rk[i] * nvec + cn));
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            const uint4 v = ep_vec<uint4, PROBS, BF16P, FP64, KM>(
+                [&](int j) -> uint4 { return mine0[j * EP_THREADS]; }, sl);
+            st_row(out + t * nvec + c, v);
+        }
+    } else {
+        ep_issue<KM>(ep_stage, rows, sl, nvec, lane);   // lane < EP_THREADS <= nvec
+        int pass = 0;   // stage buffer pass & 1
+        for (int c = lane; c - lane < nvec; c += EP_THREADS, ++pass) {
+            if (c - lane + EP_THREADS < nvec) {
+                // the next pass's copies (an empty group for a thread past the row)
+                if (c + EP_THREADS < nvec)
+                    ep_issue<KM>(ep_stage + ((pass + 1) & 1) * KM * EP_THREADS, rows, sl, nvec,
+                                 c + EP_THREADS);
+                else
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
             } else {
-                float lo[L], hi[L];
-#pragma unroll
-                for (int e = 0; e < L; ++e) lo[e] = hi[e] = 0.0f;
-                walk_ranks<PROBS, BF16P, L, KM>(row, pk, valid, last, [&](int e, float p) {
-                    lo[e] = __fadd_rd(lo[e], p);
-                    hi[e] = __fadd_ru(hi[e], p);
-                });
-#pragma unroll
-                for (int e = 0; e < L; ++e) {
-                    const uint32_t a = bf16_bits(lo[e]), b = bf16_bits(hi[e]);
-                    bits[e] = static_cast<uint16_t>(a);
-                    if (a != b || (a & 0x7fffu) > 0x7f80u) open |= 1u << e;
-                }
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
             }
-            if (open) {
-#pragma unroll
-                for (int e = 0; e < L; ++e)
-                    if (open >> e & 1u)
-                        bits[e] = rank_sum_f64<PROBS, BF16P, KM>(row, pk, valid, last, e);
+            if (c < nvec) {
+                const uint4 *const mine = mine0 + (pass & 1) * KM * EP_THREADS;
+                const uint4 v = ep_vec<uint4, PROBS, BF16P, FP64, KM>(
+                    [&](int j) -> uint4 { return mine[j * EP_THREADS]; }, sl);
+                st_row(out + t * nvec + c, v);
             }
-            if (c < nvec) st_row(out + t * nvec + c, pack_bits(bits));
-        } else {
-            float acc[L];
-#pragma unroll
-            for (int e = 0; e < L; ++e) acc[e] = 0.0f;
-            if constexpr (BF16P && L == 8) {
-                walk_ranks2<PROBS, KM>(row, pk, valid, last, [&](int i, uint64_t p) {
-                    float lo, hi;
-                    f2_split(p, lo, hi);
-                    add_bf16x2(pack_bf16x2(lo, hi), acc[2 * i], acc[2 * i + 1]);
-                });
-            } else {
-                walk_ranks<PROBS, BF16P, L, KM>(row, pk, valid, last,
-                                            [&](int e, float p) { acc[e] = __fadd_rn(acc[e], p); });
-            }
-            if (c < nvec) st_row(out + t * nvec + c, pack(acc));
         }
     }
 }
@@ -497,6 +637,14 @@ void launch_ep(const void *rows, const float *probs, const int32_t *map, const i
     const int64_t per_block = EP_THREADS >> l;
     const unsigned blocks = (unsigned)((T + per_block - 1) / per_block);
     const size_t smem = ep_stage_bytes<V, KM>();
+    if constexpr (Lanes<V>::N == 8 && KM == 8) {
+        if (nvec >= EP_THREADS) {
+            (void)launch_pdl(k_unpermute_ep_token<PROBS, BF16P, FP64>, (unsigned)T, EP_THREADS,
+                             ep_token_stage_bytes<FP64>(), s, (const uint4 *)rows, probs, map,
+                             idx, T, K, nvec, per_rank, (uint4 *)out);
+            return;
+        }
+    }
     (void)launch_pdl(k_unpermute_ep<V, PROBS, BF16P, FP64, KM>, blocks, EP_THREADS, smem, s,
         (const V *)rows, probs, map, idx, T, K, nvec, l, per_rank, (V *)out);
 }
