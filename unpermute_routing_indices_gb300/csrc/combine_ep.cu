@@ -554,14 +554,17 @@ __global__ void __launch_bounds__(EP_THREADS, ep_min_blocks(KM))
 // same in every thread of the CTA, and the kernel has no token-group
 // arithmetic.  The fp32-sum forms keep two stage buffers (the next pass's
 // copies in flight while this one computes) at 6 CTAs per SM.  The fp64
-// forms need fewer registers here (50 against 76-78), and run one stage
+// forms need fewer registers here (60 against 76-78), and run one stage
 // buffer at 8 CTAs per SM: each pass's copies are waited for at once, while
-// the next pass's rows are prefetched into L2 (prefetch.global.L2), so that
-// its copies hit in L2.  Measured on the skewed T=16384, H=4096, ep=8
-// combine, against the general kernel: fp32 174.5 -> 171.5 us, bf16
-// partials 183.5 -> 174.7, fp64 sum with fp32 / bf16 partials 192.9 / 200.0
-// -> 179.3 / 187.0 (two buffers at 6 CTAs: 186.4 / 197.4; one buffer at 7,
-// 9 or 10 CTAs: 181.8-190.1 / 187.0-202.9).
+// the next pass's rows are prefetched into L2, so that its copies hit in L2.
+// One thread issues that prefetch as one bulk prefetch per slot (the pass's
+// vectors of a row are contiguous), which costs the other warps no issue
+// slots; a prefetch.global.L2 per thread and slot cost 8 instructions per
+// warp and pass.  Measured on the skewed T=16384, H=4096, ep=8 combine,
+// against the general kernel: fp32 174.5 -> 171.5 us, bf16 partials
+// 183.5 -> 174.7, fp64 sum with fp32 / bf16 partials 192.9 / 200.0 -> 178.7
+// / 181.6 (per-thread prefetches: 179.3 / 187.0; two buffers at 6 CTAs:
+// 186.4 / 197.4; one buffer at 7, 9 or 10 CTAs: 181.8-190.1 / 187.0-202.9).
 template <bool FP64>
 __host__ __device__ constexpr int ep_token_bufs() { return FP64 ? 1 : 2; }
 template <bool FP64>
@@ -591,12 +594,19 @@ __global__ void __launch_bounds__(EP_THREADS, FP64 ? 8 : 6)
     if constexpr (ep_token_bufs<FP64>() == 1) {
         for (int c = lane; c < nvec; c += EP_THREADS) {
             ep_issue<KM>(ep_stage, rows, sl, nvec, c);
-            const int cn = c + EP_THREADS;
+            // the next pass's rows, one contiguous run of up to EP_THREADS
+            // vectors per slot, prefetched into L2 by one thread (bulk
+            // prefetches: 16-byte aligned, whole vectors)
+            const int cn0 = c - lane + EP_THREADS;
+            if (threadIdx.x == 0 && cn0 < nvec) {
+                const int nbytes = (nvec - cn0 < EP_THREADS ? nvec - cn0 : EP_THREADS) * 16;
 #pragma unroll
-            for (int i = 0; i < KM; ++i)
-                if ((sl.valid >> i & 1u) && cn < nvec)
-                    asm volatile("prefetch.global.L2 [%0];"
-                                 ::"l"(rows + (int64_t)sl.rk[i] * nvec + cn));
+                for (int i = 0; i < KM; ++i)
+                    if (sl.valid >> i & 1u)
+                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                                     ::"l"(rows + (int64_t)sl.rk[i] * nvec + cn0), "r"(nbytes)
+                                     : "memory");
+            }
             asm volatile("cp.async.wait_group 0;" ::: "memory");
             const uint4 v = ep_vec<uint4, PROBS, BF16P, FP64, KM>(
                 [&](int j) -> uint4 { return mine0[j * EP_THREADS]; }, sl);
