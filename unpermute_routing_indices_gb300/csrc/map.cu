@@ -352,6 +352,9 @@ constexpr int MAP_MODE_PDL = 0, MAP_MODE_SCANNED = 1, MAP_MODE_SINGLE = 2, MAP_M
 constexpr int64_t MAP_SINGLE_MAX = MP_MAP_SINGLE_MAX;
 static_assert(MAP_SINGLE_MAX <= (int64_t)MAP_SUB * MAP_MAX_F, "one tile must hold the routes");
 
+#ifndef MP_MAP_CLUSTER_MAX
+#define MP_MAP_CLUSTER_MAX 16
+#endif
 template <int MODE, bool CACHE>
 __global__ void __launch_bounds__(MAP_THREADS)
     k_map_rank(const int32_t *__restrict__ idx, int64_t n, int E, int f, int ntiles, int cap,
@@ -459,11 +462,18 @@ __global__ void __launch_bounds__(MAP_THREADS)
         cluster_arrive();
         cluster_wait();    // every tile's histogram is visible across the cluster
         for (int b = tid; b <= E; b += MAP_THREADS) {
+            // every tile's count of b requested before any is added (one
+            // distributed-shared-memory round trip instead of one per tile:
+            // mid map, 12 tiles, 11.8 -> 11.0 us)
+            int32_t v[MP_MAP_CLUSTER_MAX];
+#pragma unroll
+            for (int c = 0; c < MP_MAP_CLUSTER_MAX; ++c)
+                v[c] = c < ntiles ? ld_cluster(s_tot + b, (unsigned)c) : 0;
             int32_t tot = 0, pre = 0;
-            for (int c = 0; c < ntiles; ++c) {
-                const int32_t v = ld_cluster(s_tot + b, (unsigned)c);
-                tot += v;
-                pre += (c < tile) ? v : 0;
+#pragma unroll
+            for (int c = 0; c < MP_MAP_CLUSTER_MAX; ++c) {
+                tot += v[c];
+                pre += (c < tile) ? v[c] : 0;
             }
             s_off[b] = (b < E) ? min(tot, cap) : 0;   // rows the expert keeps
             s_base[b] = pre;
@@ -606,9 +616,6 @@ inline size_t map_workspace_bytes(int64_t n, int E)
 
 // The cluster form: tiles of 2048 * f routes, f from MP_MAP_CLUSTER_F0 up to
 // MAP_MAX_F, one CTA each, at most MP_MAP_CLUSTER_MAX CTAs in the cluster.
-#ifndef MP_MAP_CLUSTER_MAX
-#define MP_MAP_CLUSTER_MAX 16
-#endif
 #ifndef MP_MAP_CLUSTER_F0
 #define MP_MAP_CLUSTER_F0 1
 #endif

@@ -467,6 +467,14 @@ inline bool vec_ok(int32_t H, std::initializer_list<const void *> ptrs)
 }
 
 constexpr int PERMUTE_VPT = MP_PERMUTE_VPT;
+#ifndef MP_PERMUTE_VPT_MID
+#define MP_PERMUTE_VPT_MID 2
+#endif
+// Rows of 129 to 256 vectors (1,032 to 2,048 bf16) take MP_PERMUTE_VPT_MID
+// vectors per thread, so that a token is one pass of a whole 128-thread CTA
+// rather than half a CTA: the T=4,096, H=2,048, K=6 fwd+bwd step 97.5 ->
+// 95.2 us.  With H=4,096 or 7,168 four per thread stay faster (two per
+// thread: T=16,384 step 868 -> 872 us).
 constexpr int UNPERMUTE_VPT = MP_UNPERMUTE_VPT;
 constexpr int BWD_VPT = MP_BWD_VPT;
 constexpr int ELEM_VPT = 8;
@@ -482,6 +490,17 @@ void launch_permute(const void *x, const float *probs, const int32_t *map, int64
     else
         (void)launch_pdl(k_permute<V, VPT, false>, g.blocks, ROW_THREADS, 0, s,
             (const V *)x, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr);
+}
+
+// The permute's row copy on 16-byte vectors (see PERMUTE_VPT above).
+inline void launch_permute_vec(const void *x, const float *probs, const int32_t *map,
+                               int64_t T, int K, int nvec, void *out, float *out_probs,
+                               cudaStream_t s)
+{
+    if (nvec > ROW_THREADS && nvec <= 2 * ROW_THREADS)
+        launch_permute<uint4, MP_PERMUTE_VPT_MID>(x, probs, map, T, K, nvec, out, out_probs, s);
+    else
+        launch_permute<uint4, PERMUTE_VPT>(x, probs, map, T, K, nvec, out, out_probs, s);
 }
 
 template <typename V, int VPT>
@@ -554,7 +573,7 @@ extern "C" mp_status_t mp_permute(const mp_bf16_t *x, const float *probs,
     if ((probs == nullptr) != (out_probs == nullptr)) return MP_ERR_INVALID_ARG;
     cudaStream_t s = as_stream(stream);
     if (vec_ok(H, {x, out}))
-        launch_permute<uint4, PERMUTE_VPT>(x, probs, row_id_map, T, K, H / 8, out, out_probs, s);
+        launch_permute_vec(x, probs, row_id_map, T, K, H / 8, out, out_probs, s);
     else
         launch_permute<uint16_t, ELEM_VPT>(x, probs, row_id_map, T, K, H, out, out_probs, s);
     return check_launch();
@@ -607,8 +626,7 @@ extern "C" mp_status_t mp_unpermute_bwd(const mp_bf16_t *g_y, const mp_bf16_t *r
     if (probs == nullptr) {
         // No merging probs: the token's gradient goes unchanged to each row.
         if (vec_ok(H, {g_y, g_rows}))
-            launch_permute<uint4, PERMUTE_VPT>(g_y, nullptr, row_id_map, T, K, H / 8, g_rows,
-                                               nullptr, s);
+            launch_permute_vec(g_y, nullptr, row_id_map, T, K, H / 8, g_rows, nullptr, s);
         else
             launch_permute<uint16_t, ELEM_VPT>(g_y, nullptr, row_id_map, T, K, H, g_rows, nullptr,
                                                s);
