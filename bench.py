@@ -57,14 +57,18 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     -k regex:"^<kernel>$" -s <n> -c 1 python bench.py --workload <w> --steps 3
     #     --warmup 3 --no-cpu --no-chunks --no-extras   (one pass per launch)
-    ("permute", "skewed", 16384): {"bytes": 135335680 + 1013217280, "src": "dab27408089bd60d"},
-    ("unpermute", "skewed", 16384): {"bytes": 1074811648 + 124241664, "src": "dab27408089bd60d"},
-    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209064704 + 1021931520, "src": "dab27408089bd60d"},
-    ("permute_bwd", "skewed", 16384): {"bytes": 1074286336 + 124208128, "src": "dab27408089bd60d"},
-    ("permute", "large", 32768): {"bytes": 472273664 + 3699056128, "src": "dab27408089bd60d"},
-    ("unpermute", "large", 32768): {"bytes": 3760316160 + 459798528, "src": "dab27408089bd60d"},
-    ("unpermute_bwd", "large", 32768): {"bytes": 4230583808 + 3709066496, "src": "dab27408089bd60d"},
-    ("permute_bwd", "large", 32768): {"bytes": 3759203840 + 459582464, "src": "dab27408089bd60d"},
+    ("permute", "mid", 4096): {"bytes": 16993536 + 39499264, "src": "b959d1c1d180bc7b"},
+    ("unpermute", "mid", 4096): {"bytes": 100873472 + 4257536, "src": "b959d1c1d180bc7b"},
+    ("unpermute_bwd", "mid", 4096): {"bytes": 117667328 + 41248000, "src": "b959d1c1d180bc7b"},
+    ("permute_bwd", "mid", 4096): {"bytes": 100787200 + 3976192, "src": "b959d1c1d180bc7b"},
+    ("permute", "skewed", 16384): {"bytes": 135339520 + 1013187584, "src": "b959d1c1d180bc7b"},
+    ("unpermute", "skewed", 16384): {"bytes": 1074830848 + 124274688, "src": "b959d1c1d180bc7b"},
+    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209063936 + 1021859840, "src": "b959d1c1d180bc7b"},
+    ("permute_bwd", "skewed", 16384): {"bytes": 1074286080 + 124511232, "src": "b959d1c1d180bc7b"},
+    ("permute", "large", 32768): {"bytes": 472371712 + 3698497280, "src": "b959d1c1d180bc7b"},
+    ("unpermute", "large", 32768): {"bytes": 3760239360 + 459808256, "src": "b959d1c1d180bc7b"},
+    ("unpermute_bwd", "large", 32768): {"bytes": 4230064128 + 3708571392, "src": "b959d1c1d180bc7b"},
+    ("permute_bwd", "large", 32768): {"bytes": 3759188224 + 459572992, "src": "b959d1c1d180bc7b"},
 }
 
 
