@@ -39,6 +39,23 @@ namespace {
 
 constexpr int ROW_THREADS = MP_ROW_THREADS;
 constexpr int KB = MP_SLOT_BATCH;  // slots whose rows are in flight together
+// The register-form gather and backward are also compiled for a batch of
+// KB_SMALL slots, which tokens of at most KB_SMALL slots take: the registers
+// of the unused slots of a KB batch cost resident CTAs.  On 16-byte vectors
+// that backward is compiled for 6 CTAs per SM (76 registers; the KB form for
+// 5, which it reaches at 92).
+// Measured on the T=4,096, H=2,048, K=6 fwd+bwd step: 95.2 -> 86.6 us
+// (unpermute_bwd 41.0 -> 36.8 us, unpermute 23.1 -> 22.2); either change
+// alone: 98.4 (slot batch, whose backward then took more registers) and
+// 92.9 us (CTA cap).  The cap on the KB form (K = 8) made the skewed
+// T=2,048 step slower (115.7 -> 117.9 us).
+constexpr int KB_SMALL = 6;
+// CTAs per SM the register-form backward is compiled for, by vector type
+// (16-byte vectors or single elements) and slot batch.
+__host__ __device__ constexpr int bwd_min_blocks(bool vec, int sb)
+{
+    return vec ? (sb <= KB_SMALL ? 6 : 5) : 3;
+}
 
 struct RowGrid {
     int tpt_log2;
@@ -96,7 +113,7 @@ __global__ void __launch_bounds__(ROW_THREADS)
 }
 
 // acc = fmaf(p, r, acc) per slot in slot order (PROBS), or acc = acc + r.
-template <typename V, int VPT, bool PROBS, bool GATHER_PROBS>
+template <typename V, int VPT, bool PROBS, bool GATHER_PROBS, int SB>
 __global__ void __launch_bounds__(ROW_THREADS)
     k_unpermute(const V *__restrict__ rows, const float *__restrict__ probs,
                 const int32_t *__restrict__ map, int64_t T, int K, int nvec, int tpt_log2,
@@ -117,18 +134,18 @@ __global__ void __launch_bounds__(ROW_THREADS)
         for (int j = 0; j < VPT; ++j)
 #pragma unroll
             for (int e = 0; e < L; ++e) acc[j][e] = 0.0f;
-        for (int kb = 0; kb < K; kb += KB) {
-            int32_t rk[KB];
-            float pk[KB];
+        for (int kb = 0; kb < K; kb += SB) {
+            int32_t rk[SB];
+            float pk[SB];
 #pragma unroll
-            for (int i = 0; i < KB; ++i) {
+            for (int i = 0; i < SB; ++i) {
                 const int k = kb + i;
                 rk[i] = (k < K) ? __ldg(m + k) : -1;
                 pk[i] = (PROBS && k < K) ? __ldg(probs + t * K + k) : 1.0f;
             }
-            V r[KB][VPT];
+            V r[SB][VPT];
 #pragma unroll
-            for (int i = 0; i < KB; ++i)
+            for (int i = 0; i < SB; ++i)
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
                     const int c = c0 + j * tpt + lane;
@@ -136,7 +153,7 @@ __global__ void __launch_bounds__(ROW_THREADS)
                                                        : zero_vec<V>();
                 }
 #pragma unroll
-            for (int i = 0; i < KB; ++i) {
+            for (int i = 0; i < SB; ++i) {
                 if (rk[i] < 0) continue;
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
@@ -164,8 +181,8 @@ __global__ void __launch_bounds__(ROW_THREADS)
 
 // Backward of the weighted combine.  All threads stay to the end (the probs
 // gradient is a CTA reduction), so tokens past T run with no routed slot.
-template <typename V, int VPT>
-__global__ void __launch_bounds__(ROW_THREADS)
+template <typename V, int VPT, int SB>
+__global__ void __launch_bounds__(ROW_THREADS, bwd_min_blocks(Lanes<V>::N == 8, SB))
     k_unpermute_bwd(const V *__restrict__ gy, const V *__restrict__ rows,
                     const float *__restrict__ probs, const int32_t *__restrict__ map, int64_t T,
                     int K, int nvec, int tpt_log2, V *__restrict__ g_rows,
@@ -174,18 +191,18 @@ __global__ void __launch_bounds__(ROW_THREADS)
     pdl_trigger();
     pdl_wait();
     constexpr int L = Lanes<V>::N;
-    __shared__ float s_red[ROW_THREADS / 32][KB];
+    __shared__ float s_red[ROW_THREADS / 32][SB];
     const int tpt = 1 << tpt_log2;
     const int lane = threadIdx.x & (tpt - 1);
     const int64_t t = (int64_t)blockIdx.x * (ROW_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
     const bool active = t < T;
     const int32_t *m = map + t * K;
 
-    for (int kb = 0; kb < K; kb += KB) {
-        int32_t rk[KB];
-        float pk[KB], dot[KB];
+    for (int kb = 0; kb < K; kb += SB) {
+        int32_t rk[SB];
+        float pk[SB], dot[SB];
 #pragma unroll
-        for (int i = 0; i < KB; ++i) {
+        for (int i = 0; i < SB; ++i) {
             const int k = kb + i;
             rk[i] = (active && k < K) ? __ldg(m + k) : -1;
             pk[i] = (active && k < K) ? __ldg(probs + t * K + k) : 0.0f;
@@ -193,14 +210,14 @@ __global__ void __launch_bounds__(ROW_THREADS)
         }
         for (int c0 = 0; c0 < nvec; c0 += tpt * VPT) {
             V g[VPT];
-            V r[KB][VPT];
+            V r[SB][VPT];
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
                 const int c = c0 + j * tpt + lane;
                 g[j] = (active && c < nvec) ? ld_stream(gy + t * nvec + c) : zero_vec<V>();
             }
 #pragma unroll
-            for (int i = 0; i < KB; ++i)
+            for (int i = 0; i < SB; ++i)
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
                     const int c = c0 + j * tpt + lane;
@@ -208,7 +225,7 @@ __global__ void __launch_bounds__(ROW_THREADS)
                                                        : zero_vec<V>();
                 }
 #pragma unroll
-            for (int i = 0; i < KB; ++i) {
+            for (int i = 0; i < SB; ++i) {
                 if (rk[i] < 0) continue;
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
@@ -230,17 +247,17 @@ __global__ void __launch_bounds__(ROW_THREADS)
         // inside the warp, then the token's warps in order.
         const int width = tpt < 32 ? tpt : 32;
 #pragma unroll
-        for (int i = 0; i < KB; ++i)
+        for (int i = 0; i < SB; ++i)
             for (int o = width >> 1; o > 0; o >>= 1) dot[i] += __shfl_xor_sync(FULL_MASK, dot[i], o);
         if (tpt > 32) {
             const int warp = threadIdx.x >> 5;
             if ((threadIdx.x & 31) == 0)
 #pragma unroll
-                for (int i = 0; i < KB; ++i) s_red[warp][i] = dot[i];
+                for (int i = 0; i < SB; ++i) s_red[warp][i] = dot[i];
             __syncthreads();
             if (active && lane == 0) {
                 const int w0 = warp, nw = tpt >> 5;
-                for (int i = 0; i < KB && kb + i < K; ++i) {
+                for (int i = 0; i < SB && kb + i < K; ++i) {
                     float s = 0.0f;
                     for (int w = 0; w < nw; ++w) s += s_red[w0 + w][i];
                     g_probs[t * K + kb + i] = rk[i] >= 0 ? s : 0.0f;
@@ -248,7 +265,7 @@ __global__ void __launch_bounds__(ROW_THREADS)
             }
             __syncthreads();
         } else if (active && lane == 0) {
-            for (int i = 0; i < KB && kb + i < K; ++i)
+            for (int i = 0; i < SB && kb + i < K; ++i)
                 g_probs[t * K + kb + i] = rk[i] >= 0 ? dot[i] : 0.0f;
         }
     }
@@ -503,6 +520,23 @@ inline void launch_permute_vec(const void *x, const float *probs, const int32_t 
         launch_permute<uint4, PERMUTE_VPT>(x, probs, map, T, K, nvec, out, out_probs, s);
 }
 
+template <typename V, int VPT, int SB>
+void launch_unpermute_reg(const RowGrid &g, const void *rows, const float *probs,
+                          const int32_t *map, int64_t T, int K, int nvec, void *out,
+                          const float *g_out_probs, float *g_probs, cudaStream_t s)
+{
+    if (probs != nullptr)
+        (void)launch_pdl(k_unpermute<V, VPT, true, false, SB>, g.blocks, ROW_THREADS, 0, s,
+            (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr, nullptr);
+    else if (g_probs != nullptr)
+        (void)launch_pdl(k_unpermute<V, VPT, false, true, SB>, g.blocks, ROW_THREADS, 0, s,
+            (const V *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, g_out_probs,
+            g_probs);
+    else
+        (void)launch_pdl(k_unpermute<V, VPT, false, false, SB>, g.blocks, ROW_THREADS, 0, s,
+            (const V *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr, nullptr);
+}
+
 template <typename V, int VPT>
 void launch_unpermute(const void *rows, const float *probs, const int32_t *map, int64_t T, int K,
                       int nvec, void *out, const float *g_out_probs, float *g_probs,
@@ -527,16 +561,12 @@ void launch_unpermute(const void *rows, const float *probs, const int32_t *map, 
             return;
         }
     }
-    if (probs != nullptr)
-        (void)launch_pdl(k_unpermute<V, VPT, true, false>, g.blocks, ROW_THREADS, 0, s,
-            (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr, nullptr);
-    else if (g_probs != nullptr)
-        (void)launch_pdl(k_unpermute<V, VPT, false, true>, g.blocks, ROW_THREADS, 0, s,
-            (const V *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, g_out_probs,
-            g_probs);
+    if (K <= KB_SMALL)
+        launch_unpermute_reg<V, VPT, KB_SMALL>(g, rows, probs, map, T, K, nvec, out, g_out_probs,
+                                               g_probs, s);
     else
-        (void)launch_pdl(k_unpermute<V, VPT, false, false>, g.blocks, ROW_THREADS, 0, s,
-            (const V *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (V *)out, nullptr, nullptr);
+        launch_unpermute_reg<V, VPT, KB>(g, rows, probs, map, T, K, nvec, out, g_out_probs,
+                                         g_probs, s);
 }
 
 template <typename V, int VPT>
@@ -554,8 +584,14 @@ void launch_unpermute_bwd(const void *gy, const void *rows, const float *probs,
             return;
         }
     }
-    (void)launch_pdl(k_unpermute_bwd<V, VPT>, g.blocks, ROW_THREADS, 0, s,
-        (const V *)gy, (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)g_rows, g_probs);
+    if (K <= KB_SMALL)
+        (void)launch_pdl(k_unpermute_bwd<V, VPT, KB_SMALL>, g.blocks, ROW_THREADS, 0, s,
+            (const V *)gy, (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)g_rows,
+            g_probs);
+    else
+        (void)launch_pdl(k_unpermute_bwd<V, VPT, KB>, g.blocks, ROW_THREADS, 0, s,
+            (const V *)gy, (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)g_rows,
+            g_probs);
 }
 
 }  // namespace
