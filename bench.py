@@ -57,18 +57,18 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     -k regex:"^<kernel>$" -s <n> -c 1 python bench.py --workload <w> --steps 3
     #     --warmup 3 --no-cpu --no-chunks --no-extras   (one pass per launch)
-    ("permute", "mid", 4096): {"bytes": 16993536 + 39499264, "src": "b959d1c1d180bc7b"},
-    ("unpermute", "mid", 4096): {"bytes": 100873472 + 4257536, "src": "b959d1c1d180bc7b"},
-    ("unpermute_bwd", "mid", 4096): {"bytes": 117667328 + 41248000, "src": "b959d1c1d180bc7b"},
-    ("permute_bwd", "mid", 4096): {"bytes": 100787200 + 3976192, "src": "b959d1c1d180bc7b"},
-    ("permute", "skewed", 16384): {"bytes": 135339520 + 1013187584, "src": "b959d1c1d180bc7b"},
-    ("unpermute", "skewed", 16384): {"bytes": 1074830848 + 124274688, "src": "b959d1c1d180bc7b"},
-    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209063936 + 1021859840, "src": "b959d1c1d180bc7b"},
-    ("permute_bwd", "skewed", 16384): {"bytes": 1074286080 + 124511232, "src": "b959d1c1d180bc7b"},
-    ("permute", "large", 32768): {"bytes": 472371712 + 3698497280, "src": "b959d1c1d180bc7b"},
-    ("unpermute", "large", 32768): {"bytes": 3760239360 + 459808256, "src": "b959d1c1d180bc7b"},
-    ("unpermute_bwd", "large", 32768): {"bytes": 4230064128 + 3708571392, "src": "b959d1c1d180bc7b"},
-    ("permute_bwd", "large", 32768): {"bytes": 3759188224 + 459572992, "src": "b959d1c1d180bc7b"},
+    ("permute", "mid", 4096): {"bytes": 16989440 + 39174400, "src": "c4dd9e7044a01074"},
+    ("unpermute", "mid", 4096): {"bytes": 100872448 + 4094976, "src": "c4dd9e7044a01074"},
+    ("unpermute_bwd", "mid", 4096): {"bytes": 117660928 + 41899264, "src": "c4dd9e7044a01074"},
+    ("permute_bwd", "mid", 4096): {"bytes": 100773888 + 4072704, "src": "c4dd9e7044a01074"},
+    ("permute", "skewed", 16384): {"bytes": 135334144 + 1013267200, "src": "c4dd9e7044a01074"},
+    ("unpermute", "skewed", 16384): {"bytes": 1074813184 + 124237824, "src": "c4dd9e7044a01074"},
+    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209104896 + 1021850880, "src": "c4dd9e7044a01074"},
+    ("permute_bwd", "skewed", 16384): {"bytes": 1074301440 + 124519680, "src": "c4dd9e7044a01074"},
+    ("permute", "large", 32768): {"bytes": 472343552 + 3698615040, "src": "c4dd9e7044a01074"},
+    ("unpermute", "large", 32768): {"bytes": 3760238848 + 459857664, "src": "c4dd9e7044a01074"},
+    ("unpermute_bwd", "large", 32768): {"bytes": 4230624000 + 3708288768, "src": "c4dd9e7044a01074"},
+    ("permute_bwd", "large", 32768): {"bytes": 3759191552 + 459753728, "src": "c4dd9e7044a01074"},
 }
 
 
