@@ -42,19 +42,20 @@ constexpr int KB = MP_SLOT_BATCH;  // slots whose rows are in flight together
 // The register-form gather and backward are also compiled for a batch of
 // KB_SMALL slots, which tokens of at most KB_SMALL slots take: the registers
 // of the unused slots of a KB batch cost resident CTAs.  On 16-byte vectors
-// that backward is compiled for 6 CTAs per SM (76 registers; the KB form for
-// 5, which it reaches at 92).
-// Measured on the T=4,096, H=2,048, K=6 fwd+bwd step: 95.2 -> 86.6 us
-// (unpermute_bwd 41.0 -> 36.8 us, unpermute 23.1 -> 22.2); either change
-// alone: 98.4 (slot batch, whose backward then took more registers) and
-// 92.9 us (CTA cap).  The cap on the KB form (K = 8) made the skewed
-// T=2,048 step slower (115.7 -> 117.9 us).
+// that backward is compiled for 8 CTAs per SM (64 registers, no spills; the
+// KB form for 5, which it reaches at 92 to 94).  Measured on the T=4,096,
+// H=2,048, K=6 fwd+bwd step: 95.2 -> 86.6 us with 6 CTAs per SM
+// (unpermute_bwd 41.0 -> 36.8 us, unpermute 23.1 -> 22.2), 84.8 us with 8
+// (unpermute_bwd 34.7 us; 7: 84.7 / 34.9); either change alone: 98.4 (slot
+// batch, whose backward then took more registers) and 92.9 us (a cap of 6).
+// A cap of 6 on the KB form (K = 8) made the skewed T=2,048 step slower
+// (115.7 -> 117.9 us).
 constexpr int KB_SMALL = 6;
 // CTAs per SM the register-form backward is compiled for, by vector type
 // (16-byte vectors or single elements) and slot batch.
 __host__ __device__ constexpr int bwd_min_blocks(bool vec, int sb)
 {
-    return vec ? (sb <= KB_SMALL ? 6 : 5) : 3;
+    return vec ? (sb <= KB_SMALL ? 8 : 5) : 3;
 }
 
 struct RowGrid {
