@@ -57,18 +57,18 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     -k regex:"^<kernel>$" -s <n> -c 1 python bench.py --workload <w> --steps 3
     #     --warmup 3 --no-cpu --no-chunks --no-extras   (one pass per launch)
-    ("permute", "mid", 4096): {"bytes": 16989440 + 39174400, "src": "c4dd9e7044a01074"},
-    ("unpermute", "mid", 4096): {"bytes": 100872448 + 4094976, "src": "c4dd9e7044a01074"},
-    ("unpermute_bwd", "mid", 4096): {"bytes": 117660928 + 41899264, "src": "c4dd9e7044a01074"},
-    ("permute_bwd", "mid", 4096): {"bytes": 100773888 + 4072704, "src": "c4dd9e7044a01074"},
-    ("permute", "skewed", 16384): {"bytes": 135334144 + 1013267200, "src": "c4dd9e7044a01074"},
-    ("unpermute", "skewed", 16384): {"bytes": 1074813184 + 124237824, "src": "c4dd9e7044a01074"},
-    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209104896 + 1021850880, "src": "c4dd9e7044a01074"},
-    ("permute_bwd", "skewed", 16384): {"bytes": 1074301440 + 124519680, "src": "c4dd9e7044a01074"},
-    ("permute", "large", 32768): {"bytes": 472343552 + 3698615040, "src": "c4dd9e7044a01074"},
-    ("unpermute", "large", 32768): {"bytes": 3760238848 + 459857664, "src": "c4dd9e7044a01074"},
-    ("unpermute_bwd", "large", 32768): {"bytes": 4230624000 + 3708288768, "src": "c4dd9e7044a01074"},
-    ("permute_bwd", "large", 32768): {"bytes": 3759191552 + 459753728, "src": "c4dd9e7044a01074"},
+    ("permute", "mid", 4096): {"bytes": 16990464 + 39254528, "src": "1c0a28e1144275b0"},
+    ("unpermute", "mid", 4096): {"bytes": 100872960 + 4060672, "src": "1c0a28e1144275b0"},
+    ("unpermute_bwd", "mid", 4096): {"bytes": 117664768 + 42771968, "src": "1c0a28e1144275b0"},
+    ("permute_bwd", "mid", 4096): {"bytes": 100771072 + 3945728, "src": "1c0a28e1144275b0"},
+    ("permute", "skewed", 16384): {"bytes": 135437568 + 1013096448, "src": "1c0a28e1144275b0"},
+    ("unpermute", "skewed", 16384): {"bytes": 1074814976 + 124522752, "src": "1c0a28e1144275b0"},
+    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209067008 + 1021527296, "src": "1c0a28e1144275b0"},
+    ("permute_bwd", "skewed", 16384): {"bytes": 1074287104 + 124530432, "src": "1c0a28e1144275b0"},
+    ("permute", "large", 32768): {"bytes": 472401152 + 3698638848, "src": "1c0a28e1144275b0"},
+    ("unpermute", "large", 32768): {"bytes": 3760240896 + 459783168, "src": "1c0a28e1144275b0"},
+    ("unpermute_bwd", "large", 32768): {"bytes": 4230095360 + 3708396544, "src": "1c0a28e1144275b0"},
+    ("permute_bwd", "large", 32768): {"bytes": 3759373312 + 459304448, "src": "1c0a28e1144275b0"},
 }
 
 
