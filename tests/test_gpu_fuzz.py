@@ -54,7 +54,27 @@ def _routed_case(rng):
 @pytest.mark.parametrize("seed", range(24))
 def test_routed_ops_fuzz(seed):
     rng = np.random.default_rng(9000 + seed)
-    T, K, E, H, idx, probs, x, rows, gy, off = _routed_case(rng)
+    _check_routed(rng, *_routed_case(rng))
+
+
+# K across the slot batches of the register row kernels (6 and 8 slots, two
+# batches past 8), on rows that take one pass per CTA (2,048), a ragged
+# second pass (1,032) and the element path (1,001)
+@pytest.mark.parametrize("K", [5, 6, 7, 9, 14])
+@pytest.mark.parametrize("H", [2048, 1032, 1001])
+def test_routed_ops_across_slot_batches(K, H):
+    rng = np.random.default_rng(K * 10007 + H)
+    T, E = 300, 64
+    idx = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    idx[rng.random((T, K)) < 0.1] = -1
+    probs = rng.random((T, K)).astype(np.float32) + np.float32(1e-3)
+    x = wl.random_rows(T, H, K + 1)
+    rows = wl.random_rows(T * K, H, K + 2)
+    gy = wl.random_rows(T, H, K + 3)
+    _check_routed(rng, T, K, E, H, idx, probs, x, rows, gy, 0)
+
+
+def _check_routed(rng, T, K, E, H, idx, probs, x, rows, gy, off):
     o_rim, o_s2f, o_counts, o_offsets, _ = oracle.build_map(idx, E)
     rim, s2f, counts, offsets = mp.mp_build_map(d(idx), E)
     for got, want in ((rim, o_rim), (s2f, o_s2f), (counts, o_counts), (offsets, o_offsets)):
