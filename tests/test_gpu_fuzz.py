@@ -57,10 +57,10 @@ def test_routed_ops_fuzz(seed):
     _check_routed(rng, *_routed_case(rng))
 
 
-# K across the slot batches of the register row kernels (6 and 8 slots, two
-# batches past 8), on rows that take one pass per CTA (2,048), a ragged
-# second pass (1,032) and the element path (1,001)
-@pytest.mark.parametrize("K", [5, 6, 7, 9, 14])
+# K across the slot batches of the register row kernels (2, 4, 6 and 8
+# slots, two batches past 8), on rows that take one pass per CTA (2,048), a
+# ragged second pass (1,032) and the element path (1,001)
+@pytest.mark.parametrize("K", [2, 3, 5, 6, 7, 9, 14])
 @pytest.mark.parametrize("H", [2048, 1032, 1001])
 def test_routed_ops_across_slot_batches(K, H):
     rng = np.random.default_rng(K * 10007 + H)

@@ -39,9 +39,11 @@ namespace {
 
 constexpr int ROW_THREADS = MP_ROW_THREADS;
 constexpr int KB = MP_SLOT_BATCH;  // slots whose rows are in flight together
-// The register-form gather and backward are also compiled for a batch of
-// KB_SMALL slots, which tokens of at most KB_SMALL slots take: the registers
-// of the unused slots of a KB batch cost resident CTAs.  On 16-byte vectors
+// The register-form gather and backward are also compiled for batches of
+// 2, 4 and KB_SMALL slots, which tokens of at most that many slots take: the
+// registers of the unused slots of a KB batch cost resident CTAs (K = 2,
+// 8,192 tokens of 4,096: fwd+bwd step 165.7 -> 148.7 us; 4,096 tokens of
+// 2,048: 52.3 -> 44.0; K = 4: 253.7 -> 250.8 and 64.2 -> 60.8).  On 16-byte vectors
 // that backward is compiled for 8 CTAs per SM (64 registers, no spills; the
 // KB form for 5, which it reaches at 92 to 94).  Measured on the T=4,096,
 // H=2,048, K=6 fwd+bwd step: 95.2 -> 86.6 us with 6 CTAs per SM
@@ -562,7 +564,13 @@ void launch_unpermute(const void *rows, const float *probs, const int32_t *map, 
             return;
         }
     }
-    if (K <= KB_SMALL)
+    if (K <= 2)
+        launch_unpermute_reg<V, VPT, 2>(g, rows, probs, map, T, K, nvec, out, g_out_probs,
+                                        g_probs, s);
+    else if (K <= 4)
+        launch_unpermute_reg<V, VPT, 4>(g, rows, probs, map, T, K, nvec, out, g_out_probs,
+                                        g_probs, s);
+    else if (K <= KB_SMALL)
         launch_unpermute_reg<V, VPT, KB_SMALL>(g, rows, probs, map, T, K, nvec, out, g_out_probs,
                                                g_probs, s);
     else
@@ -585,7 +593,15 @@ void launch_unpermute_bwd(const void *gy, const void *rows, const float *probs,
             return;
         }
     }
-    if (K <= KB_SMALL)
+    if (K <= 2)
+        (void)launch_pdl(k_unpermute_bwd<V, VPT, 2>, g.blocks, ROW_THREADS, 0, s,
+            (const V *)gy, (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)g_rows,
+            g_probs);
+    else if (K <= 4)
+        (void)launch_pdl(k_unpermute_bwd<V, VPT, 4>, g.blocks, ROW_THREADS, 0, s,
+            (const V *)gy, (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)g_rows,
+            g_probs);
+    else if (K <= KB_SMALL)
         (void)launch_pdl(k_unpermute_bwd<V, VPT, KB_SMALL>, g.blocks, ROW_THREADS, 0, s,
             (const V *)gy, (const V *)rows, probs, map, T, K, nvec, g.tpt_log2, (V *)g_rows,
             g_probs);
