@@ -57,18 +57,18 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     -k regex:"^<kernel>$" -s <n> -c 1 python bench.py --workload <w> --steps 3
     #     --warmup 3 --no-cpu --no-chunks --no-extras   (one pass per launch)
-    ("permute", "mid", 4096): {"bytes": 16990464 + 39254528, "src": "1c0a28e1144275b0"},
-    ("unpermute", "mid", 4096): {"bytes": 100872960 + 4060672, "src": "1c0a28e1144275b0"},
-    ("unpermute_bwd", "mid", 4096): {"bytes": 117664768 + 42771968, "src": "1c0a28e1144275b0"},
-    ("permute_bwd", "mid", 4096): {"bytes": 100771072 + 3945728, "src": "1c0a28e1144275b0"},
-    ("permute", "skewed", 16384): {"bytes": 135437568 + 1013096448, "src": "1c0a28e1144275b0"},
-    ("unpermute", "skewed", 16384): {"bytes": 1074814976 + 124522752, "src": "1c0a28e1144275b0"},
-    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209067008 + 1021527296, "src": "1c0a28e1144275b0"},
-    ("permute_bwd", "skewed", 16384): {"bytes": 1074287104 + 124530432, "src": "1c0a28e1144275b0"},
-    ("permute", "large", 32768): {"bytes": 472401152 + 3698638848, "src": "1c0a28e1144275b0"},
-    ("unpermute", "large", 32768): {"bytes": 3760240896 + 459783168, "src": "1c0a28e1144275b0"},
-    ("unpermute_bwd", "large", 32768): {"bytes": 4230095360 + 3708396544, "src": "1c0a28e1144275b0"},
-    ("permute_bwd", "large", 32768): {"bytes": 3759373312 + 459304448, "src": "1c0a28e1144275b0"},
+    ("permute", "mid", 4096): {"bytes": 16991744 + 39191296, "src": "df7ab508c8f22d57"},
+    ("unpermute", "mid", 4096): {"bytes": 100872448 + 4431360, "src": "df7ab508c8f22d57"},
+    ("unpermute_bwd", "mid", 4096): {"bytes": 117661696 + 43040768, "src": "df7ab508c8f22d57"},
+    ("permute_bwd", "mid", 4096): {"bytes": 100773376 + 3946496, "src": "df7ab508c8f22d57"},
+    ("permute", "skewed", 16384): {"bytes": 135343616 + 1013358080, "src": "df7ab508c8f22d57"},
+    ("unpermute", "skewed", 16384): {"bytes": 1074822400 + 124493824, "src": "df7ab508c8f22d57"},
+    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209082624 + 1021869568, "src": "df7ab508c8f22d57"},
+    ("permute_bwd", "skewed", 16384): {"bytes": 1074288128 + 124353024, "src": "df7ab508c8f22d57"},
+    ("permute", "large", 32768): {"bytes": 472726784 + 3698916096, "src": "df7ab508c8f22d57"},
+    ("unpermute", "large", 32768): {"bytes": 3760239360 + 459858688, "src": "df7ab508c8f22d57"},
+    ("unpermute_bwd", "large", 32768): {"bytes": 4230139904 + 3709153280, "src": "df7ab508c8f22d57"},
+    ("permute_bwd", "large", 32768): {"bytes": 3759262208 + 459578880, "src": "df7ab508c8f22d57"},
 }
 
 
