@@ -39,11 +39,14 @@ namespace {
 
 constexpr int ROW_THREADS = MP_ROW_THREADS;
 constexpr int KB = MP_SLOT_BATCH;  // slots whose rows are in flight together
-// The register-form gather and backward are also compiled for batches of
-// 2, 4 and KB_SMALL slots, which tokens of at most that many slots take: the
-// registers of the unused slots of a KB batch cost resident CTAs (K = 2,
-// 8,192 tokens of 4,096: fwd+bwd step 165.7 -> 148.7 us; 4,096 tokens of
-// 2,048: 52.3 -> 44.0; K = 4: 253.7 -> 250.8 and 64.2 -> 60.8).  On 16-byte vectors
+// The gathers and the backward, register and staged forms, are also
+// compiled for batches of 2, 4 and KB_SMALL slots, which tokens of at most
+// that many slots take: the registers (and, staged, the shared memory) of the
+// unused slots of a KB batch cost resident CTAs.  K = 2, 8,192 tokens of
+// 4,096 (register forms): fwd+bwd step 165.7 -> 148.7 us; 4,096 tokens of
+// 2,048: 52.3 -> 44.0; K = 4: 253.7 -> 250.8 and 64.2 -> 60.8.  Staged
+// forms, K = 2, 16,384 / 32,768 tokens of 4,096: 328.2 / 632.0 -> 283.3 /
+// 547.7 us; K = 4, 32,768 tokens of 2,048: 519.1 -> 479.1.  On 16-byte vectors
 // that backward is compiled for 8 CTAs per SM (64 registers, no spills; the
 // KB form for 5, which it reaches at 92 to 94).  Measured on the T=4,096,
 // H=2,048, K=6 fwd+bwd step: 95.2 -> 86.6 us with 6 CTAs per SM
@@ -274,8 +277,9 @@ __global__ void __launch_bounds__(ROW_THREADS, bwd_min_blocks(Lanes<V>::N == 8, 
     }
 }
 
-// Staged forms (16-byte vectors, one vector per thread per pass, K <= KB).
-// Each thread copies its own slots' row vectors (and, backward, g_y's) into
+// Staged forms (16-byte vectors, one vector per thread per pass, K <= SB, a
+// slot batch; the shared memory holds SB slots per buffer, plus g_y's
+// backward).  Each thread copies its own slots' row vectors (and g_y's) into
 // shared memory with cp.async and reads back only those, so no barrier is
 // needed.  Two buffers keep a pass ahead: the copies for pass p + 1 are issued
 // before pass p is computed, so the rows hold no registers while in flight
@@ -283,8 +287,9 @@ __global__ void __launch_bounds__(ROW_THREADS, bwd_min_blocks(Lanes<V>::N == 8, 
 // same order, as k_unpermute / k_unpermute_bwd.
 constexpr int STAGE_BUFS = 2;
 // The staged forms run only on grids of at least this many CTAs, for the
-// gathers and the backward alike.  Their shared memory caps an SM at 6 CTAs
-// where the register forms run 7 (gathers) or 5 (backward).  On the skewed
+// gathers and the backward alike.  With 8-slot batches their shared memory
+// caps an SM at 6 CTAs where the register forms run 7 (gathers) or 5
+// (backward).  On the skewed
 // fwd+bwd step (H=4096, one token per CTA) the staged kernels make the step
 // faster from 16,384 tokens (0.880 -> 0.870 ms; 32,768: 1.731 -> 1.695;
 // 65,536: 3.433 -> 3.350) and slower below (4,096: 0.231 -> 0.241 ms).  A
@@ -330,7 +335,7 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <bool PROBS, bool GATHER_PROBS>
+template <bool PROBS, bool GATHER_PROBS, int SB>
 __global__ void __launch_bounds__(ROW_THREADS)
     k_unpermute_staged(const uint4 *__restrict__ rows, const float *__restrict__ probs,
                        const int32_t *__restrict__ map, int64_t T, int K, int nvec,
@@ -339,23 +344,23 @@ __global__ void __launch_bounds__(ROW_THREADS)
 {
     pdl_trigger();
     pdl_wait();
-    extern __shared__ uint4 row_stage[];   // [STAGE_BUFS][KB][ROW_THREADS]
+    extern __shared__ uint4 row_stage[];   // [STAGE_BUFS][SB][ROW_THREADS]
     const int tpt = 1 << tpt_log2;
     const int lane = threadIdx.x & (tpt - 1);
     const int64_t t = (int64_t)blockIdx.x * (ROW_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
     if (t >= T) return;
     const int32_t *m = map + t * K;
-    int32_t rk[KB];
-    float pk[KB];
+    int32_t rk[SB];
+    float pk[SB];
 #pragma unroll
-    for (int i = 0; i < KB; ++i) {
+    for (int i = 0; i < SB; ++i) {
         rk[i] = (i < K) ? __ldg(m + i) : -1;
         pk[i] = (PROBS && i < K) ? __ldg(probs + t * K + i) : 1.0f;
     }
     const auto issue = [&](int c, int buf) {
-        uint4 *const dst = row_stage + buf * KB * ROW_THREADS + threadIdx.x;
+        uint4 *const dst = row_stage + buf * SB * ROW_THREADS + threadIdx.x;
 #pragma unroll
-        for (int i = 0; i < KB; ++i)
+        for (int i = 0; i < SB; ++i)
             if (rk[i] >= 0) cp_async16(dst + i * ROW_THREADS, rows + (int64_t)rk[i] * nvec + c);
         cp_async_commit();
     };
@@ -368,12 +373,12 @@ __global__ void __launch_bounds__(ROW_THREADS)
         } else {
             cp_async_wait<0>();
         }
-        const uint4 *const mine = row_stage + (pass & 1) * KB * ROW_THREADS + threadIdx.x;
+        const uint4 *const mine = row_stage + (pass & 1) * SB * ROW_THREADS + threadIdx.x;
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < KB; ++i) {
+        for (int i = 0; i < SB; ++i) {
             if (rk[i] < 0) continue;
             float f[8];
             unpack(mine[i * ROW_THREADS], f);
@@ -391,6 +396,7 @@ __global__ void __launch_bounds__(ROW_THREADS)
     }
 }
 
+template <int SB>
 __global__ void __launch_bounds__(ROW_THREADS)
     k_unpermute_bwd_staged(const uint4 *__restrict__ gy, const uint4 *__restrict__ rows,
                            const float *__restrict__ probs, const int32_t *__restrict__ map,
@@ -399,26 +405,26 @@ __global__ void __launch_bounds__(ROW_THREADS)
 {
     pdl_trigger();
     pdl_wait();
-    extern __shared__ uint4 row_stage[];   // [STAGE_BUFS][KB + 1][ROW_THREADS]; slot KB: g_y
-    __shared__ float s_red[ROW_THREADS / 32][KB];
+    extern __shared__ uint4 row_stage[];   // [STAGE_BUFS][SB + 1][ROW_THREADS]; slot SB: g_y
+    __shared__ float s_red[ROW_THREADS / 32][SB];
     const int tpt = 1 << tpt_log2;
     const int lane = threadIdx.x & (tpt - 1);
     const int64_t t = (int64_t)blockIdx.x * (ROW_THREADS >> tpt_log2) + (threadIdx.x >> tpt_log2);
     const bool active = t < T;
     const int32_t *m = map + t * K;
-    int32_t rk[KB];
-    float pk[KB], dot[KB];
+    int32_t rk[SB];
+    float pk[SB], dot[SB];
 #pragma unroll
-    for (int i = 0; i < KB; ++i) {
+    for (int i = 0; i < SB; ++i) {
         rk[i] = (active && i < K) ? __ldg(m + i) : -1;
         pk[i] = (active && i < K) ? __ldg(probs + t * K + i) : 0.0f;
         dot[i] = 0.0f;
     }
     const auto issue = [&](int c, int buf) {
-        uint4 *const dst = row_stage + buf * (KB + 1) * ROW_THREADS + threadIdx.x;
-        cp_async16(dst + KB * ROW_THREADS, gy + t * nvec + c);
+        uint4 *const dst = row_stage + buf * (SB + 1) * ROW_THREADS + threadIdx.x;
+        cp_async16(dst + SB * ROW_THREADS, gy + t * nvec + c);
 #pragma unroll
-        for (int i = 0; i < KB; ++i)
+        for (int i = 0; i < SB; ++i)
             if (rk[i] >= 0) cp_async16(dst + i * ROW_THREADS, rows + (int64_t)rk[i] * nvec + c);
         cp_async_commit();
     };
@@ -432,11 +438,11 @@ __global__ void __launch_bounds__(ROW_THREADS)
             } else {
                 cp_async_wait<0>();
             }
-            const uint4 *const mine = row_stage + (pass & 1) * (KB + 1) * ROW_THREADS + threadIdx.x;
+            const uint4 *const mine = row_stage + (pass & 1) * (SB + 1) * ROW_THREADS + threadIdx.x;
             float gf[8];
-            unpack(mine[KB * ROW_THREADS], gf);
+            unpack(mine[SB * ROW_THREADS], gf);
 #pragma unroll
-            for (int i = 0; i < KB; ++i) {
+            for (int i = 0; i < SB; ++i) {
                 if (rk[i] < 0) continue;
                 float rf[8], o[8];
                 unpack(mine[i * ROW_THREADS], rf);
@@ -452,24 +458,24 @@ __global__ void __launch_bounds__(ROW_THREADS)
     // Each slot's partial reduced over the token's threads, as in k_unpermute_bwd.
     const int width = tpt < 32 ? tpt : 32;
 #pragma unroll
-    for (int i = 0; i < KB; ++i)
+    for (int i = 0; i < SB; ++i)
         for (int o = width >> 1; o > 0; o >>= 1) dot[i] += __shfl_xor_sync(FULL_MASK, dot[i], o);
     if (tpt > 32) {
         const int warp = threadIdx.x >> 5;
         if ((threadIdx.x & 31) == 0)
 #pragma unroll
-            for (int i = 0; i < KB; ++i) s_red[warp][i] = dot[i];
+            for (int i = 0; i < SB; ++i) s_red[warp][i] = dot[i];
         __syncthreads();
         if (active && lane == 0) {
             const int w0 = warp, nw = tpt >> 5;
-            for (int i = 0; i < KB && i < K; ++i) {
+            for (int i = 0; i < SB && i < K; ++i) {
                 float s = 0.0f;
                 for (int w = 0; w < nw; ++w) s += s_red[w0 + w][i];
                 g_probs[t * K + i] = rk[i] >= 0 ? s : 0.0f;
             }
         }
     } else if (active && lane == 0) {
-        for (int i = 0; i < KB && i < K; ++i) g_probs[t * K + i] = rk[i] >= 0 ? dot[i] : 0.0f;
+        for (int i = 0; i < SB && i < K; ++i) g_probs[t * K + i] = rk[i] >= 0 ? dot[i] : 0.0f;
     }
 }
 
@@ -523,6 +529,37 @@ inline void launch_permute_vec(const void *x, const float *probs, const int32_t 
         launch_permute<uint4, PERMUTE_VPT>(x, probs, map, T, K, nvec, out, out_probs, s);
 }
 
+template <int SB>
+void launch_unpermute_st(const RowGrid &g, const void *rows, const float *probs,
+                         const int32_t *map, int64_t T, int K, int nvec, void *out,
+                         const float *g_out_probs, float *g_probs, cudaStream_t s)
+{
+    const size_t smem = (size_t)STAGE_BUFS * SB * ROW_THREADS * sizeof(uint4);
+    if (probs != nullptr)
+        (void)launch_pdl(k_unpermute_staged<true, false, SB>, g.blocks, ROW_THREADS, smem, s,
+            (const uint4 *)rows, probs, map, T, K, nvec, g.tpt_log2, (uint4 *)out,
+            nullptr, nullptr);
+    else if (g_probs != nullptr)
+        (void)launch_pdl(k_unpermute_staged<false, true, SB>, g.blocks, ROW_THREADS, smem, s,
+            (const uint4 *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (uint4 *)out,
+            g_out_probs, g_probs);
+    else
+        (void)launch_pdl(k_unpermute_staged<false, false, SB>, g.blocks, ROW_THREADS, smem,
+            s, (const uint4 *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (uint4 *)out,
+            nullptr, nullptr);
+}
+
+template <int SB>
+void launch_unpermute_bwd_st(const RowGrid &g, const void *gy, const void *rows,
+                             const float *probs, const int32_t *map, int64_t T, int K,
+                             int nvec, void *g_rows, float *g_probs, cudaStream_t s)
+{
+    const size_t smem = (size_t)STAGE_BUFS * (SB + 1) * ROW_THREADS * sizeof(uint4);
+    (void)launch_pdl(k_unpermute_bwd_staged<SB>, g.blocks, ROW_THREADS, smem, s,
+        (const uint4 *)gy, (const uint4 *)rows, probs, map, T, K, nvec, g.tpt_log2,
+        (uint4 *)g_rows, g_probs);
+}
+
 template <typename V, int VPT, int SB>
 void launch_unpermute_reg(const RowGrid &g, const void *rows, const float *probs,
                           const int32_t *map, int64_t T, int K, int nvec, void *out,
@@ -548,19 +585,18 @@ void launch_unpermute(const void *rows, const float *probs, const int32_t *map, 
     const RowGrid g = row_grid(T, nvec, VPT);
     if constexpr (Lanes<V>::N == 8 && VPT == 1) {
         if (K <= KB && g.blocks >= STAGE_MIN_BLOCKS) {
-            const size_t smem = (size_t)STAGE_BUFS * KB * ROW_THREADS * sizeof(uint4);
-            if (probs != nullptr)
-                (void)launch_pdl(k_unpermute_staged<true, false>, g.blocks, ROW_THREADS, smem, s,
-                    (const uint4 *)rows, probs, map, T, K, nvec, g.tpt_log2, (uint4 *)out,
-                    nullptr, nullptr);
-            else if (g_probs != nullptr)
-                (void)launch_pdl(k_unpermute_staged<false, true>, g.blocks, ROW_THREADS, smem, s,
-                    (const uint4 *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (uint4 *)out,
-                    g_out_probs, g_probs);
+            if (K <= 2)
+                launch_unpermute_st<2>(g, rows, probs, map, T, K, nvec, out, g_out_probs,
+                                       g_probs, s);
+            else if (K <= 4)
+                launch_unpermute_st<4>(g, rows, probs, map, T, K, nvec, out, g_out_probs,
+                                       g_probs, s);
+            else if (K <= KB_SMALL)
+                launch_unpermute_st<KB_SMALL>(g, rows, probs, map, T, K, nvec, out, g_out_probs,
+                                              g_probs, s);
             else
-                (void)launch_pdl(k_unpermute_staged<false, false>, g.blocks, ROW_THREADS, smem,
-                    s, (const uint4 *)rows, nullptr, map, T, K, nvec, g.tpt_log2, (uint4 *)out,
-                    nullptr, nullptr);
+                launch_unpermute_st<KB>(g, rows, probs, map, T, K, nvec, out, g_out_probs,
+                                        g_probs, s);
             return;
         }
     }
@@ -586,10 +622,18 @@ void launch_unpermute_bwd(const void *gy, const void *rows, const float *probs,
     const RowGrid g = row_grid(T, nvec, VPT);
     if constexpr (Lanes<V>::N == 8 && VPT == 1) {
         if (K <= KB && g.blocks >= STAGE_MIN_BLOCKS_BWD) {
-            const size_t smem = (size_t)STAGE_BUFS * (KB + 1) * ROW_THREADS * sizeof(uint4);
-            (void)launch_pdl(k_unpermute_bwd_staged, g.blocks, ROW_THREADS, smem, s,
-                (const uint4 *)gy, (const uint4 *)rows, probs, map, T, K, nvec, g.tpt_log2,
-                (uint4 *)g_rows, g_probs);
+            if (K <= 2)
+                launch_unpermute_bwd_st<2>(g, gy, rows, probs, map, T, K, nvec, g_rows, g_probs,
+                                           s);
+            else if (K <= 4)
+                launch_unpermute_bwd_st<4>(g, gy, rows, probs, map, T, K, nvec, g_rows, g_probs,
+                                           s);
+            else if (K <= KB_SMALL)
+                launch_unpermute_bwd_st<KB_SMALL>(g, gy, rows, probs, map, T, K, nvec, g_rows,
+                                                  g_probs, s);
+            else
+                launch_unpermute_bwd_st<KB>(g, gy, rows, probs, map, T, K, nvec, g_rows, g_probs,
+                                            s);
             return;
         }
     }
