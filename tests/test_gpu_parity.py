@@ -267,7 +267,8 @@ def test_unpermute_ulp_fallback_not_needed():
     assert bf16_ulp_distance(y, o).max() == 0
 
 
-def test_staged_row_kernels_full_compare():
+@pytest.mark.parametrize("K", [8, 5, 3, 2])   # the 8-, 6-, 4- and 2-slot batches
+def test_staged_row_kernels_full_compare(K):
     """16,385 tokens, one per CTA (H = 1,032: 129 vectors, so a second pass
     with one lane busy), make grids past 16,384 CTAs, which run the forms that
     stage their rows in shared memory: unpermute, its backward and the permute
@@ -275,7 +276,7 @@ def test_staged_row_kernels_full_compare():
     with the oracle in full."""
     T, H = 16385, 1032
     idx, probs, E = wl.routing("skewed", T=T)
-    K = idx.shape[1]
+    idx, probs = idx[:, :K].copy(), np.ascontiguousarray(probs[:, :K])
     rng = np.random.default_rng(5)
     idx = idx.copy()
     idx[rng.random(idx.shape) < 0.1] = -1
