@@ -57,18 +57,18 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     -k regex:"^<kernel>$" -s <n> -c 1 python bench.py --workload <w> --steps 3
     #     --warmup 3 --no-cpu --no-chunks --no-extras   (one pass per launch)
-    ("permute", "mid", 4096): {"bytes": 16991744 + 39191296, "src": "df7ab508c8f22d57"},
-    ("unpermute", "mid", 4096): {"bytes": 100872448 + 4431360, "src": "df7ab508c8f22d57"},
-    ("unpermute_bwd", "mid", 4096): {"bytes": 117661696 + 43040768, "src": "df7ab508c8f22d57"},
-    ("permute_bwd", "mid", 4096): {"bytes": 100773376 + 3946496, "src": "df7ab508c8f22d57"},
-    ("permute", "skewed", 16384): {"bytes": 135343616 + 1013358080, "src": "df7ab508c8f22d57"},
-    ("unpermute", "skewed", 16384): {"bytes": 1074822400 + 124493824, "src": "df7ab508c8f22d57"},
-    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209082624 + 1021869568, "src": "df7ab508c8f22d57"},
-    ("permute_bwd", "skewed", 16384): {"bytes": 1074288128 + 124353024, "src": "df7ab508c8f22d57"},
-    ("permute", "large", 32768): {"bytes": 472726784 + 3698916096, "src": "df7ab508c8f22d57"},
-    ("unpermute", "large", 32768): {"bytes": 3760239360 + 459858688, "src": "df7ab508c8f22d57"},
-    ("unpermute_bwd", "large", 32768): {"bytes": 4230139904 + 3709153280, "src": "df7ab508c8f22d57"},
-    ("permute_bwd", "large", 32768): {"bytes": 3759262208 + 459578880, "src": "df7ab508c8f22d57"},
+    ("permute", "mid", 4096): {"bytes": 16996096 + 39769856, "src": "7a9d586390032011"},
+    ("unpermute", "mid", 4096): {"bytes": 100872960 + 4067840, "src": "7a9d586390032011"},
+    ("unpermute_bwd", "mid", 4096): {"bytes": 117661696 + 42933760, "src": "7a9d586390032011"},
+    ("permute_bwd", "mid", 4096): {"bytes": 100772864 + 4005120, "src": "7a9d586390032011"},
+    ("permute", "skewed", 16384): {"bytes": 135343616 + 1013276416, "src": "7a9d586390032011"},
+    ("unpermute", "skewed", 16384): {"bytes": 1074813184 + 124578048, "src": "7a9d586390032011"},
+    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209063168 + 1021812224, "src": "7a9d586390032011"},
+    ("permute_bwd", "skewed", 16384): {"bytes": 1074286336 + 124214528, "src": "7a9d586390032011"},
+    ("permute", "large", 32768): {"bytes": 472344576 + 3699003392, "src": "7a9d586390032011"},
+    ("unpermute", "large", 32768): {"bytes": 3760239616 + 459824128, "src": "7a9d586390032011"},
+    ("unpermute_bwd", "large", 32768): {"bytes": 4230116352 + 3708436992, "src": "7a9d586390032011"},
+    ("permute_bwd", "large", 32768): {"bytes": 3759188224 + 459731968, "src": "7a9d586390032011"},
 }
 
 
