@@ -51,24 +51,25 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture of one launch of that kernel alone, keyed by (op, workload,
-# T); a figure counts only while the profiled kernel source is unchanged
-# (sha256 prefix of its .cu file and common.cuh).  No matching capture: null.
+# T); a figure counts only while the profiled kernel code is unchanged
+# (sha256 prefix of its .cu file and common.cuh, comments left out).  No
+# matching capture: null.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     -k regex:"^<kernel>$" -s <n> -c 1 python bench.py --workload <w> --steps 3
     #     --warmup 3 --no-cpu --no-chunks --no-extras   (one pass per launch)
-    ("permute", "mid", 4096): {"bytes": 16996096 + 39769856, "src": "7a9d586390032011"},
-    ("unpermute", "mid", 4096): {"bytes": 100872960 + 4067840, "src": "7a9d586390032011"},
-    ("unpermute_bwd", "mid", 4096): {"bytes": 117661696 + 42933760, "src": "7a9d586390032011"},
-    ("permute_bwd", "mid", 4096): {"bytes": 100772864 + 4005120, "src": "7a9d586390032011"},
-    ("permute", "skewed", 16384): {"bytes": 135343616 + 1013276416, "src": "7a9d586390032011"},
-    ("unpermute", "skewed", 16384): {"bytes": 1074813184 + 124578048, "src": "7a9d586390032011"},
-    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209063168 + 1021812224, "src": "7a9d586390032011"},
-    ("permute_bwd", "skewed", 16384): {"bytes": 1074286336 + 124214528, "src": "7a9d586390032011"},
-    ("permute", "large", 32768): {"bytes": 472344576 + 3699003392, "src": "7a9d586390032011"},
-    ("unpermute", "large", 32768): {"bytes": 3760239616 + 459824128, "src": "7a9d586390032011"},
-    ("unpermute_bwd", "large", 32768): {"bytes": 4230116352 + 3708436992, "src": "7a9d586390032011"},
-    ("permute_bwd", "large", 32768): {"bytes": 3759188224 + 459731968, "src": "7a9d586390032011"},
+    ("permute", "mid", 4096): {"bytes": 16996096 + 39769856, "src": "b9743c693b5060ce"},
+    ("unpermute", "mid", 4096): {"bytes": 100872960 + 4067840, "src": "b9743c693b5060ce"},
+    ("unpermute_bwd", "mid", 4096): {"bytes": 117661696 + 42933760, "src": "b9743c693b5060ce"},
+    ("permute_bwd", "mid", 4096): {"bytes": 100772864 + 4005120, "src": "b9743c693b5060ce"},
+    ("permute", "skewed", 16384): {"bytes": 135343616 + 1013276416, "src": "b9743c693b5060ce"},
+    ("unpermute", "skewed", 16384): {"bytes": 1074813184 + 124578048, "src": "b9743c693b5060ce"},
+    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209063168 + 1021812224, "src": "b9743c693b5060ce"},
+    ("permute_bwd", "skewed", 16384): {"bytes": 1074286336 + 124214528, "src": "b9743c693b5060ce"},
+    ("permute", "large", 32768): {"bytes": 472344576 + 3699003392, "src": "b9743c693b5060ce"},
+    ("unpermute", "large", 32768): {"bytes": 3760239616 + 459824128, "src": "b9743c693b5060ce"},
+    ("unpermute_bwd", "large", 32768): {"bytes": 4230116352 + 3708436992, "src": "b9743c693b5060ce"},
+    ("permute_bwd", "large", 32768): {"bytes": 3759188224 + 459731968, "src": "b9743c693b5060ce"},
 }
 
 
@@ -133,12 +134,23 @@ def ncu_traffic(op, workload, T):
     return tr["bytes"] if tr is not None and tr["src"] == src_hash(src) else None
 
 
+def code_only(text):
+    """C++ source without its comments and blank lines (a comment-only edit
+    leaves the compiled kernels, and so their profiled traffic, unchanged)."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def src_hash(name):
-    """Hash of a kernel's source file and the device helpers it includes."""
+    """Hash of the code of a kernel's source file and of the device helpers
+    it includes, comments left out."""
     h = hashlib.sha256()
     for part in (name, "common.cuh"):
-        with open(os.path.join(ROOT, "unpermute_routing_indices_gb300", "csrc", part), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "unpermute_routing_indices_gb300", "csrc", part)) as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

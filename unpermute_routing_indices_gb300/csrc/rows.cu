@@ -39,22 +39,24 @@ namespace {
 
 constexpr int ROW_THREADS = MP_ROW_THREADS;
 constexpr int KB = MP_SLOT_BATCH;  // slots whose rows are in flight together
-// The gathers and the backward, register and staged forms, are also
-// compiled for batches of 2, 4 and KB_SMALL slots, which tokens of at most
-// that many slots take: the registers (and, staged, the shared memory) of the
-// unused slots of a KB batch cost resident CTAs.  K = 2, 8,192 tokens of
-// 4,096 (register forms): fwd+bwd step 165.7 -> 148.7 us; 4,096 tokens of
-// 2,048: 52.3 -> 44.0; K = 4: 253.7 -> 250.8 and 64.2 -> 60.8.  Staged
-// forms, K = 2, 16,384 / 32,768 tokens of 4,096: 328.2 / 632.0 -> 283.3 /
-// 547.7 us; K = 4, 32,768 tokens of 2,048: 519.1 -> 479.1.  On 16-byte vectors
-// that backward is compiled for 8 CTAs per SM (64 registers, no spills; the
-// KB form for 5, which it reaches at 92 to 94).  Measured on the T=4,096,
-// H=2,048, K=6 fwd+bwd step: 95.2 -> 86.6 us with 6 CTAs per SM
-// (unpermute_bwd 41.0 -> 36.8 us, unpermute 23.1 -> 22.2), 84.8 us with 8
-// (unpermute_bwd 34.7 us; 7: 84.7 / 34.9); either change alone: 98.4 (slot
-// batch, whose backward then took more registers) and 92.9 us (a cap of 6).
-// A cap of 6 on the KB form (K = 8) made the skewed T=2,048 step slower
-// (115.7 -> 117.9 us).
+// Slot batches.  The gathers and the backward, register and staged forms,
+// are compiled for batches of 2, 4, KB_SMALL and KB slots, and a token of K
+// slots takes the smallest batch that holds it (K > KB: batches of KB, in the
+// register forms only).  The registers, and in the staged forms the shared
+// memory, of a batch's unused slots would cost resident CTAs.  Fwd+bwd
+// steps, K = 2: 8,192 tokens of 4,096 (register forms) 165.7 -> 148.7 us;
+// 4,096 tokens of 2,048: 52.3 -> 44.0; 16,384 / 32,768 tokens of 4,096
+// (staged) 328.2 / 632.0 -> 283.3 / 547.7.  K = 4: 253.7 -> 250.8, 64.2 ->
+// 60.8; 32,768 tokens of 2,048 (staged) 519.1 -> 479.1.
+//
+// The register-form backward on 16-byte vectors is compiled for 8 CTAs per
+// SM with batches of up to KB_SMALL slots (64 registers, no spills) and for
+// 5 with KB (92 to 94 registers).  On the T=4,096, H=2,048, K=6 fwd+bwd step:
+// 95.2 -> 86.6 us with 6 CTAs per SM (unpermute_bwd 41.0 -> 36.8 us,
+// unpermute 23.1 -> 22.2), 84.8 us with 8 (unpermute_bwd 34.7 us; 7 CTAs:
+// 84.7 / 34.9); the 6-slot batch alone 98.4 (its backward then took more
+// registers), the cap of 6 alone 92.9.  A cap of 6 on the KB form (K = 8)
+// made the skewed T=2,048 step slower (115.7 -> 117.9 us).
 constexpr int KB_SMALL = 6;
 // CTAs per SM the register-form backward is compiled for, by vector type
 // (16-byte vectors or single elements) and slot batch.
