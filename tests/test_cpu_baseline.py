@@ -107,3 +107,12 @@ def test_reference_arm_prints_the_contract_line():
     assert line["metric"] == bench.METRIC and line["unit"] == "GB/s"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+
+
+def test_traffic_source_check_ignores_comments_only():
+    """The DRAM-traffic figures are keyed to the kernel code: a comment or
+    blank-line edit keeps the key, a code edit changes it."""
+    src = "int a = 1;  // one\n/* block\n   comment */\n\nint b = a + 2;\n"
+    assert bench.code_only(src) == "int a = 1;\nint b = a + 2;"
+    assert bench.code_only(src.replace("// one", "// two")) == bench.code_only(src)
+    assert bench.code_only(src.replace("a + 2", "a + 3")) != bench.code_only(src)
