@@ -74,6 +74,22 @@ def test_routed_ops_across_slot_batches(K, H):
     _check_routed(rng, T, K, E, H, idx, probs, x, rows, gy, 0)
 
 
+# The permute's vector widths on wide rows: 32-byte vectors (H = 4,096 from a
+# 32-byte aligned base), 16-byte ones when the base is only 16-byte aligned
+# (offset by 8 elements) or the vector count is odd (H = 4,104)
+@pytest.mark.parametrize("H,off", [(4096, 0), (4096, 8), (4104, 0), (7168, 0)])
+def test_routed_ops_wide_rows_vector_widths(H, off):
+    rng = np.random.default_rng(H + off)
+    T, K, E = 200, 8, 128
+    idx = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    idx[rng.random((T, K)) < 0.1] = -1
+    probs = rng.random((T, K)).astype(np.float32) + np.float32(1e-3)
+    x = wl.random_rows(T, H, 11)
+    rows = wl.random_rows(T * K, H, 12)
+    gy = wl.random_rows(T, H, 13)
+    _check_routed(rng, T, K, E, H, idx, probs, x, rows, gy, off)
+
+
 def _check_routed(rng, T, K, E, H, idx, probs, x, rows, gy, off):
     o_rim, o_s2f, o_counts, o_offsets, _ = oracle.build_map(idx, E)
     rim, s2f, counts, offsets = mp.mp_build_map(d(idx), E)

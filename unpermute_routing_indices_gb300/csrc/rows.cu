@@ -18,6 +18,35 @@
 #include "common.cuh"
 
 namespace mp {
+
+// 32-byte vectors (256-bit loads and stores, sm_100 and later) for the
+// permute's row copy on wide rows; the ld / st / zero helpers of uint4 and
+// uint16_t are in common.cuh.
+struct alignas(32) u32x8 {
+    uint4 a, b;
+};
+__device__ __forceinline__ u32x8 ld_stream(const u32x8 *p)
+{
+    u32x8 v;
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(v.a.x), "=r"(v.a.y), "=r"(v.a.z), "=r"(v.a.w), "=r"(v.b.x), "=r"(v.b.y),
+          "=r"(v.b.z), "=r"(v.b.w)
+        : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_row(u32x8 *p, const u32x8 &v)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"l"(p), "r"(v.a.x), "r"(v.a.y), "r"(v.a.z), "r"(v.a.w), "r"(v.b.x),
+                   "r"(v.b.y), "r"(v.b.z), "r"(v.b.w)
+                 : "memory");
+}
+template <> __device__ __forceinline__ u32x8 zero_vec<u32x8>()
+{
+    return u32x8{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+}
+inline bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
 namespace {
 
 // Launch shape (overridable at build time for tuning sweeps).
@@ -502,7 +531,12 @@ constexpr int PERMUTE_VPT = MP_PERMUTE_VPT;
 // vectors per thread, so that a token is one pass of a whole 128-thread CTA
 // rather than half a CTA: the T=4,096, H=2,048, K=6 fwd+bwd step 97.5 ->
 // 95.2 us.  With H=4,096 or 7,168 four per thread stay faster (two per
-// thread: T=16,384 step 868 -> 872 us).
+// thread: T=16,384 step 868 -> 872 us).  Wider rows (more than 256
+// vectors), 32-byte aligned with an even vector count, move as 32-byte
+// vectors, four per thread: half the load and store instructions
+// (permute on the skewed T=16,384 batch 180.3 -> 179.2 us, the large
+// T=8,192 step 790.4 -> 783.7 us; on 2,048-element rows they were slower,
+// 84.3 -> 86.1 us for the mid step).
 constexpr int UNPERMUTE_VPT = MP_UNPERMUTE_VPT;
 constexpr int BWD_VPT = MP_BWD_VPT;
 constexpr int ELEM_VPT = 8;
@@ -525,6 +559,10 @@ inline void launch_permute_vec(const void *x, const float *probs, const int32_t 
                                int64_t T, int K, int nvec, void *out, float *out_probs,
                                cudaStream_t s)
 {
+    if (nvec > 2 * ROW_THREADS && nvec % 2 == 0 && aligned32(x) && aligned32(out)) {
+        launch_permute<u32x8, PERMUTE_VPT>(x, probs, map, T, K, nvec / 2, out, out_probs, s);
+        return;
+    }
     if (nvec > ROW_THREADS && nvec <= 2 * ROW_THREADS)
         launch_permute<uint4, MP_PERMUTE_VPT_MID>(x, probs, map, T, K, nvec, out, out_probs, s);
     else
