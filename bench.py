@@ -58,18 +58,18 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     -k regex:"^<kernel>$" -s <n> -c 1 python bench.py --workload <w> --steps 3
     #     --warmup 3 --no-cpu --no-chunks --no-extras   (one pass per launch)
-    ("permute", "mid", 4096): {"bytes": 16996096 + 39769856, "src": "b9743c693b5060ce"},
-    ("unpermute", "mid", 4096): {"bytes": 100872960 + 4067840, "src": "b9743c693b5060ce"},
-    ("unpermute_bwd", "mid", 4096): {"bytes": 117661696 + 42933760, "src": "b9743c693b5060ce"},
-    ("permute_bwd", "mid", 4096): {"bytes": 100772864 + 4005120, "src": "b9743c693b5060ce"},
-    ("permute", "skewed", 16384): {"bytes": 135343616 + 1013276416, "src": "b9743c693b5060ce"},
-    ("unpermute", "skewed", 16384): {"bytes": 1074813184 + 124578048, "src": "b9743c693b5060ce"},
-    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209063168 + 1021812224, "src": "b9743c693b5060ce"},
-    ("permute_bwd", "skewed", 16384): {"bytes": 1074286336 + 124214528, "src": "b9743c693b5060ce"},
-    ("permute", "large", 32768): {"bytes": 472344576 + 3699003392, "src": "b9743c693b5060ce"},
-    ("unpermute", "large", 32768): {"bytes": 3760239616 + 459824128, "src": "b9743c693b5060ce"},
-    ("unpermute_bwd", "large", 32768): {"bytes": 4230116352 + 3708436992, "src": "b9743c693b5060ce"},
-    ("permute_bwd", "large", 32768): {"bytes": 3759188224 + 459731968, "src": "b9743c693b5060ce"},
+    ("permute", "mid", 4096): {"bytes": 16988928 + 39224064, "src": "273e278c5dfd5c1a"},
+    ("unpermute", "mid", 4096): {"bytes": 100871424 + 4141568, "src": "273e278c5dfd5c1a"},
+    ("unpermute_bwd", "mid", 4096): {"bytes": 117661440 + 43231488, "src": "273e278c5dfd5c1a"},
+    ("permute_bwd", "mid", 4096): {"bytes": 100771328 + 4138496, "src": "273e278c5dfd5c1a"},
+    ("permute", "skewed", 16384): {"bytes": 135352576 + 1012453888, "src": "273e278c5dfd5c1a"},
+    ("unpermute", "skewed", 16384): {"bytes": 1074831104 + 124492544, "src": "273e278c5dfd5c1a"},
+    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209064704 + 1022038272, "src": "273e278c5dfd5c1a"},
+    ("permute_bwd", "skewed", 16384): {"bytes": 1074291712 + 124587776, "src": "273e278c5dfd5c1a"},
+    ("permute", "large", 32768): {"bytes": 472448512 + 3697826304, "src": "273e278c5dfd5c1a"},
+    ("unpermute", "large", 32768): {"bytes": 3760582144 + 459815424, "src": "273e278c5dfd5c1a"},
+    ("unpermute_bwd", "large", 32768): {"bytes": 4230062848 + 3708630528, "src": "273e278c5dfd5c1a"},
+    ("permute_bwd", "large", 32768): {"bytes": 3759234560 + 459634176, "src": "273e278c5dfd5c1a"},
 }
 
 
