@@ -121,6 +121,33 @@ def test_sort_pad_many_chunks_large_output():
     np.testing.assert_array_equal(h(y_p), probs)
 
 
+@pytest.mark.parametrize("H,shift", [(512, 0), (512, 8), (520, 0)])
+def test_sort_pad_large_output_vector_widths(H, shift):
+    """Outputs of more than 16,384 rows copy 32-byte vectors when the tensors
+    start on 32-byte boundaries and a row is an even number of 16-byte
+    vectors (H = 512), else 16-byte ones: a base 8 elements (16 bytes) past
+    the boundary, or rows of 65 16-byte vectors (H = 520)."""
+    G, R, align = 16, 8, 8
+    sizes, order = _meta(77 + H + shift, G, R, max_size=400)
+    N = int(sizes.sum())
+    out_rows = N + G * (align - 1) + 5
+    assert out_rows > 16384
+    x = wl.random_rows(N, H, 6)
+    probs = np.random.default_rng(7).random(N).astype(np.float32)
+    xb = torch.empty(N * H + shift, dtype=torch.bfloat16, device=DEV)
+    dx = xb[shift:].view(N, H)
+    dx.copy_(d(x))
+    ob = torch.empty(out_rows * H + shift, dtype=torch.bfloat16, device=DEV)
+    dout = ob[shift:].view(out_rows, H)
+    out, out_p, row_map, _ = mp.mp_sort_chunks_pad(dx, d(sizes), d(order), G, align, out_rows,
+                                                   d(probs), out=dout)
+    o_out, o_out_p, o_map, _, _ = oracle.sort_chunks_pad(x, probs, sizes, order, G, align,
+                                                         out_rows)
+    np.testing.assert_array_equal(h(row_map), o_map)
+    np.testing.assert_array_equal(h(out), o_out)
+    np.testing.assert_array_equal(h(out_p), o_out_p)
+
+
 def test_sort_pad_status_bits():
     x = wl.random_rows(64, 16, 5)
     p = np.arange(64, dtype=np.float32)

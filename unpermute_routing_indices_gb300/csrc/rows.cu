@@ -19,34 +19,6 @@
 
 namespace mp {
 
-// 32-byte vectors (256-bit loads and stores, sm_100 and later) for the
-// permute's row copy on wide rows; the ld / st / zero helpers of uint4 and
-// uint16_t are in common.cuh.
-struct alignas(32) u32x8 {
-    uint4 a, b;
-};
-__device__ __forceinline__ u32x8 ld_stream(const u32x8 *p)
-{
-    u32x8 v;
-    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-        : "=r"(v.a.x), "=r"(v.a.y), "=r"(v.a.z), "=r"(v.a.w), "=r"(v.b.x), "=r"(v.b.y),
-          "=r"(v.b.z), "=r"(v.b.w)
-        : "l"(p));
-    return v;
-}
-__device__ __forceinline__ void st_row(u32x8 *p, const u32x8 &v)
-{
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-                 ::"l"(p), "r"(v.a.x), "r"(v.a.y), "r"(v.a.z), "r"(v.a.w), "r"(v.b.x),
-                   "r"(v.b.y), "r"(v.b.z), "r"(v.b.w)
-                 : "memory");
-}
-template <> __device__ __forceinline__ u32x8 zero_vec<u32x8>()
-{
-    return u32x8{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-}
-inline bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
-
 namespace {
 
 // Launch shape (overridable at build time for tuning sweeps).
