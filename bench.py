@@ -58,18 +58,18 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     -k regex:"^<kernel>$" -s <n> -c 1 python bench.py --workload <w> --steps 3
     #     --warmup 3 --no-cpu --no-chunks --no-extras   (one pass per launch)
-    ("permute", "mid", 4096): {"bytes": 16988928 + 39224064, "src": "273e278c5dfd5c1a"},
-    ("unpermute", "mid", 4096): {"bytes": 100871424 + 4141568, "src": "273e278c5dfd5c1a"},
-    ("unpermute_bwd", "mid", 4096): {"bytes": 117661440 + 43231488, "src": "273e278c5dfd5c1a"},
-    ("permute_bwd", "mid", 4096): {"bytes": 100771328 + 4138496, "src": "273e278c5dfd5c1a"},
-    ("permute", "skewed", 16384): {"bytes": 135352576 + 1012453888, "src": "273e278c5dfd5c1a"},
-    ("unpermute", "skewed", 16384): {"bytes": 1074831104 + 124492544, "src": "273e278c5dfd5c1a"},
-    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209064704 + 1022038272, "src": "273e278c5dfd5c1a"},
-    ("permute_bwd", "skewed", 16384): {"bytes": 1074291712 + 124587776, "src": "273e278c5dfd5c1a"},
-    ("permute", "large", 32768): {"bytes": 472448512 + 3697826304, "src": "273e278c5dfd5c1a"},
-    ("unpermute", "large", 32768): {"bytes": 3760582144 + 459815424, "src": "273e278c5dfd5c1a"},
-    ("unpermute_bwd", "large", 32768): {"bytes": 4230062848 + 3708630528, "src": "273e278c5dfd5c1a"},
-    ("permute_bwd", "large", 32768): {"bytes": 3759234560 + 459634176, "src": "273e278c5dfd5c1a"},
+    ("permute", "mid", 4096): {"bytes": 16990976 + 39353088, "src": "4de68a6e1acd2556"},
+    ("unpermute", "mid", 4096): {"bytes": 100872960 + 4466432, "src": "4de68a6e1acd2556"},
+    ("unpermute_bwd", "mid", 4096): {"bytes": 117673984 + 43074560, "src": "4de68a6e1acd2556"},
+    ("permute_bwd", "mid", 4096): {"bytes": 100771840 + 3934720, "src": "4de68a6e1acd2556"},
+    ("permute", "skewed", 16384): {"bytes": 135397888 + 1012604928, "src": "4de68a6e1acd2556"},
+    ("unpermute", "skewed", 16384): {"bytes": 1074866944 + 124409344, "src": "4de68a6e1acd2556"},
+    ("unpermute_bwd", "skewed", 16384): {"bytes": 1209062400 + 1021680640, "src": "4de68a6e1acd2556"},
+    ("permute_bwd", "skewed", 16384): {"bytes": 1074287360 + 124515328, "src": "4de68a6e1acd2556"},
+    ("permute", "large", 32768): {"bytes": 472453632 + 3697769216, "src": "4de68a6e1acd2556"},
+    ("unpermute", "large", 32768): {"bytes": 3760299008 + 459797760, "src": "4de68a6e1acd2556"},
+    ("unpermute_bwd", "large", 32768): {"bytes": 4230063616 + 3708089600, "src": "4de68a6e1acd2556"},
+    ("permute_bwd", "large", 32768): {"bytes": 3759203328 + 459230720, "src": "4de68a6e1acd2556"},
 }
 
 
