@@ -34,10 +34,11 @@
  *  - Tensors are dense and row-major.  bf16 tensors are passed as their
  *    16-bit patterns (mp_bf16_t).  A row of H bf16 values is 2*H bytes.
  *    Rows move as 16-byte vectors when H % 8 == 0 and every row pointer is
- *    16-byte aligned, else element by element; the permute on rows of more
- *    than 2,048 bf16 and the sort+pad on outputs of more than 16,384 rows
- *    move 32-byte vectors when H % 16 == 0 and the tensors are 32-byte
- *    aligned.  Results are identical on every path.
+ *    16-byte aligned, else element by element.  The permute on rows of more
+ *    than 4 KiB and the sort+pad on outputs of more than 16,384 rows of at
+ *    least 1 KiB move 32-byte vectors when the row size is a multiple of 32
+ *    bytes and the tensors are 32-byte aligned.  Results are identical on
+ *    every path.
  *  - Routes: T tokens, K slots per token, R = T*K <= 2^31 - 1.
  *    E <= MP_MAX_EXPERTS.
  *  - Errors found on the host (a NULL required pointer, a negative or
