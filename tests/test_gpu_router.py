@@ -51,6 +51,9 @@ def _check_probs(got, want):
     (900, 128, 4, 2, 1, "ties"),        # s = 2, 4 slots per lane
     (700, 1024, 16, 4, 3, "skew"),      # s = 8, 32 slots per lane (the rescan path)
     (500, 8, 8, 1, 1, "normal"),        # K = E
+    # the K = 8 forms (unrolled rounds) on ties, ungrouped and grouped
+    (2000, 128, 8, 1, 1, "ties"),
+    (1500, 256, 8, 4, 2, "ties"),
 ])
 def test_topk_softmax_parity(T, E, K, G, TG, kind):
     logits = _logits(T, E, T + E, ties=(kind == "ties"), skew=(kind == "skew"))
